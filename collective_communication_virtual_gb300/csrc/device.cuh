@@ -1,0 +1,210 @@
+// device.cuh -- element reductions and memory helpers shared by the kernels.
+//
+// Element semantics (the communicator-wide reading of the reductions):
+//  * fp32 sum/prod: one IEEE binary32 op, round to nearest even (__fadd_rn/__fmul_rn,
+//    which the compiler never contracts into an FMA);
+//  * fp16/bf16 sum/prod: widen both operands to fp32 (exact), one fp32 op (RNE), round
+//    to the storage type (RNE) -- every ring hop stores its partial in that type;
+//  * int32 sum/prod: wrap modulo 2^32;
+//  * min/max: the running partial a is kept unless the incoming b compares strictly
+//    below / above it (compared as fp32 for 16-bit floats); the selected element keeps
+//    its bits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace vc {
+
+enum { kSum = 0, kProd = 1, kMin = 2, kMax = 3 };
+enum { kF32 = 0, kF16 = 1, kBF16 = 2, kI32 = 3 };
+
+template <int DT> struct DTypeOf;
+template <> struct DTypeOf<kF32> { using T = float; static constexpr int size = 4; };
+template <> struct DTypeOf<kF16> { using T = __half; static constexpr int size = 2; };
+template <> struct DTypeOf<kBF16> { using T = __nv_bfloat16; static constexpr int size = 2; };
+template <> struct DTypeOf<kI32> { using T = int32_t; static constexpr int size = 4; };
+
+// ---- one element, on raw bits --------------------------------------------------------
+
+template <int OP>
+__device__ __forceinline__ float op_f32(float a, float b) {
+    if (OP == kSum) return __fadd_rn(a, b);
+    if (OP == kProd) return __fmul_rn(a, b);
+    if (OP == kMin) return (b < a) ? b : a;
+    return (b > a) ? b : a;
+}
+
+template <int OP>
+__device__ __forceinline__ uint32_t op_i32(uint32_t a, uint32_t b) {
+    if (OP == kSum) return a + b;
+    if (OP == kProd) return a * b;
+    if (OP == kMin) return ((int32_t)b < (int32_t)a) ? b : a;
+    return ((int32_t)b > (int32_t)a) ? b : a;
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+    return __uint_as_float((uint32_t)h << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+    return __half_as_ushort(__float2half_rn(f));
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <int DT>
+__device__ __forceinline__ float widen16(uint16_t h) {
+    return DT == kF16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h);
+}
+template <int DT>
+__device__ __forceinline__ uint16_t narrow16(float f) {
+    return DT == kF16 ? f32_to_f16_bits(f) : f32_to_bf16_bits(f);
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint16_t op_16(uint16_t a, uint16_t b) {
+    const float fa = widen16<DT>(a), fb = widen16<DT>(b);
+    if (OP == kSum) return narrow16<DT>(__fadd_rn(fa, fb));
+    if (OP == kProd) return narrow16<DT>(__fmul_rn(fa, fb));
+    if (OP == kMin) return (fb < fa) ? b : a;
+    return (fb > fa) ? b : a;
+}
+
+// One 32-bit word: one fp32/int32 element or two 16-bit elements.
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t op_word(uint32_t a, uint32_t b) {
+    if (DT == kF32) return __float_as_uint(op_f32<OP>(__uint_as_float(a), __uint_as_float(b)));
+    if (DT == kI32) return op_i32<OP>(a, b);
+    const uint32_t lo = op_16<DT, OP>((uint16_t)(a & 0xFFFFu), (uint16_t)(b & 0xFFFFu));
+    const uint32_t hi = op_16<DT, OP>((uint16_t)(a >> 16), (uint16_t)(b >> 16));
+    return lo | (hi << 16);
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint4 op_vec(uint4 a, uint4 b) {
+    return make_uint4(op_word<DT, OP>(a.x, b.x), op_word<DT, OP>(a.y, b.y),
+                      op_word<DT, OP>(a.z, b.z), op_word<DT, OP>(a.w, b.w));
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint2 op_vec(uint2 a, uint2 b) {
+    return make_uint2(op_word<DT, OP>(a.x, b.x), op_word<DT, OP>(a.y, b.y));
+}
+
+// Element-level op on a value held in the low bits of a u32 (scalar paths).
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t op_elem(uint32_t a, uint32_t b) {
+    if (DT == kF32 || DT == kI32) return op_word<DT, OP>(a, b);
+    return op_16<DT, OP>((uint16_t)a, (uint16_t)b);
+}
+
+// ---- epilogue: out = (float)acc * scale, stored as OUT ------------------------------
+
+template <int DT>
+__device__ __forceinline__ float elem_to_f32(uint32_t v) {
+    if (DT == kF32) return __uint_as_float(v);
+    return widen16<DT>((uint16_t)v);
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t f32_to_elem(float f) {
+    if (OUT == kF32) return __float_as_uint(f);
+    return narrow16<OUT>(f);
+}
+
+// ---- memory ---------------------------------------------------------------------------
+
+// User buffers: streamed once, so keep them out of L1.  Plain (not .nc) loads, so the
+// same code is correct when a receive buffer aliases a send buffer.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Element loads/stores for the scalar paths (esz = 2 or 4).
+template <int ESZ>
+__device__ __forceinline__ uint32_t ld_elem(const void* base, size_t e) {
+    if (ESZ == 4) return *((const uint32_t*)base + e);
+    return *((const uint16_t*)base + e);
+}
+template <int ESZ>
+__device__ __forceinline__ void st_elem(void* base, size_t e, uint32_t v) {
+    if (ESZ == 4) *((uint32_t*)base + e) = v;
+    else *((uint16_t*)base + e) = (uint16_t)v;
+}
+
+// FIFO traffic: L2 only (another SM produced it), and ordered by the protocol's flags.
+__device__ __forceinline__ uint4 ld_cg(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_cg(void* p, uint4 v) {
+    asm volatile("st.global.cg.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void ld_volatile_u64x2(const void* p, unsigned long long& a,
+                                                  unsigned long long& b) {
+    asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_volatile_u64x2(void* p, unsigned long long a,
+                                                  unsigned long long b) {
+    asm volatile("st.volatile.global.v2.u64 [%0], {%1,%2};" :: "l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_volatile_u64(void* p, unsigned long long v) {
+    asm volatile("st.volatile.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(void* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// First error wins (decided by an atomic on the device copy of the status word); the
+// winner mirrors the record into the pinned host copy that vcommGetAsyncError reads.
+__device__ __forceinline__ void report_error(Status* dev, volatile Status* host, unsigned code,
+                                             unsigned ch, unsigned rank, unsigned step) {
+    if (atomicCAS(&dev->code, 0u, code) == 0u) {
+        dev->channel = ch;
+        dev->rank = rank;
+        dev->step = step;
+        if (host) {
+            host->channel = ch;
+            host->rank = rank;
+            host->step = step;
+            __threadfence_system();
+            host->code = code;
+            __threadfence_system();
+        }
+    }
+}
+
+}  // namespace vc

@@ -1,0 +1,107 @@
+// internal.h -- argument blocks and launchers shared by the host side of libvcomm and
+// its kernels.  Not part of the public ABI (that is include/vcomm.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "vcomm.h"
+
+namespace vc {
+
+constexpr int kFifoSlots = 8;        // NCCL_STEPS: slots per (channel, rank) FIFO
+constexpr int kChunkSlots = 4;       // ALLREDUCE_CHUNKSTEPS = NCCL_STEPS / 2
+constexpr int kSliceSlots = 2;       // ALLREDUCE_SLICESTEPS = NCCL_STEPS / 4
+constexpr int kOnePassThreads = 512;
+constexpr int kRingThreads = 512;
+constexpr int kCtrlStride = 32;      // u64 words per (channel, rank) control block (256 B)
+
+// First-error-wins status word.  The device copy decides the winner; a mirror in
+// pinned, device-mapped host memory lets the host read it without synchronizing.
+struct Status {
+    unsigned int code;               // vResult_t, 0 = no error
+    unsigned int channel;
+    unsigned int rank;
+    unsigned int step;               // ring: slot sequence number that gave up
+};
+
+// One-pass kernels: all-reduce, reduce-scatter, all-gather, broadcast, all-to-all.
+struct OnePassArgs {
+    const void* send[VCOMM_MAX_RANKS];
+    void* recv[VCOMM_MAX_RANKS];
+    int nRanks;
+    int ctasPerChannel;
+    int root;                        // broadcast
+    int hasScale;                    // reduce-scatter epilogue
+    float scale;
+    size_t count;                    // AR: count; RS: N*recvcount; AG: sendcount; BC: count; A2A: block
+    size_t blockElems;               // B
+    size_t chanElems;                // elements of each block owned by one channel
+};
+
+struct A2AvArgs {
+    const void* send[VCOMM_MAX_RANKS];
+    void* recv[VCOMM_MAX_RANKS];
+    const int32_t* counts;           // [sender * N + receiver]
+    const int32_t* sdispls;          // [sender * N + receiver]
+    const int32_t* rdispls;          // [receiver * N + sender]
+    int nRanks;
+    int elemSize;
+    size_t tileBytes;
+    Status* status;                  // device copy
+    volatile Status* statusHost;     // pinned mirror
+};
+
+// Staged ring kernels: one CTA per (channel, rank).
+struct RingArgs {
+    const void* send[VCOMM_MAX_RANKS];
+    void* recv[VCOMM_MAX_RANKS];
+    int nRanks;
+    int nChannels;
+    int coll;                        // vColl_t: AR, RS, AG or BC
+    int op;                          // vRedOp_t
+    int root;
+    int aligned;                     // user buffers allow 16-byte vectors
+    int hasScale;
+    float scale;
+    size_t count;                    // as OnePassArgs
+    size_t blockElems;
+    size_t chanElems;
+    size_t chunkElems;               // elements per block per chunk (4 slots)
+    size_t slotElems;                // payload elements per slot
+    size_t slotBytes;                // physical bytes per slot
+    char* fifo;                      // (channel, rank) FIFO at fifo + (ch * N + r) * 8 * slotBytes
+    unsigned long long* ctrl;        // (channel, rank) block: [0] = head, [16] = tail
+    unsigned long long epochHi;      // launch epoch << 32 (Simple counters, LL128 flags)
+    unsigned int llEpoch;            // (epoch & 0xFF) << 24 (LL flags)
+    unsigned long long timeoutNs;
+    volatile unsigned int* abortHost;   // host-set abort (pinned, mapped)
+    unsigned int* abortDev;          // set by any CTA that gives up
+    Status* status;                  // device copy
+    volatile Status* statusHost;     // pinned mirror
+    int testStallRank;               // test hook: this rank never posts data (-1 = off)
+};
+
+// Launchers (defined in the kernel translation units).  Each returns the launch status.
+cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, bool vec,
+                                     int grid, int threads, cudaStream_t s);
+cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
+                                          vDataType_t outType, bool vec, int grid, int threads,
+                                          cudaStream_t s);
+cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+                                     int threads, cudaStream_t s);
+cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+                                     int threads, cudaStream_t s);
+cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+                                    int threads, cudaStream_t s);
+cudaError_t launch_alltoallv(const A2AvArgs& a, int grid, int threads, cudaStream_t s);
+
+// Cooperative launch of the staged ring (all CTAs co-resident or the launch fails).
+cudaError_t launch_ring(const RingArgs& a, vDataType_t dt, vRedOp_t op, vDataType_t outType,
+                        vProto_t proto, int grid, int threads, cudaStream_t s);
+// Largest co-resident grid for the ring kernel of this type/op/protocol.
+cudaError_t ring_max_coresident(vDataType_t dt, vRedOp_t op, vDataType_t outType, vProto_t proto,
+                                int threads, int smCount, int* maxCtas);
+
+}  // namespace vc

@@ -1,0 +1,262 @@
+// k_onepass.cu -- one-pass reduction kernels: all-reduce and reduce-scatter.
+//
+// Every virtual rank's buffer is addressable from one kernel, so instead of moving
+// partials from rank to rank (2(N-1) ring steps, "NCCL book" section 2.3) each thread
+// reads element e of all N ranks once, reduces them in the ring's order, and writes the
+// result once per output: 2*N*S bytes for an all-reduce, the minimum.  This is the
+// virtual-rank form of the symmetric-memory kernels that read peers' buffers directly
+// (NCCL book chapter 5 section 5; "AI Systems Performance Engineering (3)", NVLS and
+// symmetric memory).
+//
+// Order: block b of the buffer is reduced as ranks b+1, b+2, ..., b (mod N), each partial
+// rounded to the data type -- exactly the partial a ring reduce-scatter accumulates
+// (RingARAlgorithm::getNextSendAddr: at stage s rank r handles chunk (r + N - 1 - s) mod N).
+// Channels own contiguous sub-ranges of every block (NCCL book section 2.2); a channel's
+// CTAs stride over its sub-range.  Blocks, channel ranges and 16-byte vectors all start
+// on 16-byte boundaries, so a vector never straddles two blocks.
+#include "device.cuh"
+
+namespace vc {
+
+// Load the element vector at element offset `off` of every rank, starting at rank
+// `first` and wrapping, and reduce in that order.  Up to 8 loads are in flight before the
+// first use.
+template <int DT, int OP>
+__device__ __forceinline__ uint4 reduce_vec_ring(const OnePassArgs& a, int first, size_t boff) {
+    const int N = a.nRanks;
+    uint4 acc = ld_stream((const char*)a.send[first] + boff);
+    int rk = first + 1 == N ? 0 : first + 1;
+    for (int k = 1; k < N; k += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            if (k + j < N) {
+                v[j] = ld_stream((const char*)a.send[rk] + boff);
+                rk = rk + 1 == N ? 0 : rk + 1;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            if (k + j < N) acc = op_vec<DT, OP>(acc, v[j]);
+    }
+    return acc;
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t reduce_elem_ring(const OnePassArgs& a, int first, size_t e) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    const int N = a.nRanks;
+    uint32_t acc = ld_elem<ESZ>(a.send[first], e);
+    int rk = first + 1 == N ? 0 : first + 1;
+    for (int k = 1; k < N; k++) {
+        acc = op_elem<DT, OP>(acc, ld_elem<ESZ>(a.send[rk], e));
+        rk = rk + 1 == N ? 0 : rk + 1;
+    }
+    return acc;
+}
+
+// Per channel the work is (block, unit) pairs, flattened so that small buffers still
+// spread over all threads: unit i of block b covers elements [lo_b + i*U, lo_b + (i+1)*U)
+// with U = 16 / esz on the vector path (1 otherwise) and lo_b = b*B + ch*Lc.  Only the
+// very end of the buffer can cut a vector short; its elements go element by element.
+struct ChannelSpan {
+    size_t lo;       // first element of this channel's range in block 0
+    size_t units;    // units per block (of the full-length range)
+};
+
+__device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch, size_t unit) {
+    ChannelSpan s;
+    const size_t lo = min((size_t)ch * a.chanElems, a.blockElems);
+    const size_t hi = min((size_t)(ch + 1) * a.chanElems, a.blockElems);
+    s.lo = lo;
+    s.units = (hi - lo + unit - 1) / unit;
+    return s;
+}
+
+// All-reduce.  grid = nChannels * ctasPerChannel.
+template <int DT, int OP, bool VEC>
+__global__ void __launch_bounds__(kOnePassThreads)
+k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    constexpr int U = VEC ? 16 / ESZ : 1;
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
+    const ChannelSpan sp = channel_span(a, ch, U);
+    const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, a.blockElems);
+    const size_t total = sp.units * (size_t)N;
+    for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < total; j += stride) {
+        const int b = (int)(j / sp.units);
+        const size_t i = j - (size_t)b * sp.units;
+        const size_t base = (size_t)b * a.blockElems;
+        const size_t e = base + sp.lo + i * U;
+        const size_t hi = min(base + chEnd, a.count);
+        if (e >= hi) continue;
+        const int first = b + 1 == N ? 0 : b + 1;
+        if (VEC && e + U <= hi) {
+            const size_t boff = e * ESZ;
+            const uint4 acc = reduce_vec_ring<DT, OP>(a, first, boff);
+            for (int r = 0; r < N; r++) st_stream((char*)a.recv[r] + boff, acc);
+        } else {
+            for (size_t x = e; x < min(e + U, hi); x++) {
+                const uint32_t acc = reduce_elem_ring<DT, OP>(a, first, x);
+                for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], x, acc);
+            }
+        }
+    }
+}
+
+// Store a reduced 16-byte vector of DT elements as OUT elements, out = (float)acc * scale
+// when hasScale (or a plain store when OUT == DT and no scale).
+template <int DT, int OUT>
+__device__ __forceinline__ void store_epilogue_vec(void* outBase, size_t outElem, uint4 acc,
+                                                   bool hasScale, float scale) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    constexpr int OSZ = DTypeOf<OUT>::size;
+    if (DT == OUT && !hasScale) {
+        st_stream((char*)outBase + outElem * OSZ, acc);
+        return;
+    }
+    constexpr int VE = 16 / ESZ;
+    uint32_t w[4] = {acc.x, acc.y, acc.z, acc.w};
+    uint32_t o[VE];
+#pragma unroll
+    for (int i = 0; i < VE; i++) {
+        const uint32_t bits = ESZ == 4 ? w[i] : ((w[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+        float f = elem_to_f32<DT>(bits);
+        if (hasScale) f = __fmul_rn(f, scale);
+        o[i] = f32_to_elem<OUT>(f);
+    }
+    if (OSZ == 4) {
+#pragma unroll
+        for (int q = 0; q < VE / 4; q++)
+            st_stream((char*)outBase + (outElem + 4 * q) * 4,
+                      make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+    } else {
+        st_stream((char*)outBase + outElem * 2,
+                  make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16),
+                             o[6] | (o[7] << 16)));
+    }
+}
+
+template <int DT, int OUT>
+__device__ __forceinline__ void store_epilogue_elem(void* outBase, size_t outElem, uint32_t acc,
+                                                    bool hasScale, float scale) {
+    constexpr int OSZ = DTypeOf<OUT>::size;
+    if (DT == OUT && !hasScale) {
+        st_elem<OSZ>(outBase, outElem, acc);
+        return;
+    }
+    float f = elem_to_f32<DT>(acc);
+    if (hasScale) f = __fmul_rn(f, scale);
+    st_elem<OSZ>(outBase, outElem, f32_to_elem<OUT>(f));
+}
+
+// Reduce-scatter: block r = [r*rc, (r+1)*rc) of every send buffer lands in recv[r].
+// a.count = N * rc, a.blockElems = rc.  VEC requires rc % (16 / esz) == 0.
+template <int DT, int OP, int OUT, bool VEC>
+__global__ void __launch_bounds__(kOnePassThreads)
+k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    constexpr int U = VEC ? 16 / ESZ : 1;
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
+    const size_t rc = a.blockElems;
+    const bool hasScale = a.hasScale != 0;
+    const ChannelSpan sp = channel_span(a, ch, U);
+    const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, rc);
+    const size_t total = sp.units * (size_t)N;
+    for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < total; j += stride) {
+        const int r = (int)(j / sp.units);
+        const size_t i = j - (size_t)r * sp.units;
+        const size_t t = sp.lo + i * U;                 // element within block r
+        if (t >= chEnd) continue;
+        const size_t base = (size_t)r * rc;
+        const int first = r + 1 == N ? 0 : r + 1;
+        if (VEC && t + U <= chEnd) {
+            const uint4 acc = reduce_vec_ring<DT, OP>(a, first, (base + t) * ESZ);
+            store_epilogue_vec<DT, OUT>(a.recv[r], t, acc, hasScale, a.scale);
+        } else {
+            for (size_t x = t; x < min(t + U, chEnd); x++) {
+                const uint32_t acc = reduce_elem_ring<DT, OP>(a, first, base + x);
+                store_epilogue_elem<DT, OUT>(a.recv[r], x, acc, hasScale, a.scale);
+            }
+        }
+    }
+}
+
+// ---- dispatch --------------------------------------------------------------------------
+
+template <int DT, int OP>
+static cudaError_t ar_dispatch_vec(const OnePassArgs& a, bool vec, int grid, int threads,
+                                   cudaStream_t s) {
+    if (vec) k_allreduce_onepass<DT, OP, true><<<grid, threads, 0, s>>>(a);
+    else k_allreduce_onepass<DT, OP, false><<<grid, threads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t ar_dispatch_op(const OnePassArgs& a, vRedOp_t op, bool vec, int grid, int threads,
+                                  cudaStream_t s) {
+    switch (op) {
+    case vSum: return ar_dispatch_vec<DT, kSum>(a, vec, grid, threads, s);
+    case vProd: return ar_dispatch_vec<DT, kProd>(a, vec, grid, threads, s);
+    case vMin: return ar_dispatch_vec<DT, kMin>(a, vec, grid, threads, s);
+    case vMax: return ar_dispatch_vec<DT, kMax>(a, vec, grid, threads, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, bool vec,
+                                     int grid, int threads, cudaStream_t s) {
+    switch (dt) {
+    case vFloat32: return ar_dispatch_op<kF32>(a, op, vec, grid, threads, s);
+    case vFloat16: return ar_dispatch_op<kF16>(a, op, vec, grid, threads, s);
+    case vBFloat16: return ar_dispatch_op<kBF16>(a, op, vec, grid, threads, s);
+    case vInt32: return ar_dispatch_op<kI32>(a, op, vec, grid, threads, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int DT, int OP, int OUT>
+static cudaError_t rs_dispatch_vec(const OnePassArgs& a, bool vec, int grid, int threads,
+                                   cudaStream_t s) {
+    if (vec) k_reduce_scatter_onepass<DT, OP, OUT, true><<<grid, threads, 0, s>>>(a);
+    else k_reduce_scatter_onepass<DT, OP, OUT, false><<<grid, threads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT, int OUT>
+static cudaError_t rs_dispatch_op(const OnePassArgs& a, vRedOp_t op, bool vec, int grid,
+                                  int threads, cudaStream_t s) {
+    switch (op) {
+    case vSum: return rs_dispatch_vec<DT, kSum, OUT>(a, vec, grid, threads, s);
+    case vProd: return rs_dispatch_vec<DT, kProd, OUT>(a, vec, grid, threads, s);
+    case vMin: return rs_dispatch_vec<DT, kMin, OUT>(a, vec, grid, threads, s);
+    case vMax: return rs_dispatch_vec<DT, kMax, OUT>(a, vec, grid, threads, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
+                                          vDataType_t outType, bool vec, int grid, int threads,
+                                          cudaStream_t s) {
+    const bool toF32 = outType == vFloat32 && dt != vFloat32;
+    if (outType != dt && !toF32) return cudaErrorInvalidValue;
+    switch (dt) {
+    case vFloat32: return rs_dispatch_op<kF32, kF32>(a, op, vec, grid, threads, s);
+    case vFloat16:
+        return toF32 ? rs_dispatch_op<kF16, kF32>(a, op, vec, grid, threads, s)
+                     : rs_dispatch_op<kF16, kF16>(a, op, vec, grid, threads, s);
+    case vBFloat16:
+        return toF32 ? rs_dispatch_op<kBF16, kF32>(a, op, vec, grid, threads, s)
+                     : rs_dispatch_op<kBF16, kBF16>(a, op, vec, grid, threads, s);
+    case vInt32: return rs_dispatch_op<kI32, kI32>(a, op, vec, grid, threads, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vc

@@ -1,0 +1,166 @@
+// planner.cpp -- host-side planning of one collective: block partition, channel split,
+// ring chunk/slot geometry, algorithm and protocol choice, launch shape.  Pure host
+// arithmetic with no CUDA calls, so it is unit-tested without a GPU.
+//
+// Sources for the rules:
+//  * block size B = alignUp(ceil(count / N), 16 / elemSize): the tail-chunk rule of
+//    RingARAlgorithm::getNextSendAddr (NCCL book section 2.3);
+//  * channels: each channel owns count / nChannels of the data (NCCL book section 2.2,
+//    channel walkthrough step 3); here the split is applied inside every block, rounded
+//    up to 16 bytes, so a channel's share of each block starts on a vector boundary;
+//  * ring geometry: FIFOs of NCCL_STEPS = 8 slots, a chunk = ALLREDUCE_CHUNKSTEPS = 4
+//    slots, a slice = ALLREDUCE_SLICESTEPS = 2 slots (NCCL book chapter 6, ncclInfo);
+//  * protocol payload: LL carries half the bytes of its slots, LL128 120 of every 128
+//    (NCCL book chapter 5, ring.cc: busBw * 0.5 for LL, * 0.92 = 120/128 for LL128);
+//  * bus bandwidth factor nSteps / nRanks with nSteps = 2(N-1) for all-reduce and N-1
+//    otherwise (NCCL book chapter 5, ring.cc, algBw = busBw * nRanks / nSteps).
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+size_t elem_size(int dt) {
+    switch (dt) {
+    case vFloat32: case vInt32: return 4;
+    case vFloat16: case vBFloat16: return 2;
+    default: return 0;
+    }
+}
+
+size_t div_up(size_t a, size_t b) { return (a + b - 1) / b; }
+size_t align_up(size_t a, size_t b) { return div_up(a, b) * b; }
+
+size_t pow2_floor(size_t x) {
+    size_t p = 1;
+    while (p * 2 <= x) p *= 2;
+    return p;
+}
+
+}  // namespace
+
+extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
+    if (!q || !p) return vInvalidArgument;
+    std::memset(p, 0, sizeof(*p));
+    const int N = q->nRanks;
+    if (N < 1 || N > VCOMM_MAX_RANKS) return vInvalidArgument;
+    if (q->nChannels < 1 || q->nChannels > VCOMM_MAX_CHANNELS) return vInvalidArgument;
+    if (q->coll < vCollAllReduce || q->coll > vCollAllToAllv) return vInvalidArgument;
+    if (q->proto < vProtoSimple || q->proto > vProtoAuto) return vInvalidArgument;
+    if (q->algo < vAlgoAuto || q->algo > vAlgoRing) return vInvalidArgument;
+    const size_t esz = elem_size(q->datatype);
+    if (esz == 0) return vInvalidArgument;
+    if (q->chunkBytes != 0 && (q->chunkBytes < 4096 || q->chunkBytes > (64u << 20) ||
+                               (q->chunkBytes & (q->chunkBytes - 1)) != 0))
+        return vInvalidArgument;
+    const size_t VE = 16 / esz;
+    const size_t count = q->count;
+    const int smCount = q->smCount > 0 ? q->smCount : 152;
+    const size_t l2 = q->l2Bytes > 0 ? q->l2Bytes : (size_t)126 << 20;
+
+    // ---- blocks -----------------------------------------------------------------------
+    size_t B = 0;          // elements per rank block
+    size_t total = 0;      // elements of the block space (what channel ranges clamp to)
+    switch (q->coll) {
+    case vCollAllReduce: B = align_up(div_up(count, (size_t)N), VE); total = count; break;
+    case vCollReduceScatter: B = count; total = count * (size_t)N; break;
+    case vCollAllGather: B = count; total = count * (size_t)N; break;
+    case vCollBroadcast: B = count; total = count; break;
+    case vCollAllToAll: B = count; total = count * (size_t)N * (size_t)N; break;
+    case vCollAllToAllv: B = 0; total = 0; break;
+    }
+    p->blockElems = B;
+    p->nChannels = q->nChannels;
+    p->channelElems = B ? align_up(div_up(B, (size_t)q->nChannels), VE) : 0;
+
+    // ---- vector path ------------------------------------------------------------------
+    bool vec = q->aligned16 != 0;
+    if (q->coll == vCollReduceScatter || q->coll == vCollAllGather || q->coll == vCollAllToAll)
+        vec = vec && (count % VE == 0);        // block starts r*count must stay 16-byte aligned
+    p->vectorized = vec ? 1 : 0;
+
+    // ---- algorithm --------------------------------------------------------------------
+    bool ring = q->algo == vAlgoRing && N > 1 &&
+                (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ||
+                 q->coll == vCollAllGather || q->coll == vCollBroadcast);
+    p->algo = ring ? vAlgoRing : vAlgoOnePass;
+    p->launches = 1;
+
+    // ---- traffic model ----------------------------------------------------------------
+    const double S = (double)count * (double)esz;
+    switch (q->coll) {
+    case vCollAllReduce: p->minBytes = 2.0 * N * S; p->busFactor = 2.0 * (N - 1) / N; break;
+    case vCollReduceScatter: p->minBytes = (double)N * N * S + N * S; p->busFactor = (double)(N - 1) / N; break;
+    case vCollAllGather: p->minBytes = (double)N * S + (double)N * N * S; p->busFactor = (double)(N - 1) / N; break;
+    case vCollBroadcast: p->minBytes = S + (double)N * S; p->busFactor = (double)(N - 1) / N; break;
+    case vCollAllToAll: p->minBytes = 2.0 * N * N * S; p->busFactor = (double)(N - 1) / N; break;
+    default: p->minBytes = 0; p->busFactor = (double)(N - 1) / N; break;
+    }
+
+    if (!ring) {
+        // One pass: about two resident CTAs of 512 threads per SM, dealt evenly to the
+        // channels; never more CTAs than a channel has vectors to move.
+        p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
+        p->threadsPerCta = vc::kOnePassThreads;
+        const int target = 2 * smCount;
+        int per = std::max(1, (int)div_up((size_t)target, (size_t)q->nChannels));
+        size_t work = 0;    // vectors (or elements) one channel moves per block pass
+        if (q->coll == vCollAllToAllv) {
+            work = (size_t)1 << 40;
+        } else {
+            const size_t chElems = std::min(p->channelElems, B);
+            size_t blocks = q->coll == vCollBroadcast ? 1 : (size_t)N;
+            if (q->coll == vCollAllToAll) blocks = (size_t)N * N;
+            work = div_up(chElems, vec ? VE : 1) * (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ? blocks : 1);
+        }
+        const size_t maxPer = std::max<size_t>(1, div_up(work, (size_t)p->threadsPerCta));
+        per = (int)std::min<size_t>((size_t)per, maxPer);
+        if (q->coll == vCollAllToAllv) { p->nChannels = 1; per = target; }
+        p->ctasPerChannel = per;
+        p->gridCtas = per * p->nChannels;
+        (void)total;
+        return vSuccess;
+    }
+
+    // ---- ring geometry ------------------------------------------------------------------
+    int proto = q->proto;
+    const double perChannelBytes = (double)p->channelElems * esz;
+    if (proto == vProtoAuto)
+        proto = perChannelBytes < 64.0 * 1024 ? vProtoLL : perChannelBytes < 1024.0 * 1024 ? vProtoLL128 : vProtoSimple;
+    p->proto = proto;
+    size_t chunk = q->chunkBytes;
+    if (chunk == 0) {
+        // Keep all FIFOs (2 chunks per (channel, rank)) within half of L2.
+        const size_t fit = l2 / 2 / (2 * (size_t)q->nChannels * (size_t)N);
+        chunk = std::min<size_t>((size_t)1 << 20, std::max<size_t>(16384, pow2_floor(fit)));
+    }
+    const size_t slotBytes = chunk / vc::kChunkSlots;   // >= 1 KiB, a multiple of 256
+    size_t slotPayload = slotBytes;
+    if (proto == vProtoLL) slotPayload = slotBytes / 2;
+    else if (proto == vProtoLL128) slotPayload = slotBytes / 128 * 120;
+    p->slotBytes = slotBytes;
+    p->slotPayloadElems = slotPayload / esz;
+    p->chunkElems = p->slotPayloadElems * vc::kChunkSlots;
+    p->fifoBytes = slotBytes * vc::kFifoSlots;
+    p->nChannels = q->nChannels;
+    p->ctasPerChannel = N;
+    p->gridCtas = N * q->nChannels;
+    p->threadsPerCta = vc::kRingThreads;
+    // The 16-byte path of the ring also needs every slot and chunk to start on a vector.
+    if (p->slotPayloadElems % VE != 0) p->vectorized = 0;
+    return vSuccess;
+}
+
+extern "C" vResult_t vPlanChannelRange(const vPlanInfo_t* p, size_t count, int channel, int block,
+                                       size_t* lo, size_t* hi) {
+    if (!p || !lo || !hi || channel < 0 || channel >= p->nChannels || block < 0) return vInvalidArgument;
+    const size_t base = (size_t)block * p->blockElems;
+    size_t l = base + std::min((size_t)channel * p->channelElems, p->blockElems);
+    size_t h = base + std::min((size_t)(channel + 1) * p->channelElems, p->blockElems);
+    l = std::min(l, count);
+    h = std::min(h, count);
+    *lo = l;
+    *hi = std::max(l, h);
+    return vSuccess;
+}

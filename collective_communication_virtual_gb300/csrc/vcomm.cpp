@@ -1,0 +1,594 @@
+// vcomm.cpp -- the C ABI of libvcomm: communicator lifecycle, argument checks, planning
+// and launch of the collectives on the caller's stream.
+//
+// Checks follow ncclEnqueueCheck / taskAppend (NCCL book chapter 6): a bad communicator
+// or argument returns vInvalidArgument without enqueuing anything; count == 0 returns
+// vSuccess at once; a sticky asynchronous error makes every later call return it
+// (NCCL book section 2.1, asyncResult).  The communicator carries start/end magic words
+// like ncclComm so a destroyed or foreign handle is refused.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+constexpr unsigned long long kMagic = 0x76636F6D6D763031ull;   // "vcommv01"
+
+struct Config {
+    vAlgo_t algo = vAlgoAuto;
+    size_t chunkBytes = 0;           // 0: planner default
+    int timeoutMs = 2000;
+    bool debug = false;
+};
+
+}  // namespace
+
+struct vcomm {
+    unsigned long long startMagic;
+    int nRanks;
+    int nChannels;
+    vProto_t proto;
+    Config cfg;
+    int device;
+    int smCount;
+    size_t l2Bytes;
+    int cooperative;
+    // status: device copy decides the first error; pinned mirror for the host
+    vc::Status* statusDev;
+    vc::Status* statusHost;          // pinned, mapped
+    vc::Status* statusHostDev;       // its device address
+    unsigned int* abortHost;         // pinned, mapped
+    unsigned int* abortHostDev;
+    unsigned int* abortDev;
+    vResult_t hostError;             // sticky error found on the host side
+    // ring staging
+    char* fifo;
+    size_t fifoCap;
+    unsigned long long* ctrl;
+    unsigned int epoch;
+    int testStallRank;
+    cudaEvent_t lastEvent;
+    bool eventRecorded;
+    unsigned long long endMagic;
+};
+
+namespace {
+
+size_t elem_size(int dt) {
+    switch (dt) {
+    case vFloat32: case vInt32: return 4;
+    case vFloat16: case vBFloat16: return 2;
+    default: return 0;
+    }
+}
+
+bool comm_ok(const vcomm* c) {
+    return c != nullptr && c->startMagic == kMagic && c->endMagic == kMagic;
+}
+
+// Make the communicator's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+vResult_t sticky(vcomm* c) {
+    if (c->hostError != vSuccess) return c->hostError;
+    const unsigned code = *(volatile unsigned*)&c->statusHost->code;
+    return (vResult_t)code;
+}
+
+vResult_t cuda_fail(vcomm* c, cudaError_t e, const char* what) {
+    if (c && c->cfg.debug) std::fprintf(stderr, "vcomm: %s failed: %s\n", what, cudaGetErrorString(e));
+    cudaGetLastError();     // clear a non-sticky launch error
+    return vUnhandledCudaError;
+}
+
+void read_env(Config* cfg) {
+    if (const char* s = std::getenv("VCOMM_ALGO")) {
+        if (!std::strcmp(s, "onepass")) cfg->algo = vAlgoOnePass;
+        else if (!std::strcmp(s, "ring")) cfg->algo = vAlgoRing;
+        else cfg->algo = vAlgoAuto;
+    }
+    if (const char* s = std::getenv("VCOMM_CHUNK_BYTES")) {
+        const unsigned long long v = std::strtoull(s, nullptr, 0);
+        if (v >= 4096 && v <= (64ull << 20) && (v & (v - 1)) == 0) cfg->chunkBytes = (size_t)v;
+    }
+    if (const char* s = std::getenv("VCOMM_TIMEOUT_MS")) {
+        const long v = std::strtol(s, nullptr, 0);
+        if (v >= 1 && v <= 3600 * 1000) cfg->timeoutMs = (int)v;
+    }
+    if (const char* s = std::getenv("VCOMM_DEBUG")) cfg->debug = !std::strcmp(s, "INFO");
+}
+
+void free_comm(vcomm* c) {
+    if (c->lastEvent) cudaEventDestroy(c->lastEvent);
+    if (c->fifo) cudaFree(c->fifo);
+    if (c->ctrl) cudaFree(c->ctrl);
+    if (c->statusDev) cudaFree(c->statusDev);
+    if (c->abortDev) cudaFree(c->abortDev);
+    if (c->statusHost) cudaFreeHost(c->statusHost);
+    if (c->abortHost) cudaFreeHost(c->abortHost);
+    c->startMagic = c->endMagic = 0;
+    delete c;
+}
+
+const char* coll_name(int coll) {
+    static const char* n[] = {"AllReduce", "ReduceScatter", "AllGather", "Broadcast", "AllToAll", "AllToAllv"};
+    return (coll >= 0 && coll <= 5) ? n[coll] : "?";
+}
+
+void debug_plan(const vcomm* c, int coll, size_t count, int dt, const vPlanInfo_t& p) {
+    if (!c->cfg.debug) return;
+    std::fprintf(stderr,
+                 "vcomm INFO %s count=%zu dt=%d N=%d algo=%s proto=%d channels=%d ctas/ch=%d grid=%d "
+                 "threads=%d vec=%d B=%zu Lc=%zu chunk=%zu slotElems=%zu slotBytes=%zu\n",
+                 coll_name(coll), count, dt, c->nRanks, p.algo == vAlgoRing ? "ring" : "onepass", p.proto,
+                 p.nChannels, p.ctasPerChannel, p.gridCtas, p.threadsPerCta, p.vectorized, p.blockElems,
+                 p.channelElems, p.chunkElems, p.slotPayloadElems, p.slotBytes);
+}
+
+bool ptr_aligned(const void* p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// Common checks of the pointer arrays.  Returns vSuccess and sets *aligned16.
+vResult_t check_ptrs(const vcomm* c, const void* const* send, void* const* recv, size_t esz,
+                     int root, bool needAllSend, int* aligned16) {
+    if (!send || !recv) return vInvalidArgument;
+    bool a16 = true;
+    for (int r = 0; r < c->nRanks; r++) {
+        if (needAllSend || r == root) {
+            if (!send[r] || !ptr_aligned(send[r], esz)) return vInvalidArgument;
+            a16 = a16 && ptr_aligned(send[r], 16);
+        }
+        if (!recv[r] || !ptr_aligned(recv[r], esz)) return vInvalidArgument;
+        a16 = a16 && ptr_aligned(recv[r], 16);
+    }
+    *aligned16 = a16 ? 1 : 0;
+    return vSuccess;
+}
+
+vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned16, vPlanInfo_t* p) {
+    vPlanRequest_t q;
+    std::memset(&q, 0, sizeof(q));
+    q.nRanks = c->nRanks;
+    q.nChannels = c->nChannels;
+    q.proto = c->proto;
+    q.algo = c->cfg.algo;
+    q.coll = coll;
+    q.datatype = dt;
+    q.count = count;
+    q.chunkBytes = c->cfg.chunkBytes;
+    q.aligned16 = aligned16;
+    q.smCount = c->smCount;
+    q.l2Bytes = c->l2Bytes;
+    return vPlanCompute(&q, p);
+}
+
+vResult_t finish_launch(vcomm* c, cudaError_t e, cudaStream_t stream, const char* what) {
+    if (e != cudaSuccess) {
+        c->hostError = vUnhandledCudaError;
+        return cuda_fail(c, e, what);
+    }
+    if (cudaEventRecord(c->lastEvent, stream) == cudaSuccess) c->eventRecorded = true;
+    return vSuccess;
+}
+
+void fill_onepass(vc::OnePassArgs* a, const vcomm* c, const void* const* send, void* const* recv,
+                  const vPlanInfo_t& p, size_t count) {
+    std::memset(a, 0, sizeof(*a));
+    for (int r = 0; r < c->nRanks; r++) {
+        a->send[r] = send ? send[r] : nullptr;
+        a->recv[r] = recv[r];
+    }
+    a->nRanks = c->nRanks;
+    a->ctasPerChannel = p.ctasPerChannel;
+    a->count = count;
+    a->blockElems = p.blockElems;
+    a->chanElems = p.channelElems;
+}
+
+// Grow the ring FIFOs and control words if this plan needs more than the communicator has.
+vResult_t ensure_fifo(vcomm* c, const vPlanInfo_t& p) {
+    const size_t need = (size_t)c->nChannels * c->nRanks * p.fifoBytes;
+    if (!c->ctrl) {
+        const size_t ctrlBytes = (size_t)c->nChannels * c->nRanks * vc::kCtrlStride * sizeof(unsigned long long);
+        cudaError_t e = cudaMalloc(&c->ctrl, ctrlBytes);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaMalloc(ctrl)");
+        e = cudaMemset(c->ctrl, 0, ctrlBytes);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemset(ctrl)");
+    }
+    if (need <= c->fifoCap) return vSuccess;
+    if (c->eventRecorded) cudaEventSynchronize(c->lastEvent);
+    if (c->fifo) cudaFree(c->fifo);
+    c->fifo = nullptr;
+    c->fifoCap = 0;
+    cudaError_t e = cudaMalloc(&c->fifo, need);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaMalloc(fifo)");
+    e = cudaMemset(c->fifo, 0, need);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemset(fifo)");
+    c->fifoCap = need;
+    return vSuccess;
+}
+
+vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* const* recv,
+                           size_t count, vDataType_t dt, vRedOp_t op, vDataType_t outType, int root,
+                           bool hasScale, float scale, const vPlanInfo_t& p, cudaStream_t stream) {
+    if (!c->cooperative) return vInvalidUsage;
+    int maxCtas = 0;
+    cudaError_t e = vc::ring_max_coresident(dt, op, outType, (vProto_t)p.proto, p.threadsPerCta,
+                                            c->smCount, &maxCtas);
+    if (e != cudaSuccess) return cuda_fail(c, e, "occupancy");
+    if (p.gridCtas > maxCtas) {
+        if (c->cfg.debug)
+            std::fprintf(stderr, "vcomm: ring needs %d co-resident CTAs, device holds %d\n", p.gridCtas, maxCtas);
+        return vInvalidUsage;
+    }
+    vResult_t res = ensure_fifo(c, p);
+    if (res != vSuccess) return res;
+    c->epoch++;
+    if ((c->epoch & 0xFFu) == 0) {
+        // LL flags keep only the low byte of the epoch: clear stale flags when it wraps.
+        e = cudaMemsetAsync(c->fifo, 0, c->fifoCap, stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(fifo)");
+        c->epoch++;
+    }
+    vc::RingArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int r = 0; r < c->nRanks; r++) {
+        a.send[r] = send[r];
+        a.recv[r] = recv[r];
+    }
+    a.nRanks = c->nRanks;
+    a.nChannels = c->nChannels;
+    a.coll = coll;
+    a.op = op;
+    a.root = root;
+    a.aligned = p.vectorized;
+    a.hasScale = hasScale ? 1 : 0;
+    a.scale = scale;
+    switch (coll) {
+    case vCollAllReduce: case vCollBroadcast: a.count = count; break;
+    default: a.count = count * (size_t)c->nRanks; break;
+    }
+    a.blockElems = p.blockElems;
+    a.chanElems = p.channelElems;
+    a.chunkElems = p.chunkElems;
+    a.slotElems = p.slotPayloadElems;
+    a.slotBytes = p.slotBytes;
+    a.fifo = c->fifo;
+    a.ctrl = c->ctrl;
+    a.epochHi = (unsigned long long)c->epoch << 32;
+    a.llEpoch = (c->epoch & 0xFFu) << 24;
+    a.timeoutNs = (unsigned long long)c->cfg.timeoutMs * 1000000ull;
+    a.abortHost = c->abortHostDev;
+    a.abortDev = c->abortDev;
+    a.status = c->statusDev;
+    a.statusHost = c->statusHostDev;
+    a.testStallRank = c->testStallRank;
+    e = vc::launch_ring(a, dt, op, outType, (vProto_t)p.proto, p.gridCtas, p.threadsPerCta, stream);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();
+        return vInvalidUsage;
+    }
+    return finish_launch(c, e, stream, "ring launch");
+}
+
+// Shared front half of every collective.
+struct Front {
+    vResult_t res;
+    int aligned16;
+};
+
+Front front(vcomm* c, const void* const* send, void* const* recv, size_t count, int dt, int root,
+            bool needAllSend) {
+    Front f{vSuccess, 0};
+    if (!comm_ok(c)) { f.res = vInvalidArgument; return f; }
+    vResult_t s = sticky(c);
+    if (s != vSuccess) { f.res = s; return f; }
+    const size_t esz = elem_size(dt);
+    if (esz == 0) { f.res = vInvalidArgument; return f; }
+    // N*N*count*esz must fit comfortably in size_t
+    const size_t n2 = (size_t)c->nRanks * (size_t)c->nRanks;
+    if (count > ((size_t)1 << 62) / (n2 * esz)) { f.res = vInvalidArgument; return f; }
+    if (count == 0) return f;
+    f.res = check_ptrs(c, send, recv, esz, root, needAllSend, &f.aligned16);
+    return f;
+}
+
+bool valid_op(int op) { return op >= vSum && op <= vMax; }
+
+}  // namespace
+
+extern "C" {
+
+const char* vcommGetErrorString(vResult_t r) {
+    switch (r) {
+    case vSuccess: return "no error";
+    case vUnhandledCudaError: return "unhandled cuda error";
+    case vSystemError: return "system error";
+    case vInternalError: return "internal error";
+    case vInvalidArgument: return "invalid argument";
+    case vInvalidUsage: return "invalid usage";
+    case vTimeout: return "timeout";
+    case vInProgress: return "in progress";
+    case vAborted: return "aborted";
+    }
+    return "unknown result code";
+}
+
+vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol) {
+    if (!comm) return vInvalidArgument;
+    *comm = nullptr;
+    if (nRanks < 1 || nRanks > VCOMM_MAX_RANKS) return vInvalidArgument;
+    if (nChannels < 1 || nChannels > VCOMM_MAX_CHANNELS) return vInvalidArgument;
+    if (protocol < vProtoSimple || protocol > vProtoAuto) return vInvalidArgument;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+    vcomm* c = new (std::nothrow) vcomm();
+    if (!c) return vSystemError;
+    std::memset((void*)c, 0, sizeof(*c));
+    c->cfg = Config();
+    read_env(&c->cfg);
+    c->nRanks = nRanks;
+    c->nChannels = nChannels;
+    c->proto = protocol;
+    c->device = dev;
+    c->testStallRank = -1;
+    c->hostError = vSuccess;
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) goto fail;
+    c->smCount = v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) goto fail;
+    c->l2Bytes = (size_t)v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) goto fail;
+    c->cooperative = v;
+    if ((e = cudaMalloc(&c->statusDev, sizeof(vc::Status))) != cudaSuccess) goto fail;
+    if ((e = cudaMemset(c->statusDev, 0, sizeof(vc::Status))) != cudaSuccess) goto fail;
+    if ((e = cudaMalloc(&c->abortDev, sizeof(unsigned int))) != cudaSuccess) goto fail;
+    if ((e = cudaMemset(c->abortDev, 0, sizeof(unsigned int))) != cudaSuccess) goto fail;
+    if ((e = cudaHostAlloc(&c->statusHost, sizeof(vc::Status), cudaHostAllocMapped)) != cudaSuccess) goto fail;
+    std::memset(c->statusHost, 0, sizeof(vc::Status));
+    if ((e = cudaHostGetDevicePointer(&c->statusHostDev, c->statusHost, 0)) != cudaSuccess) goto fail;
+    if ((e = cudaHostAlloc(&c->abortHost, sizeof(unsigned int), cudaHostAllocMapped)) != cudaSuccess) goto fail;
+    *c->abortHost = 0;
+    if ((e = cudaHostGetDevicePointer(&c->abortHostDev, c->abortHost, 0)) != cudaSuccess) goto fail;
+    if ((e = cudaEventCreateWithFlags(&c->lastEvent, cudaEventDisableTiming)) != cudaSuccess) goto fail;
+    c->startMagic = c->endMagic = kMagic;
+    *comm = c;
+    return vSuccess;
+fail:
+    {
+        vResult_t r = cuda_fail(c, e, "vcommInit");
+        free_comm(c);
+        return r;
+    }
+}
+
+vResult_t vcommDestroy(vcomm_t c) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    DeviceGuard g(c->device);
+    if (c->eventRecorded) cudaEventSynchronize(c->lastEvent);
+    free_comm(c);
+    return vSuccess;
+}
+
+vResult_t vcommGetAsyncError(vcomm_t c, vResult_t* err) {
+    if (!comm_ok(c) || !err) return vInvalidArgument;
+    *err = sticky(c);
+    return vSuccess;
+}
+
+vResult_t vcommAbort(vcomm_t c) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    *(volatile unsigned int*)c->abortHost = 1u;
+    if (c->hostError == vSuccess) c->hostError = vAborted;
+    return vSuccess;
+}
+
+vResult_t vcommSetAlgo(vcomm_t c, vAlgo_t algo) {
+    if (!comm_ok(c) || algo < vAlgoAuto || algo > vAlgoRing) return vInvalidArgument;
+    c->cfg.algo = algo;
+    return vSuccess;
+}
+
+vResult_t vcommSetProtocol(vcomm_t c, vProto_t proto) {
+    if (!comm_ok(c) || proto < vProtoSimple || proto > vProtoAuto) return vInvalidArgument;
+    c->proto = proto;
+    return vSuccess;
+}
+
+vResult_t vcommSetChunkBytes(vcomm_t c, size_t chunkBytes) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    if (chunkBytes != 0 &&
+        (chunkBytes < 4096 || chunkBytes > (64u << 20) || (chunkBytes & (chunkBytes - 1)) != 0))
+        return vInvalidArgument;
+    c->cfg.chunkBytes = chunkBytes;
+    return vSuccess;
+}
+
+vResult_t vcommSetTimeoutMs(vcomm_t c, int timeoutMs) {
+    if (!comm_ok(c) || timeoutMs < 1) return vInvalidArgument;
+    c->cfg.timeoutMs = timeoutMs;
+    return vSuccess;
+}
+
+vResult_t vcommTestSetStallRank(vcomm_t c, int rank) {
+    if (!comm_ok(c) || rank < -1 || rank >= c->nRanks) return vInvalidArgument;
+    c->testStallRank = rank;
+    return vSuccess;
+}
+
+vResult_t vcommQueryPlan(vcomm_t c, vColl_t coll, size_t count, vDataType_t dt, int aligned16,
+                         vPlanInfo_t* plan) {
+    if (!comm_ok(c) || !plan) return vInvalidArgument;
+    return make_plan(c, coll, count, dt, aligned16, plan);
+}
+
+vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
+                     vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    Front f = front(c, send, recv, count, dt, 0, true);
+    if (f.res != vSuccess || count == 0) return f.res;
+    if (!valid_op(op)) return vInvalidArgument;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollAllReduce, count, dt, f.aligned16, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollAllReduce, count, dt, p);
+    if (p.algo == vAlgoRing)
+        return launch_ring_plan(c, vCollAllReduce, send, recv, count, dt, op, dt, 0, false, 1.0f, p, stream);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, count);
+    return finish_launch(c, vc::launch_allreduce_onepass(a, dt, op, p.vectorized != 0, p.gridCtas,
+                                                         p.threadsPerCta, stream), stream, "allreduce");
+}
+
+static vResult_t reduce_scatter_impl(const void* const* send, void* const* recv, size_t rc,
+                                     vDataType_t dt, vRedOp_t op, vDataType_t outType, bool hasScale,
+                                     float scale, vcomm_t c, cudaStream_t stream) {
+    Front f = front(c, send, recv, rc, dt, 0, true);
+    if (f.res != vSuccess || rc == 0) return f.res;
+    if (!valid_op(op)) return vInvalidArgument;
+    if (outType != dt && !(outType == vFloat32 && (dt == vFloat16 || dt == vBFloat16))) return vInvalidArgument;
+    for (int r = 0; r < c->nRanks; r++)
+        if (!ptr_aligned(recv[r], elem_size(outType))) return vInvalidArgument;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollReduceScatter, rc, dt, f.aligned16, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollReduceScatter, rc, dt, p);
+    if (p.algo == vAlgoRing)
+        return launch_ring_plan(c, vCollReduceScatter, send, recv, rc, dt, op, outType, 0, hasScale, scale, p,
+                                stream);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, rc * (size_t)c->nRanks);
+    a.hasScale = hasScale ? 1 : 0;
+    a.scale = scale;
+    return finish_launch(c, vc::launch_reduce_scatter_onepass(a, dt, op, outType, p.vectorized != 0,
+                                                              p.gridCtas, p.threadsPerCta, stream),
+                         stream, "reduce_scatter");
+}
+
+vResult_t vReduceScatter(const void* const* send, void* const* recv, size_t recvcount, vDataType_t dt,
+                         vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    return reduce_scatter_impl(send, recv, recvcount, dt, op, dt, false, 1.0f, c, stream);
+}
+
+vResult_t vReduceScatterScaleCast(const void* const* send, void* const* recv, size_t recvcount,
+                                  vDataType_t dt, vRedOp_t op, vDataType_t outType, float scale,
+                                  vcomm_t c, cudaStream_t stream) {
+    if (dt == vInt32) return vInvalidArgument;
+    return reduce_scatter_impl(send, recv, recvcount, dt, op, outType, true, scale, c, stream);
+}
+
+vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcount, vDataType_t dt,
+                     vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    (void)op;
+    Front f = front(c, send, recv, sendcount, dt, 0, true);
+    if (f.res != vSuccess || sendcount == 0) return f.res;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollAllGather, sendcount, dt, f.aligned16, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollAllGather, sendcount, dt, p);
+    if (p.algo == vAlgoRing)
+        return launch_ring_plan(c, vCollAllGather, send, recv, sendcount, dt, vSum, dt, 0, false, 1.0f, p, stream);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, sendcount);
+    return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vectorized != 0, p.gridCtas,
+                                                         p.threadsPerCta, stream), stream, "allgather");
+}
+
+vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
+                     vRedOp_t op, int root, vcomm_t c, cudaStream_t stream) {
+    (void)op;
+    if (!comm_ok(c)) return vInvalidArgument;
+    if (root < 0 || root >= c->nRanks) return vInvalidArgument;
+    Front f = front(c, send, recv, count, dt, root, false);
+    if (f.res != vSuccess || count == 0) return f.res;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollBroadcast, count, dt, f.aligned16, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollBroadcast, count, dt, p);
+    if (p.algo == vAlgoRing) {
+        const void* sends[VCOMM_MAX_RANKS];
+        for (int i = 0; i < c->nRanks; i++) sends[i] = send[i];
+        return launch_ring_plan(c, vCollBroadcast, sends, recv, count, dt, vSum, dt, root, false, 1.0f, p, stream);
+    }
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, count);
+    a.root = root;
+    return finish_launch(c, vc::launch_broadcast_onepass(a, (int)elem_size(dt), p.vectorized != 0, p.gridCtas,
+                                                         p.threadsPerCta, stream), stream, "broadcast");
+}
+
+vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
+                    vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    (void)op;
+    Front f = front(c, send, recv, count, dt, 0, true);
+    if (f.res != vSuccess || count == 0) return f.res;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollAllToAll, count, dt, f.aligned16, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollAllToAll, count, dt, p);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, count);
+    return finish_launch(c, vc::launch_alltoall_onepass(a, (int)elem_size(dt), p.vectorized != 0, p.gridCtas,
+                                                        p.threadsPerCta, stream), stream, "alltoall");
+}
+
+vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* counts,
+                     const int32_t* sdispls, const int32_t* rdispls, vDataType_t dt, vcomm_t c,
+                     cudaStream_t stream) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    vResult_t s = sticky(c);
+    if (s != vSuccess) return s;
+    const size_t esz = elem_size(dt);
+    if (esz == 0 || !counts || !sdispls || !rdispls) return vInvalidArgument;
+    int aligned16 = 0;
+    vResult_t r = check_ptrs(c, send, recv, esz, 0, true, &aligned16);
+    if (r != vSuccess) return r;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    r = make_plan(c, vCollAllToAllv, 0, dt, aligned16, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollAllToAllv, 0, dt, p);
+    vc::A2AvArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int i = 0; i < c->nRanks; i++) {
+        a.send[i] = send[i];
+        a.recv[i] = recv[i];
+    }
+    a.counts = counts;
+    a.sdispls = sdispls;
+    a.rdispls = rdispls;
+    a.nRanks = c->nRanks;
+    a.elemSize = (int)esz;
+    a.tileBytes = 64 * 1024;
+    a.status = c->statusDev;
+    a.statusHost = c->statusHostDev;
+    return finish_launch(c, vc::launch_alltoallv(a, p.gridCtas, p.threadsPerCta, stream), stream, "alltoallv");
+}
+
+}  // extern "C"

@@ -1,0 +1,267 @@
+"""ctypes binding of libvcomm (include/vcomm.h): the same entry points, argument
+marshalling only.  Every collective runs in the library's CUDA kernels; there is no
+Python or CPU fallback -- if the library is missing or a call fails, an exception is
+raised.
+
+Buffers may be given as torch tensors or as integer device addresses; ``datatype`` as a
+torch dtype or a ``vDataType_t`` value; ``stream`` as a ``torch.cuda.Stream``, a raw
+``cudaStream_t`` integer, or ``None`` for torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+# ---- enums (values of include/vcomm.h) ---------------------------------------------------
+vSuccess, vUnhandledCudaError, vSystemError, vInternalError = 0, 1, 2, 3
+vInvalidArgument, vInvalidUsage, vTimeout, vInProgress, vAborted = 4, 5, 6, 7, 8
+vFloat32, vFloat16, vBFloat16, vInt32 = 0, 1, 2, 3
+vSum, vProd, vMin, vMax = 0, 1, 2, 3
+vProtoSimple, vProtoLL, vProtoLL128, vProtoAuto = 0, 1, 2, 3
+vAlgoAuto, vAlgoOnePass, vAlgoRing = 0, 1, 2
+vCollAllReduce, vCollReduceScatter, vCollAllGather = 0, 1, 2
+vCollBroadcast, vCollAllToAll, vCollAllToAllv = 3, 4, 5
+VCOMM_MAX_RANKS = 64
+
+RESULT_NAMES = {0: "vSuccess", 1: "vUnhandledCudaError", 2: "vSystemError", 3: "vInternalError",
+                4: "vInvalidArgument", 5: "vInvalidUsage", 6: "vTimeout", 7: "vInProgress",
+                8: "vAborted"}
+OPS = {"sum": vSum, "prod": vProd, "min": vMin, "max": vMax}
+PROTOCOLS = {"simple": vProtoSimple, "ll": vProtoLL, "ll128": vProtoLL128, "auto": vProtoAuto}
+ALGOS = {"auto": vAlgoAuto, "onepass": vAlgoOnePass, "ring": vAlgoRing}
+
+
+class VcommError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {RESULT_NAMES.get(code, code)}")
+
+
+class vPlanRequest_t(ctypes.Structure):
+    _fields_ = [("nRanks", ctypes.c_int), ("nChannels", ctypes.c_int), ("proto", ctypes.c_int),
+                ("algo", ctypes.c_int), ("coll", ctypes.c_int), ("datatype", ctypes.c_int),
+                ("count", ctypes.c_size_t), ("chunkBytes", ctypes.c_size_t),
+                ("aligned16", ctypes.c_int), ("smCount", ctypes.c_int), ("l2Bytes", ctypes.c_size_t)]
+
+
+class vPlanInfo_t(ctypes.Structure):
+    _fields_ = [("algo", ctypes.c_int), ("proto", ctypes.c_int), ("nChannels", ctypes.c_int),
+                ("ctasPerChannel", ctypes.c_int), ("gridCtas", ctypes.c_int),
+                ("threadsPerCta", ctypes.c_int), ("vectorized", ctypes.c_int),
+                ("launches", ctypes.c_int), ("blockElems", ctypes.c_size_t),
+                ("channelElems", ctypes.c_size_t), ("chunkElems", ctypes.c_size_t),
+                ("slotPayloadElems", ctypes.c_size_t), ("slotBytes", ctypes.c_size_t),
+                ("fifoBytes", ctypes.c_size_t), ("minBytes", ctypes.c_double),
+                ("busFactor", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+
+_SIGNATURES = {
+    "vcommInit": ([ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+    "vcommDestroy": ([ctypes.c_void_p], ctypes.c_int),
+    "vcommGetAsyncError": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "vcommAbort": ([ctypes.c_void_p], ctypes.c_int),
+    "vcommGetErrorString": ([ctypes.c_int], ctypes.c_char_p),
+    "vcommSetAlgo": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "vcommSetProtocol": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "vcommSetChunkBytes": ([ctypes.c_void_p, ctypes.c_size_t], ctypes.c_int),
+    "vcommSetTimeoutMs": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "vcommTestSetStallRank": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "vcommQueryPlan": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                        ctypes.POINTER(vPlanInfo_t)], ctypes.c_int),
+    "vPlanCompute": ([ctypes.POINTER(vPlanRequest_t), ctypes.POINTER(vPlanInfo_t)], ctypes.c_int),
+    "vPlanChannelRange": ([ctypes.POINTER(vPlanInfo_t), ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                           ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "vAllReduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vReduceScatter": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                        ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vReduceScatterScaleCast": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vAllGather": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vBroadcast": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vAllToAll": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vAllToAllv": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                    ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libvcomm.so (built in-tree by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libvcomm.so is not built ({path}); run "
+                               "collective_communication_virtual_gb300.build.build() first")
+        L = ctypes.CDLL(path)
+        for name, (args, res) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes, f.restype = args, res
+        _lib = L
+    return _lib
+
+
+# ---- marshalling helpers -------------------------------------------------------------------
+
+def _dtype_code(dt) -> int:
+    if isinstance(dt, int):
+        return dt
+    import torch
+    return {torch.float32: vFloat32, torch.float16: vFloat16, torch.bfloat16: vBFloat16,
+            torch.int32: vInt32}[dt]
+
+
+def _op_code(op) -> int:
+    return OPS[op] if isinstance(op, str) else int(op)
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _ptr_array(bufs):
+    arr = (ctypes.c_void_p * len(bufs))()
+    for i, b in enumerate(bufs):
+        arr[i] = _addr(b)
+    return arr
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str) -> None:
+    if code != vSuccess:
+        raise VcommError(code, where)
+
+
+# ---- the C ABI, one wrapper per entry point --------------------------------------------------
+
+def vcommInit(n_ranks: int, n_channels: int = 1, protocol=vProtoSimple) -> ctypes.c_void_p:
+    comm = ctypes.c_void_p()
+    proto = PROTOCOLS[protocol] if isinstance(protocol, str) else protocol
+    _check(lib().vcommInit(ctypes.byref(comm), n_ranks, n_channels, proto), "vcommInit")
+    return comm
+
+
+def vcommDestroy(comm) -> None:
+    _check(lib().vcommDestroy(comm), "vcommDestroy")
+
+
+def vcommGetAsyncError(comm) -> int:
+    err = ctypes.c_int(0)
+    _check(lib().vcommGetAsyncError(comm, ctypes.byref(err)), "vcommGetAsyncError")
+    return err.value
+
+
+def vcommAbort(comm) -> None:
+    _check(lib().vcommAbort(comm), "vcommAbort")
+
+
+def vcommGetErrorString(code: int) -> str:
+    return lib().vcommGetErrorString(code).decode()
+
+
+def vcommSetAlgo(comm, algo) -> None:
+    _check(lib().vcommSetAlgo(comm, ALGOS[algo] if isinstance(algo, str) else algo), "vcommSetAlgo")
+
+
+def vcommSetProtocol(comm, protocol) -> None:
+    proto = PROTOCOLS[protocol] if isinstance(protocol, str) else protocol
+    _check(lib().vcommSetProtocol(comm, proto), "vcommSetProtocol")
+
+
+def vcommSetChunkBytes(comm, chunk_bytes: int) -> None:
+    _check(lib().vcommSetChunkBytes(comm, chunk_bytes), "vcommSetChunkBytes")
+
+
+def vcommSetTimeoutMs(comm, ms: int) -> None:
+    _check(lib().vcommSetTimeoutMs(comm, ms), "vcommSetTimeoutMs")
+
+
+def vcommTestSetStallRank(comm, rank: int) -> None:
+    _check(lib().vcommTestSetStallRank(comm, rank), "vcommTestSetStallRank")
+
+
+def vcommQueryPlan(comm, coll: int, count: int, datatype, aligned16: bool = True) -> dict:
+    info = vPlanInfo_t()
+    _check(lib().vcommQueryPlan(comm, coll, count, _dtype_code(datatype), int(aligned16),
+                                ctypes.byref(info)), "vcommQueryPlan")
+    return info.as_dict()
+
+
+def vPlanCompute(**req) -> vPlanInfo_t:
+    q = vPlanRequest_t()
+    for k, v in req.items():
+        setattr(q, k, v)
+    info = vPlanInfo_t()
+    _check(lib().vPlanCompute(ctypes.byref(q), ctypes.byref(info)), "vPlanCompute")
+    return info
+
+
+def vPlanChannelRange(plan: vPlanInfo_t, count: int, channel: int, block: int) -> tuple[int, int]:
+    lo, hi = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().vPlanChannelRange(ctypes.byref(plan), count, channel, block, ctypes.byref(lo),
+                                   ctypes.byref(hi)), "vPlanChannelRange")
+    return lo.value, hi.value
+
+
+def vAllReduce(sendbuffs, recvbuffs, count: int, datatype, op, comm, stream=None) -> None:
+    _check(lib().vAllReduce(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+                            _op_code(op), comm, _stream(stream)), "vAllReduce")
+
+
+def vReduceScatter(sendbuffs, recvbuffs, recvcount: int, datatype, op, comm, stream=None) -> None:
+    _check(lib().vReduceScatter(_ptr_array(sendbuffs), _ptr_array(recvbuffs), recvcount,
+                                _dtype_code(datatype), _op_code(op), comm, _stream(stream)), "vReduceScatter")
+
+
+def vReduceScatterScaleCast(sendbuffs, recvbuffs, recvcount: int, datatype, op, out_type, scale: float,
+                            comm, stream=None) -> None:
+    _check(lib().vReduceScatterScaleCast(_ptr_array(sendbuffs), _ptr_array(recvbuffs), recvcount,
+                                         _dtype_code(datatype), _op_code(op), _dtype_code(out_type),
+                                         ctypes.c_float(scale), comm, _stream(stream)),
+           "vReduceScatterScaleCast")
+
+
+def vAllGather(sendbuffs, recvbuffs, sendcount: int, datatype, op, comm, stream=None) -> None:
+    _check(lib().vAllGather(_ptr_array(sendbuffs), _ptr_array(recvbuffs), sendcount, _dtype_code(datatype),
+                            _op_code(op), comm, _stream(stream)), "vAllGather")
+
+
+def vBroadcast(sendbuffs, recvbuffs, count: int, datatype, op, root: int, comm, stream=None) -> None:
+    _check(lib().vBroadcast(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+                            _op_code(op), root, comm, _stream(stream)), "vBroadcast")
+
+
+def vAllToAll(sendbuffs, recvbuffs, count: int, datatype, op, comm, stream=None) -> None:
+    _check(lib().vAllToAll(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+                           _op_code(op), comm, _stream(stream)), "vAllToAll")
+
+
+def vAllToAllv(sendbuffs, recvbuffs, counts, sdispls, rdispls, datatype, comm, stream=None) -> None:
+    _check(lib().vAllToAllv(_ptr_array(sendbuffs), _ptr_array(recvbuffs), _addr(counts), _addr(sdispls),
+                            _addr(rdispls), _dtype_code(datatype), comm, _stream(stream)), "vAllToAllv")

@@ -1,0 +1,252 @@
+/*
+ * vcomm.h -- collectives among N virtual ranks that all live in one GPU's memory.
+ *
+ * A communicator (vcomm_t) stands for N ranks whose send and receive buffers are
+ * ordinary device allocations on the current GPU.  Each call moves or reduces data
+ * between those buffers entirely on that GPU; no other GPU, process or network is
+ * involved and no NCCL call is made.
+ *
+ * The interface follows the NCCL calls described in the NCCL book (aireadcode.com),
+ * section 2.1 (communicator, async error) and chapter 6 (ncclAllReduce(sendbuff,
+ * recvbuff, count, datatype, op, comm, stream) -> ncclInfo -> ncclEnqueueCheck), with
+ * one change that the virtual ranks force: every rank's buffer is named at once, so
+ * sendbuffs / recvbuffs are host arrays of N device pointers, rank r at index r.
+ * The collectives' meaning is the collective table of "AI Systems Performance
+ * Engineering (3)" (all-reduce, reduce-scatter, all-gather, broadcast, all-to-all).
+ *
+ * Stream contract ("NCCL Expert Course 29: ProcessGroupNCCL, Stream, Event and
+ * Work"): every collective is enqueued on the caller's stream and returns as soon as
+ * it is enqueued.  The caller keeps the device buffers alive and unmodified until the
+ * stream work completes.  The host pointer arrays and tables are copied before the
+ * call returns and may be freed right after it (as ncclInfo copies the user's config,
+ * NCCL book chapter 6).
+ *
+ * Errors: a call returns vInvalidArgument for bad arguments and launches nothing.
+ * Failures found on the device (a staged transfer that waits past its deadline, an
+ * abort, a bad all-to-all table) are recorded in the communicator's sticky async
+ * error (NCCL book section 2.1, asyncResult / ncclCommGetAsyncError); every later
+ * call on that communicator returns that error without launching, and the
+ * communicator must be destroyed.
+ *
+ * Threading: a communicator is used by one host thread at a time.
+ */
+#ifndef VCOMM_H
+#define VCOMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle, declared the same way cuda_runtime_api.h does. */
+typedef struct CUstream_st* cudaStream_t;
+
+#define VCOMM_MAX_RANKS 64
+#define VCOMM_MAX_CHANNELS 64
+
+typedef struct vcomm* vcomm_t;
+
+/* Result codes.  vInvalidUsage = 5 matches NCCL's ncclInvalidUsage ("NCCL Expert
+ * Course 17", duplicate-device probe, "code=5"). */
+typedef enum {
+    vSuccess = 0,
+    vUnhandledCudaError = 1, /* a CUDA runtime call failed (no device, launch error, ...) */
+    vSystemError = 2,        /* host allocation failed */
+    vInternalError = 3,
+    vInvalidArgument = 4,    /* bad pointer, size, type, op, root or communicator */
+    vInvalidUsage = 5,       /* valid arguments the communicator cannot serve, e.g. a staged
+                                protocol whose CTAs cannot all be resident at once */
+    vTimeout = 6,            /* a staged transfer waited past its deadline (async) */
+    vInProgress = 7,
+    vAborted = 8             /* vcommAbort stopped a running staged transfer (async) */
+} vResult_t;
+
+typedef enum { vFloat32 = 0, vFloat16 = 1, vBFloat16 = 2, vInt32 = 3 } vDataType_t;
+
+/* Reductions.  sum and prod on fp16/bf16 widen both operands to fp32, apply one fp32
+ * operation (round to nearest even) and round back to the storage type; int32 sum and
+ * prod wrap modulo 2^32; min/max keep the running partial unless the next element
+ * compares strictly below/above it. */
+typedef enum { vSum = 0, vProd = 1, vMin = 2, vMax = 3 } vRedOp_t;
+
+/* Staging protocols of the ring path (NCCL book section 2.4, "protocol"):
+ * Simple moves raw data through FIFO slots guarded by head/tail counters; LL packs
+ * 4 bytes of data with a 4-byte flag in every 8-byte word (half the bandwidth); LL128
+ * carries 120 bytes of data and an 8-byte flag in every 128-byte line.
+ * vProtoAuto lets the planner choose. */
+typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 } vProto_t;
+
+/* Algorithms.  vAlgoOnePass: one kernel reads every rank's buffer once and writes
+ * every output once (the virtual-rank counterpart of NCCL's symmetric-memory kernels,
+ * NCCL book chapter 5 section 5).  vAlgoRing: the literal ring of the NCCL book
+ * section 2.3, N-1 reduce-scatter steps then N-1 all-gather steps, each hop staged
+ * through a device FIFO with the communicator's protocol.  Both give identical bits.
+ * vAlgoAuto lets the planner choose. */
+typedef enum { vAlgoAuto = 0, vAlgoOnePass = 1, vAlgoRing = 2 } vAlgo_t;
+
+typedef enum {
+    vCollAllReduce = 0, vCollReduceScatter = 1, vCollAllGather = 2,
+    vCollBroadcast = 3, vCollAllToAll = 4, vCollAllToAllv = 5
+} vColl_t;
+
+/* ------------------------------------------------------------------------------- */
+/* Communicator lifecycle                                                           */
+/* ------------------------------------------------------------------------------- */
+
+/* Create a communicator of nRanks virtual ranks on the current CUDA device.
+ * nRanks in [1, VCOMM_MAX_RANKS]; nChannels in [1, VCOMM_MAX_CHANNELS] is the number
+ * of channels (independent CTA groups, each owning a contiguous sub-range of every
+ * rank's block: NCCL book section 2.2, "each channel handles count/nChannels
+ * elements"); protocol is the ring path's staging.  Out-of-range values give
+ * vInvalidArgument and *comm is left NULL (as ncclCommInitRankDev rejects nranks < 1
+ * with ncclInvalidArgument, "NCCL Expert Course 17").  No usable device gives
+ * vUnhandledCudaError.  The communicator owns a small status block in pinned host
+ * memory and, once a ring transfer is planned, its staging FIFOs in device memory.
+ * Environment (read once here): VCOMM_ALGO=auto|onepass|ring, VCOMM_CHUNK_BYTES,
+ * VCOMM_TIMEOUT_MS, VCOMM_DEBUG=INFO (prints every plan to stderr). */
+vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol);
+
+/* Wait for the communicator's last enqueued work, then free everything it owns.
+ * A NULL or already destroyed communicator gives vInvalidArgument. */
+vResult_t vcommDestroy(vcomm_t comm);
+
+/* Store the sticky asynchronous error (vSuccess if none) in *asyncError.  Reads host
+ * memory that the kernels write; it does not synchronize any stream. */
+vResult_t vcommGetAsyncError(vcomm_t comm, vResult_t* asyncError);
+
+/* Ask running and future ring transfers of this communicator to stop: their waits
+ * return and the sticky error becomes vAborted. */
+vResult_t vcommAbort(vcomm_t comm);
+
+const char* vcommGetErrorString(vResult_t result);
+
+/* Tuning knobs (host only, take effect for later calls).  chunkBytes is the ring
+ * path's bytes per rank per chunk (one chunk = 4 FIFO slots, one slice = 2 slots;
+ * NCCL book chapter 6, ALLREDUCE_CHUNKSTEPS / ALLREDUCE_SLICESTEPS); it must be a
+ * power of two in [4 KiB, 64 MiB], or 0 for the planner's default (the largest power
+ * of two <= 1 MiB that keeps all FIFOs within half of L2).  timeoutMs bounds every device-side wait (>= 1). */
+vResult_t vcommSetAlgo(vcomm_t comm, vAlgo_t algo);
+vResult_t vcommSetProtocol(vcomm_t comm, vProto_t protocol);
+vResult_t vcommSetChunkBytes(vcomm_t comm, size_t chunkBytes);
+vResult_t vcommSetTimeoutMs(vcomm_t comm, int timeoutMs);
+
+/* ------------------------------------------------------------------------------- */
+/* Collectives.  sendbuffs / recvbuffs: host arrays of nRanks device pointers.       */
+/* Any element-aligned pointer is accepted; when every pointer and the sizes allow   */
+/* 16-byte vectors the vector path runs, otherwise an element-wise path; the output  */
+/* bits are the same.  count == 0 returns vSuccess and launches nothing (NCCL book   */
+/* chapter 6, taskAppend).  With nRanks == 1 every collective is a copy.             */
+/* ------------------------------------------------------------------------------- */
+
+/* recvbuffs[r][e] = the reduction over all ranks of sendbuffs[.][e], e < count, for
+ * every rank r.  Element e belongs to block b = e / B with
+ * B = alignUp(ceil(count / nRanks), 16 / elemSize) (the tail-chunk rule of
+ * RingARAlgorithm::getNextSendAddr, NCCL book section 2.3), and block b is reduced in
+ * ring order: ranks b+1, b+2, ..., b (mod nRanks), each partial rounded to the data
+ * type.  In place (sendbuffs[r] == recvbuffs[r]) is allowed; other overlap is not. */
+vResult_t vAllReduce(const void* const* sendbuffs, void* const* recvbuffs, size_t count,
+                     vDataType_t datatype, vRedOp_t op, vcomm_t comm, cudaStream_t stream);
+
+/* sendbuffs[r] holds nRanks * recvcount elements; recvbuffs[r][t] = the reduction of
+ * sendbuffs[.][r * recvcount + t] in ring order ranks r+1, ..., r.  In place means
+ * recvbuffs[r] == sendbuffs[r] + r * recvcount. */
+vResult_t vReduceScatter(const void* const* sendbuffs, void* const* recvbuffs, size_t recvcount,
+                         vDataType_t datatype, vRedOp_t op, vcomm_t comm, cudaStream_t stream);
+
+/* vReduceScatter with a fused epilogue: recvbuffs[r][t] = (float)acc * scale computed
+ * in fp32 (round to nearest even) and stored as outType, which is vFloat32 or the
+ * input type.  datatype must be a floating type.  For gradient averaging scale is
+ * 1/nRanks ("AI Systems Performance Engineering (3)", p.grad /= world_size). */
+vResult_t vReduceScatterScaleCast(const void* const* sendbuffs, void* const* recvbuffs,
+                                  size_t recvcount, vDataType_t datatype, vRedOp_t op,
+                                  vDataType_t outType, float scale, vcomm_t comm,
+                                  cudaStream_t stream);
+
+/* recvbuffs[r][s * sendcount + t] = sendbuffs[s][t] for every r.  op is ignored (the
+ * data is moved as bytes).  In place means sendbuffs[r] == recvbuffs[r] + r * sendcount. */
+vResult_t vAllGather(const void* const* sendbuffs, void* const* recvbuffs, size_t sendcount,
+                     vDataType_t datatype, vRedOp_t op, vcomm_t comm, cudaStream_t stream);
+
+/* recvbuffs[r][0..count) = sendbuffs[root][0..count) for every r; root in [0, nRanks).
+ * Only sendbuffs[root] is read; the other entries may be NULL.  op is ignored. */
+vResult_t vBroadcast(const void* const* sendbuffs, void* const* recvbuffs, size_t count,
+                     vDataType_t datatype, vRedOp_t op, int root, vcomm_t comm,
+                     cudaStream_t stream);
+
+/* Uniform all-to-all: count elements per block, nRanks blocks per buffer;
+ * recvbuffs[j][i * count + t] = sendbuffs[i][j * count + t].  op is ignored.
+ * Send and receive buffers must not overlap. */
+vResult_t vAllToAll(const void* const* sendbuffs, void* const* recvbuffs, size_t count,
+                    vDataType_t datatype, vRedOp_t op, vcomm_t comm, cudaStream_t stream);
+
+/* Variable all-to-all.  counts, sdispls and rdispls are DEVICE arrays of nRanks *
+ * nRanks int32 values, in elements: counts[i * nRanks + j] elements go from
+ * sendbuffs[i] + sdispls[i * nRanks + j] to recvbuffs[j] + rdispls[j * nRanks + i].
+ * The caller guarantees that every block lies inside its buffers.  A negative entry
+ * makes the kernel skip that block and sets the sticky error vInvalidArgument.
+ * Send and receive buffers must not overlap. */
+vResult_t vAllToAllv(const void* const* sendbuffs, void* const* recvbuffs, const int32_t* counts,
+                     const int32_t* sdispls, const int32_t* rdispls, vDataType_t datatype,
+                     vcomm_t comm, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------- */
+/* Planner (host only; needs no GPU)                                                */
+/* ------------------------------------------------------------------------------- */
+
+typedef struct {
+    int nRanks, nChannels;
+    int proto;                 /* vProto_t requested */
+    int algo;                  /* vAlgo_t requested */
+    int coll;                  /* vColl_t */
+    int datatype;              /* vDataType_t */
+    size_t count;              /* elements: AR/BC count, RS recvcount, AG sendcount, A2A block */
+    size_t chunkBytes;         /* ring chunk bytes per rank (0 = default) */
+    int aligned16;             /* 1 if every buffer pointer is 16-byte aligned */
+    int smCount;               /* streaming multiprocessors of the device */
+    size_t l2Bytes;            /* L2 cache size of the device */
+} vPlanRequest_t;
+
+typedef struct {
+    int algo;                  /* vAlgo_t chosen: vAlgoOnePass or vAlgoRing */
+    int proto;                 /* vProto_t used by the ring path */
+    int nChannels;
+    int ctasPerChannel;        /* one-pass: CTAs in each channel's group */
+    int gridCtas;              /* CTAs launched */
+    int threadsPerCta;
+    int vectorized;            /* 1 when the 16-byte vector path runs */
+    int launches;              /* kernel launches of the call */
+    size_t blockElems;         /* B: elements of one rank block (AR rule, or RS/AG block) */
+    size_t channelElems;       /* elements of each block that one channel owns */
+    size_t chunkElems;         /* ring: elements per block per chunk */
+    size_t slotPayloadElems;   /* ring: data elements carried by one FIFO slot */
+    size_t slotBytes;          /* ring: bytes of one FIFO slot (payload + flags) */
+    size_t fifoBytes;          /* ring: bytes of one (channel, rank) FIFO, 8 slots */
+    double minBytes;           /* algorithmic minimum HBM bytes read + written */
+    double busFactor;          /* busBW = algBW * busFactor (nSteps / nRanks) */
+} vPlanInfo_t;
+
+/* Compute the plan a collective with these parameters would run.  Pure host
+ * arithmetic; returns vInvalidArgument for out-of-range requests. */
+vResult_t vPlanCompute(const vPlanRequest_t* request, vPlanInfo_t* plan);
+
+/* The element range [*lo, *hi) of block `block` owned by `channel` under `plan`
+ * (empty when *lo == *hi).  count is the request's total element count per rank
+ * (AR count; nRanks * recvcount for RS).  Host only. */
+vResult_t vPlanChannelRange(const vPlanInfo_t* plan, size_t count, int channel, int block,
+                            size_t* lo, size_t* hi);
+
+/* Test hook for failure detection: rank `rank` of every later ring transfer never
+ * starts (its CTAs return at once), so its neighbours' bounded waits run out and the
+ * transfer ends with the sticky error vTimeout.  -1 turns the hook off. */
+vResult_t vcommTestSetStallRank(vcomm_t comm, int rank);
+
+/* vPlanCompute for this communicator's device and settings. */
+vResult_t vcommQueryPlan(vcomm_t comm, vColl_t coll, size_t count, vDataType_t datatype,
+                         int aligned16, vPlanInfo_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VCOMM_H */

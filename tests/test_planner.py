@@ -1,0 +1,137 @@
+"""Host planner (vPlanCompute / vPlanChannelRange), no GPU needed."""
+from __future__ import annotations
+
+import pytest
+
+import oracle
+from collective_communication_virtual_gb300 import build, vcomm as V
+
+ESZ = {V.vFloat32: 4, V.vFloat16: 2, V.vBFloat16: 2, V.vInt32: 4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    V.lib()
+
+
+def plan(**kw):
+    req = dict(nRanks=8, nChannels=1, proto=V.vProtoSimple, algo=V.vAlgoAuto, coll=V.vCollAllReduce,
+               datatype=V.vFloat32, count=1024, chunkBytes=0, aligned16=1, smCount=152,
+               l2Bytes=126 << 20)
+    req.update(kw)
+    return V.vPlanCompute(**req)
+
+
+def covered(p, total, nblocks, nch):
+    seen = bytearray(total)
+    for ch in range(nch):
+        for b in range(nblocks):
+            lo, hi = V.vPlanChannelRange(p, total, ch, b)
+            for e in range(lo, hi):
+                assert not seen[e], (ch, b, e)
+                seen[e] = 1
+    return all(seen)
+
+
+@pytest.mark.parametrize("dt", [V.vFloat32, V.vBFloat16])
+def test_allreduce_partition_covers_every_element_once(dt):
+    for n in (1, 2, 3, 4, 7, 8):
+        for count in (0, 1, 5, 17, 1000, 4099, 65_537):
+            for nch in (1, 2, 3, 8, 16):
+                p = plan(nRanks=n, nChannels=nch, count=count, datatype=dt)
+                assert p.blockElems == oracle.block_elems(count, n, ESZ[dt])
+                assert covered(p, count, n, nch), (n, count, nch)
+
+
+def test_allreduce_blocks_and_channel_ranges_start_on_16_bytes():
+    for dt in (V.vFloat32, V.vFloat16):
+        for n, count, nch in [(8, 16 << 20, 32), (3, 100_003, 5), (8, 4099, 16)]:
+            p = plan(nRanks=n, nChannels=nch, count=count, datatype=dt)
+            for ch in range(nch):
+                for b in range(n):
+                    lo, hi = V.vPlanChannelRange(p, count, ch, b)
+                    if hi > lo:
+                        assert (lo * ESZ[dt]) % 16 == 0
+
+
+def test_reduce_scatter_and_copies_partition():
+    for coll, nblocks in [(V.vCollReduceScatter, None), (V.vCollAllGather, None),
+                          (V.vCollBroadcast, 1)]:
+        for n, count, nch in [(8, 4096, 8), (5, 3001, 3), (2, 1, 4)]:
+            p = plan(coll=coll, nRanks=n, nChannels=nch, count=count)
+            nb = nblocks or n
+            assert covered(p, count * nb, nb, nch)
+
+
+def test_vector_path_requires_aligned_blocks():
+    assert plan(coll=V.vCollReduceScatter, count=4096).vectorized == 1
+    assert plan(coll=V.vCollReduceScatter, count=4097).vectorized == 0
+    assert plan(coll=V.vCollAllReduce, count=4097).vectorized == 1      # only the tail is ragged
+    assert plan(coll=V.vCollAllReduce, count=4096, aligned16=0).vectorized == 0
+    assert plan(coll=V.vCollAllGather, count=8, datatype=V.vBFloat16).vectorized == 1
+    assert plan(coll=V.vCollAllGather, count=12, datatype=V.vBFloat16).vectorized == 0
+
+
+def test_ring_geometry_follows_the_step_constants():
+    for proto, payload in [(V.vProtoSimple, 1.0), (V.vProtoLL, 0.5), (V.vProtoLL128, 120 / 128)]:
+        p = plan(algo=V.vAlgoRing, proto=proto, count=1 << 24, chunkBytes=1 << 20)
+        assert p.algo == V.vAlgoRing and p.proto == proto
+        assert p.slotBytes * 4 == 1 << 20                 # a chunk is 4 slots
+        assert p.fifoBytes == 8 * p.slotBytes             # NCCL_STEPS = 8
+        assert p.slotPayloadElems * 4 == int(p.slotBytes * payload)
+        assert p.chunkElems == 4 * p.slotPayloadElems
+        assert p.gridCtas == 8 and p.ctasPerChannel == 8
+
+
+def test_default_chunk_keeps_fifos_within_half_of_l2():
+    l2 = 126 << 20
+    for n, nch in [(8, 1), (8, 8), (8, 32), (4, 64)]:
+        p = plan(algo=V.vAlgoRing, nRanks=n, nChannels=nch, count=1 << 26, l2Bytes=l2)
+        assert p.fifoBytes * n * nch <= l2 // 2 or p.slotBytes * 4 == 16384
+
+
+def test_auto_protocol_by_size():
+    small = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=1024)
+    mid = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=8 * 64 * 1024)
+    big = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=8 << 20)
+    assert (small.proto, mid.proto, big.proto) == (V.vProtoLL, V.vProtoLL128, V.vProtoSimple)
+
+
+def test_one_rank_and_alltoall_always_one_pass():
+    assert plan(nRanks=1, algo=V.vAlgoRing).algo == V.vAlgoOnePass
+    assert plan(coll=V.vCollAllToAll, algo=V.vAlgoRing).algo == V.vAlgoOnePass
+    assert plan(coll=V.vCollAllToAllv, algo=V.vAlgoRing).algo == V.vAlgoOnePass
+
+
+def test_traffic_and_bus_factor():
+    n, count = 8, 16 << 20
+    S = count * 4
+    p = plan(nRanks=n, count=count)
+    assert p.minBytes == 2 * n * S and p.busFactor == pytest.approx(2 * (n - 1) / n)
+    p = plan(nRanks=n, count=count, coll=V.vCollReduceScatter)
+    assert p.minBytes == n * n * S + n * S and p.busFactor == pytest.approx((n - 1) / n)
+    p = plan(nRanks=n, count=count, coll=V.vCollAllGather)
+    assert p.minBytes == n * S + n * n * S
+    p = plan(nRanks=n, count=count, coll=V.vCollBroadcast)
+    assert p.minBytes == S + n * S
+    p = plan(nRanks=n, count=count, coll=V.vCollAllToAll)
+    assert p.minBytes == 2 * n * n * S
+
+
+def test_grid_is_about_two_ctas_per_sm_and_never_idle():
+    p = plan(count=16 << 20, nChannels=1)
+    assert p.gridCtas == 2 * 152
+    p = plan(count=16 << 20, nChannels=32)
+    assert p.nChannels * p.ctasPerChannel == p.gridCtas and p.gridCtas >= 2 * 152
+    p = plan(count=256)                                  # 1 KiB per rank: one CTA is enough
+    assert p.gridCtas == 1
+
+
+def test_bad_requests():
+    for kw in [dict(nRanks=0), dict(nRanks=65), dict(nChannels=0), dict(nChannels=65), dict(coll=9),
+               dict(datatype=7), dict(proto=5), dict(algo=4), dict(chunkBytes=1000),
+               dict(chunkBytes=3 << 20)]:
+        with pytest.raises(V.VcommError) as e:
+            plan(**kw)
+        assert e.value.code == V.vInvalidArgument

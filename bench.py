@@ -99,6 +99,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
     def __exit__(self, *exc):
         if self.proc:
             self.proc.terminate()
@@ -185,6 +190,15 @@ def time_allreduce(V, torch, comm, send, recv, count, steps, warmup, stream):
     return start.elapsed_time(stop) / 1e3 / steps
 
 
+def load(V, torch, comm, send, recv, stream, seconds):
+    """Untimed all-reduces for about `seconds` (keeps clocks at their loaded value)."""
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        for _ in range(50):
+            V.vAllReduce(send, recv, COUNT, torch.float32, "sum", comm, stream)
+        torch.cuda.synchronize()
+
+
 def cpu_baseline_sample(torch):
     import oracle
     from collective_communication_virtual_gb300 import inputs
@@ -231,7 +245,13 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # The timed region is milliseconds long, far shorter than nvidia-smi's 200 ms
+        # sampling period, so the GPU is kept under the same load (untimed all-reduces)
+        # for about a second on either side of it; the samples bracket the timed steps.
+        clocks.wait_first()
+        load(V, torch, comm, send, recv, stream, seconds=1.0)
         t = time_allreduce(V, torch, comm, send, recv, COUNT, args.steps, args.warmup, stream)
+        load(V, torch, comm, send, recv, stream, seconds=0.5)
         if world > 1:
             tt = torch.tensor([t], device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)

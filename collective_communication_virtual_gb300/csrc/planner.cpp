@@ -103,8 +103,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         // channels; never more CTAs than a channel has vectors to move.
         p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
         p->threadsPerCta = vc::kOnePassThreads;
+        // Round down so the grid never spills into a second, mostly idle wave.
         const int target = 2 * smCount;
-        int per = std::max(1, (int)div_up((size_t)target, (size_t)q->nChannels));
+        int per = std::max(1, target / q->nChannels);
         size_t work = 0;    // vectors (or elements) one channel moves per block pass
         if (q->coll == vCollAllToAllv) {
             work = (size_t)1 << 40;

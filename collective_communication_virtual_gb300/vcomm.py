@@ -92,6 +92,8 @@ _SIGNATURES = {
                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vAllToAllv": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vAllReduceNoAlloc": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
 }
 
 
@@ -265,3 +267,12 @@ def vAllToAll(sendbuffs, recvbuffs, count: int, datatype, op, comm, stream=None)
 def vAllToAllv(sendbuffs, recvbuffs, counts, sdispls, rdispls, datatype, comm, stream=None) -> None:
     _check(lib().vAllToAllv(_ptr_array(sendbuffs), _ptr_array(recvbuffs), _addr(counts), _addr(sdispls),
                             _addr(rdispls), _dtype_code(datatype), comm, _stream(stream)), "vAllToAllv")
+
+
+def vAllReduceNoAlloc(sendbuffs, recvbuffs, count: int, datatype, op, n_ranks: int, n_channels: int = 1,
+                      protocol=vProtoSimple, stream=None) -> None:
+    """The ring all-reduce that allocates nothing (see include/vcomm.h)."""
+    proto = PROTOCOLS[protocol] if isinstance(protocol, str) else protocol
+    _check(lib().vAllReduceNoAlloc(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+                                   _op_code(op), n_ranks, n_channels, proto, _stream(stream)),
+           "vAllReduceNoAlloc")

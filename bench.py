@@ -134,6 +134,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(t, dist=None, device=None):
+    """The slowest replica's time (the job's time); t itself on a single process."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt)
+
+
+def job_busbw(world, t_max):
+    """Whole-job busBW: every replica moves BYTES_PER_RANK per virtual rank per step."""
+    return world * BYTES_PER_RANK / t_max * bus_factor(N_RANKS) / 1e9
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -252,15 +267,10 @@ def run_ours(args):
         load(V, torch, comm, send, recv, stream, seconds=1.0)
         t = time_allreduce(V, torch, comm, send, recv, COUNT, args.steps, args.warmup, stream)
         load(V, torch, comm, send, recv, stream, seconds=0.5)
-        if world > 1:
-            tt = torch.tensor([t], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_max = float(tt)
-        else:
-            t_max = t
+        t_max = max_over_ranks(t, dist if world > 1 else None, dev)
     err = V.vcommGetAsyncError(comm)
     busbw_one = BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9
-    value = world * BYTES_PER_RANK / t_max * bus_factor(N_RANKS) / 1e9
+    value = job_busbw(world, t_max)
     achieved = plan["minBytes"] / t / 1e9
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

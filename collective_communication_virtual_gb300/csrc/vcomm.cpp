@@ -177,12 +177,24 @@ vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned1
     return vPlanCompute(&q, p);
 }
 
+bool stream_capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
 vResult_t finish_launch(vcomm* c, cudaError_t e, cudaStream_t stream, const char* what) {
     if (e != cudaSuccess) {
         c->hostError = vUnhandledCudaError;
         return cuda_fail(c, e, what);
     }
-    if (cudaEventRecord(c->lastEvent, stream) == cudaSuccess) c->eventRecorded = true;
+    // Track the last eager launch for vcommDestroy; launches being captured into a graph
+    // run when the graph does, which the caller orders.
+    if (!stream_capturing(stream) && cudaEventRecord(c->lastEvent, stream) == cudaSuccess)
+        c->eventRecorded = true;
     return vSuccess;
 }
 
@@ -236,14 +248,32 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
             std::fprintf(stderr, "vcomm: ring needs %d co-resident CTAs, device holds %d\n", p.gridCtas, maxCtas);
         return vInvalidUsage;
     }
-    vResult_t res = ensure_fifo(c, p);
-    if (res != vSuccess) return res;
-    c->epoch++;
-    if ((c->epoch & 0xFFu) == 0) {
-        // LL flags keep only the low byte of the epoch: clear stale flags when it wraps.
-        e = cudaMemsetAsync(c->fifo, 0, c->fifoCap, stream);
-        if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(fifo)");
+    const bool capturing = stream_capturing(stream);
+    unsigned int epoch;
+    if (capturing) {
+        // A captured launch replays with the arguments it was captured with, so it cannot
+        // carry a fresh epoch: the graph clears the control words and FIFOs itself before
+        // every replay and uses epoch 1, which eager launches never use.  FIFOs cannot be
+        // allocated during capture: an eager ring call of at least this size must come first.
+        const size_t need = (size_t)c->nChannels * c->nRanks * p.fifoBytes;
+        if (!c->ctrl || need > c->fifoCap) return vInvalidUsage;
+        const size_t ctrlBytes = (size_t)c->nChannels * c->nRanks * vc::kCtrlStride * sizeof(unsigned long long);
+        e = cudaMemsetAsync(c->ctrl, 0, ctrlBytes, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c->fifo, 0, need, stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(capture)");
+        epoch = 1;
+    } else {
+        vResult_t res = ensure_fifo(c, p);
+        if (res != vSuccess) return res;
         c->epoch++;
+        if ((c->epoch & 0xFFu) <= 1u) {
+            // LL flags keep only the low byte of the epoch: clear stale flags when it wraps.
+            // Low bytes 0 (cleared memory) and 1 (captured graphs) are never used here.
+            e = cudaMemsetAsync(c->fifo, 0, c->fifoCap, stream);
+            if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(fifo)");
+            c->epoch = (c->epoch & ~0xFFu) | 2u;
+        }
+        epoch = c->epoch;
     }
     vc::RingArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -270,8 +300,8 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
     a.slotBytes = p.slotBytes;
     a.fifo = c->fifo;
     a.ctrl = c->ctrl;
-    a.epochHi = (unsigned long long)c->epoch << 32;
-    a.llEpoch = (c->epoch & 0xFFu) << 24;
+    a.epochHi = (unsigned long long)epoch << 32;
+    a.llEpoch = (epoch & 0xFFu) << 24;
     a.timeoutNs = (unsigned long long)c->cfg.timeoutMs * 1000000ull;
     a.abortHost = c->abortHostDev;
     a.abortDev = c->abortDev;
@@ -349,6 +379,7 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
     c->device = dev;
     c->testStallRank = -1;
     c->hostError = vSuccess;
+    c->epoch = 1;                    // eager ring launches use epochs >= 2
     int v = 0;
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) goto fail;
     c->smCount = v;

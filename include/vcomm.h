@@ -29,6 +29,12 @@
  * communicator must be destroyed.
  *
  * Threading: a communicator is used by one host thread at a time.
+ *
+ * CUDA graphs: collectives may be captured into a graph.  A ring transfer can be
+ * captured only after an eager ring call of at least the same size on the same
+ * communicator (its FIFOs are allocated then; capturing it earlier returns
+ * vInvalidUsage); the captured transfer clears its FIFOs before every replay.  Graph
+ * replays are ordered by the caller: vcommDestroy waits only for eager launches.
  */
 #ifndef VCOMM_H
 #define VCOMM_H

@@ -388,6 +388,36 @@ def test_moe_dispatch_full(comms):
 
 
 # ---------------------------------------------------------------------------------------
+# CUDA graph capture and replay (the ring clears its FIFOs inside the graph)
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VID)
+def test_graph_capture_replays_match_oracle(comms, variant):
+    algo, proto = variant
+    n, count = 8, 100_003
+    c = comms.get(n, 4, proto, algo, SMALL_CHUNK)
+    send = empty_dev(n, count, torch.float32, fill=0.0)
+    recv = empty_dev(n, count, torch.float32)
+    eager = empty_dev(n, count, torch.float32)
+    V.vAllReduce(send, recv, count, torch.float32, "sum", c)       # allocates the ring FIFOs
+    _sync_ok(c)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        V.vAllReduce(send, recv, count, torch.float32, "sum", c)
+    for seed in (1, 2, 3):
+        xs = inputs.uniform_ranks(n, count, torch.float32, seed)
+        for d, x in zip(send, xs):
+            d.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        want = oracle.allreduce(xs, "sum")
+        assert_bits_equal(recv, want, f"replay {seed}")
+        V.vAllReduce(send, eager, count, torch.float32, "sum", c)  # eager launches interleave
+        _sync_ok(c)
+        assert_bits_equal(eager, want, f"eager after replay {seed}")
+
+
+# ---------------------------------------------------------------------------------------
 # Failure detection: bounded waits, abort, sticky errors (no fault, no trap)
 # ---------------------------------------------------------------------------------------
 

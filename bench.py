@@ -296,6 +296,7 @@ def run_ours(args):
         line["e2e"] = e2e_allreduce(torch, V, comm, xs, dev, stream, steps=max(3, min(args.steps, 10)))
         line["sweep"] = sweep(torch, V, dev, stream, hbm)
         line["channel_sweep"] = channel_sweep(torch, V, send, recv, stream)
+        line["other_workloads"] = other_workloads(torch, V, dev, stream, hbm)
         line["cpu_baseline"] = cpu_baseline_sample(torch)
     elif not args.no_extras:
         line["e2e"] = None
@@ -332,33 +333,120 @@ def check_sample(torch, V, xs, recv, n_samples=4096):
 
 
 def e2e_allreduce(torch, V, comm, xs, dev, stream, steps):
-    """Host buffers in, host buffers out: H2D of every rank's input, the all-reduce, and
-    D2H of every rank's result, all inside the timed region."""
+    """Host buffers in, host buffers out, through vAllReduce.
+
+    zero_copy (reported): the caller passes pinned host buffers straight to vAllReduce; the
+    kernel reads every rank's input from host memory and writes every rank's result back
+    over NVLink-C2C, all inside the timed region.  explicit_copies: H2D of all 8 inputs,
+    the kernel on device buffers, D2H of all 8 results, serialized on one stream."""
     host_in = [x.pin_memory() for x in xs]
     host_out = [torch.empty_like(x).pin_memory() for x in xs]
     d_in = [torch.empty_like(x, device=dev) for x in xs]
     d_out = [torch.empty_like(x, device=dev) for x in xs]
 
-    def step():
+    def zero_copy():
+        V.vAllReduce(host_in, host_out, COUNT, torch.float32, "sum", comm, stream)
+
+    def explicit():
         for d, h in zip(d_in, host_in):
             d.copy_(h, non_blocking=True)
         V.vAllReduce(d_in, d_out, COUNT, torch.float32, "sum", comm, stream)
         for h, d in zip(host_out, d_out):
             h.copy_(d, non_blocking=True)
 
-    step()
-    torch.cuda.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        step()
-    stop.record(stream)
-    torch.cuda.synchronize()
-    t = start.elapsed_time(stop) / 1e3 / steps
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            fn()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(stop) / 1e3 / steps
+
+    t = timed(zero_copy)
+    t_copy = timed(explicit)
+    consistent = all(torch.equal(host_out[r], d_out[r].cpu()) for r in range(N_RANKS))
     nbytes = N_RANKS * BYTES_PER_RANK
     return {"value": BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "ms_per_step": t * 1e3,
-            "steps": steps}
+            "steps": steps, "mode": "zero-copy: kernel reads pinned host inputs and writes pinned "
+                                    "host outputs over NVLink-C2C",
+            "explicit_copies": {"value": BYTES_PER_RANK / t_copy * bus_factor(N_RANKS) / 1e9,
+                                "ms_per_step": t_copy * 1e3},
+            "results_match_device_path": consistent}
+
+
+def other_workloads(torch, V, dev, stream, hbm):
+    """Kernel time and HBM fraction of the other collectives on their workloads."""
+    from collective_communication_virtual_gb300 import inputs
+    comm = V.vcommInit(N_RANKS, 1, V.vProtoSimple)
+    V.vcommSetAlgo(comm, "onepass")
+    out = {}
+
+    def tm(fn, steps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / steps
+
+    def rec(name, t, nbytes, bytes_per_rank, factor):
+        out[name] = {"us": t * 1e6, "min_bytes": nbytes, "hbm_frac": nbytes / t / 1e9 / hbm,
+                     "busbw_gbs": bytes_per_rank / t * factor / 1e9}
+
+    n = N_RANKS
+    f1 = (n - 1) / n
+    # FSDP bucket: bf16 25 MiB per rank, reduce-scatter * 1/8 -> fp32, then all-gather
+    cnt, rc = 13_107_200, 13_107_200 // n
+    g = [x.to(dev) for x in inputs.normal_ranks(n, cnt, 1e-3, torch.bfloat16, 2)]
+    sh = [torch.empty(rc, device=dev) for _ in range(n)]
+    t = tm(lambda: V.vReduceScatterScaleCast(g, sh, rc, torch.bfloat16, "sum", torch.float32, 1.0 / n,
+                                             comm, stream))
+    rec("fsdp_reduce_scatter_scale_cast_bf16_25MiB", t, n * cnt * 2 + n * rc * 4, cnt * 2, f1)
+    shb = [s.to(torch.bfloat16) for s in sh]
+    t = tm(lambda: V.vAllGather(shb, g, rc, torch.bfloat16, "sum", comm, stream))
+    rec("fsdp_allgather_bf16_25MiB", t, n * rc * 2 + n * cnt * 2, cnt * 2, f1)
+    del g, sh, shb
+    # MoE dispatch: variable all-to-all, bf16, 8 x 4096 tokens x 4096, top-2 Zipf(1.2)
+    send, counts, sd, rd, recv_elems = inputs.moe_dispatch()
+    s_d = [x.to(dev) for x in send]
+    r_d = [torch.empty(e, dtype=torch.bfloat16, device=dev) for e in recv_elems]
+    tabs = [x.to(dev) for x in (counts, sd, rd)]
+    t = tm(lambda: V.vAllToAllv(s_d, r_d, *tabs, torch.bfloat16, comm, stream))
+    moved = int(counts.sum()) * 2
+    rec("moe_alltoallv_bf16_8x4096x4096_top2", t, 2 * moved, moved // n, f1)
+    out["moe_alltoallv_bf16_8x4096x4096_top2"]["max_recv_mib"] = max(recv_elems) * 2 / 2**20
+    del s_d, r_d
+    torch.cuda.empty_cache()
+    # uniform all-to-all at 1 GiB per rank
+    cnt = 1 << 28
+    a = [torch.empty(cnt, device=dev) for _ in range(n)]
+    b = [torch.empty(cnt, device=dev) for _ in range(n)]
+    t = tm(lambda: V.vAllToAll(a, b, cnt // n, torch.float32, "sum", comm, stream), 10)
+    rec("alltoall_fp32_1GiB", t, 2 * n * cnt * 4, cnt * 4, f1)
+    del a, b
+    torch.cuda.empty_cache()
+    # reduce-scatter, all-gather, broadcast at 64 MiB per rank (fp32)
+    x = [torch.rand(COUNT, device=dev) for _ in range(n)]
+    y = [torch.empty(COUNT, device=dev) for _ in range(n)]
+    part = [torch.empty(COUNT // n, device=dev) for _ in range(n)]
+    t = tm(lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", comm, stream))
+    rec("reduce_scatter_fp32_64MiB", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    t = tm(lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", comm, stream))
+    rec("allgather_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    t = tm(lambda: V.vBroadcast(x, y, COUNT, torch.float32, "sum", 0, comm, stream))
+    rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
+    rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    V.vcommDestroy(comm)
+    return out
 
 
 def sweep(torch, V, dev, stream, hbm):
@@ -382,19 +470,39 @@ def sweep(torch, V, dev, stream, hbm):
 
 
 def channel_sweep(torch, V, send, recv, stream):
+    """busBW of the one-pass kernel and the staged ring per channel count (and ring chunk
+    size); every configuration gives the same bits."""
     out = []
-    for algo, proto in (("onepass", V.vProtoSimple), ("ring", V.vProtoSimple)):
+    cases = [("onepass", V.vProtoSimple, "simple", None)]
+    for proto, pname in ((V.vProtoSimple, "simple"), (V.vProtoLL, "ll"), (V.vProtoLL128, "ll128")):
+        cases += [("ring", proto, pname, 128 << 10), ("ring", proto, pname, 2 << 20)]
+    for algo, proto, pname, chunk in cases:
         for ch in (1, 8, 16, 32):
             comm = V.vcommInit(N_RANKS, ch, proto)
             V.vcommSetAlgo(comm, algo)
+            if chunk:
+                V.vcommSetChunkBytes(comm, chunk)
             try:
-                t = time_allreduce(V, torch, comm, send, recv, COUNT, 5, 2, stream)
-                out.append({"algo": algo, "proto": "simple", "channels": ch,
+                t = time_allreduce(V, torch, comm, send, recv, COUNT, 3, 1, stream)
+                out.append({"algo": algo, "proto": pname, "channels": ch, "chunk_bytes": chunk,
                             "busbw_gbs": BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9})
             except V.VcommError as e:
-                out.append({"algo": algo, "channels": ch, "error": str(e)})
+                out.append({"algo": algo, "proto": pname, "channels": ch, "chunk_bytes": chunk,
+                            "error": str(e)})
             V.vcommDestroy(comm)
     return out
+
+
+def run_workloads():
+    import torch
+
+    from collective_communication_virtual_gb300 import build, vcomm as V
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm, _ = peaks()
+    print(json.dumps({"other_workloads": other_workloads(torch, V, dev, torch.cuda.current_stream(), hbm)}))
+    return 0
 
 
 def main():
@@ -404,12 +512,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, sweeps and the CPU baseline")
+    ap.add_argument("--workloads", action="store_true",
+                    help="only time the other collectives (FSDP bucket, MoE dispatch, all-to-all, "
+                         "reduce-scatter, all-gather, broadcast) and print them as one JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     sys.path.insert(0, ROOT)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workloads:
+        return run_workloads()
     return run_ours(args)
 
 

@@ -9,57 +9,83 @@
 
 namespace vc {
 
-constexpr int kCopyUnroll = 4;     // vectors in flight per thread in the block copies
+constexpr int kCopyUnroll = 8;             // vectors in flight per thread in a tile copy
+constexpr size_t kTileBytes = 64 * 1024;   // unit of work dealt to a CTA
 
-// Each kernel flattens a channel's work -- (block, unit) pairs, a unit being 16 bytes on
-// the vector path and one element otherwise -- to one index strided over the channel's
-// CTAs, kCopyUnroll units per thread at a time (all loads, then all stores).  Only the
-// end of a block can cut a vector short; those elements are copied one by one.
+// The copy kernels deal 64 KiB tiles of a channel's block ranges to the channel's CTAs
+// round-robin: tile t covers elements [lo + k*T, lo + (k+1)*T) of block p = t / tilesPerBlock.
+// Consecutive CTAs take consecutive tiles of one block, so the grid streams through a
+// few blocks at a time, and the index arithmetic costs one division per tile.  Inside a
+// tile each thread issues all its loads (up to kCopyUnroll 16-byte vectors) before its
+// stores.  Only the end of a block can cut a vector short; those elements are copied one
+// by one.
 
-// All-gather: block s = send[s][ch range], written to recv[r] + s*sc for every r.
+// Copy [lo, hi) elements from src to every dst[0..ndst) (ndst = 1 for all-to-all).
 template <int ESZ, bool VEC>
-__global__ void __launch_bounds__(kOnePassThreads)
-k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
-    constexpr int U = VEC ? 16 / ESZ : 1;
-    const int N = a.nRanks;
-    const int ch = blockIdx.x / a.ctasPerChannel;
-    const int cta = blockIdx.x - ch * a.ctasPerChannel;
-    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
-    const size_t sc = a.count;
-    const size_t lo = min((size_t)ch * a.chanElems, sc);
-    const size_t hi = min((size_t)(ch + 1) * a.chanElems, sc);
-    const size_t units = (hi - lo + U - 1) / U;
-    const size_t total = units * (size_t)N;
-    for (size_t j0 = (size_t)cta * blockDim.x + threadIdx.x; j0 < total; j0 += kCopyUnroll * stride) {
-        uint4 v[kCopyUnroll];
-        uint32_t sv[kCopyUnroll];
+__device__ __forceinline__ void tile_copy(const char* src, char* const* dst, size_t dstOff, int ndst,
+                                          size_t lo, size_t hi) {
+    if (VEC) {
+        constexpr int VE = 16 / ESZ;
+        const size_t nv = (hi - lo) / VE;
+        for (size_t i0 = threadIdx.x; i0 < nv; i0 += (size_t)kCopyUnroll * blockDim.x) {
+            uint4 v[kCopyUnroll];
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; u++) {
-            const size_t j = j0 + u * stride;
-            if (j >= total) break;
-            const int s = (int)(j / units);
-            const size_t e = lo + (j - (size_t)s * units) * U;
-            if (VEC && e + U <= hi) v[u] = ld_stream((const char*)a.send[s] + e * ESZ);
-            else if (!VEC) sv[u] = ld_elem<ESZ>(a.send[s], e);
-        }
+            for (int u = 0; u < kCopyUnroll; u++) {
+                const size_t i = i0 + (size_t)u * blockDim.x;
+                if (i < nv) v[u] = ld_stream(src + (lo + i * VE) * ESZ);
+            }
+            for (int d = 0; d < ndst; d++) {
+                char* o = dst[d] + dstOff * ESZ;
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; u++) {
-            const size_t j = j0 + u * stride;
-            if (j >= total) break;
-            const int s = (int)(j / units);
-            const size_t e = lo + (j - (size_t)s * units) * U;
-            const size_t dOff = (size_t)s * sc + e;
-            if (VEC && e + U <= hi) {
-                for (int r = 0; r < N; r++) st_stream((char*)a.recv[r] + dOff * ESZ, v[u]);
-            } else if (!VEC) {
-                for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], dOff, sv[u]);
-            } else {
-                for (size_t x = e; x < hi; x++) {
-                    const uint32_t w = ld_elem<ESZ>(a.send[s], x);
-                    for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], (size_t)s * sc + x, w);
+                for (int u = 0; u < kCopyUnroll; u++) {
+                    const size_t i = i0 + (size_t)u * blockDim.x;
+                    if (i < nv) st_stream(o + (lo + i * VE) * ESZ, v[u]);
                 }
             }
         }
+        const size_t tail = lo + nv * VE;
+        if (tail + threadIdx.x < hi) {
+            const uint32_t w = ld_elem<ESZ>(src, tail + threadIdx.x);
+            for (int d = 0; d < ndst; d++) st_elem<ESZ>(dst[d] + dstOff * ESZ, tail + threadIdx.x, w);
+        }
+    } else {
+        for (size_t e = lo + threadIdx.x; e < hi; e += blockDim.x) {
+            const uint32_t w = ld_elem<ESZ>(src, e);
+            for (int d = 0; d < ndst; d++) st_elem<ESZ>(dst[d] + dstOff * ESZ, e, w);
+        }
+    }
+}
+
+struct TileSpan {
+    size_t lo, hi;            // channel range within a block
+    size_t tileElems, tilesPerBlock;
+};
+
+template <int ESZ>
+__device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size_t blockLen) {
+    TileSpan t;
+    t.lo = min((size_t)ch * a.chanElems, blockLen);
+    t.hi = min((size_t)(ch + 1) * a.chanElems, blockLen);
+    t.tileElems = kTileBytes / ESZ;
+    t.tilesPerBlock = (t.hi - t.lo + t.tileElems - 1) / t.tileElems;
+    return t;
+}
+
+// All-gather: block s = send[s] lands at recv[r] + s*sc for every r.  a.count = sc.
+template <int ESZ, bool VEC>
+__global__ void __launch_bounds__(kOnePassThreads)
+k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t sc = a.count;
+    const TileSpan sp = tile_span<ESZ>(a, ch, sc);
+    const size_t nTiles = sp.tilesPerBlock * (size_t)N;
+    for (size_t t = cta; t < nTiles; t += a.ctasPerChannel) {
+        const int s = (int)(t / sp.tilesPerBlock);
+        const size_t k = t - (size_t)s * sp.tilesPerBlock;
+        const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
+        tile_copy<ESZ, VEC>((const char*)a.send[s], (char* const*)a.recv, (size_t)s * sc, N, tlo, thi);
     }
 }
 
@@ -67,114 +93,32 @@ k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
 template <int ESZ, bool VEC>
 __global__ void __launch_bounds__(kOnePassThreads)
 k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
-    constexpr int U = VEC ? 16 / ESZ : 1;
-    const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
-    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
-    const size_t lo = min((size_t)ch * a.chanElems, a.count);
-    const size_t hi = min((size_t)(ch + 1) * a.chanElems, a.count);
-    const size_t units = (hi - lo + U - 1) / U;
-    const char* src = (const char*)a.send[a.root];
-    for (size_t j0 = (size_t)cta * blockDim.x + threadIdx.x; j0 < units; j0 += kCopyUnroll * stride) {
-        uint4 v[kCopyUnroll];
-        uint32_t sv[kCopyUnroll];
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; u++) {
-            const size_t j = j0 + u * stride;
-            if (j >= units) break;
-            const size_t e = lo + j * U;
-            if (VEC && e + U <= hi) v[u] = ld_stream(src + e * ESZ);
-            else if (!VEC) sv[u] = ld_elem<ESZ>(src, e);
-        }
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; u++) {
-            const size_t j = j0 + u * stride;
-            if (j >= units) break;
-            const size_t e = lo + j * U;
-            if (VEC && e + U <= hi) {
-                for (int r = 0; r < N; r++) st_stream((char*)a.recv[r] + e * ESZ, v[u]);
-            } else if (!VEC) {
-                for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], e, sv[u]);
-            } else {
-                for (size_t x = e; x < hi; x++) {
-                    const uint32_t w = ld_elem<ESZ>(src, x);
-                    for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], x, w);
-                }
-            }
-        }
+    const TileSpan sp = tile_span<ESZ>(a, ch, a.count);
+    for (size_t k = cta; k < sp.tilesPerBlock; k += a.ctasPerChannel) {
+        const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
+        tile_copy<ESZ, VEC>((const char*)a.send[a.root], (char* const*)a.recv, 0, a.nRanks, tlo, thi);
     }
 }
 
-// Copy [lo, hi) elements from src to dst with kCopyUnroll vectors in flight per thread.
-template <int ESZ, bool VEC>
-__device__ __forceinline__ void copy_range(const char* src, char* dst, size_t lo, size_t hi,
-                                           size_t tid, size_t stride) {
-    if (VEC) {
-        constexpr int VE = 16 / ESZ;
-        const size_t nv = (hi - lo) / VE;
-        size_t i = tid;
-        for (; i + (kCopyUnroll - 1) * stride < nv; i += kCopyUnroll * stride) {
-            uint4 v[kCopyUnroll];
-#pragma unroll
-            for (int u = 0; u < kCopyUnroll; u++) v[u] = ld_stream(src + (lo + (i + u * stride) * VE) * ESZ);
-#pragma unroll
-            for (int u = 0; u < kCopyUnroll; u++) st_stream(dst + (lo + (i + u * stride) * VE) * ESZ, v[u]);
-        }
-        for (; i < nv; i += stride) st_stream(dst + (lo + i * VE) * ESZ, ld_stream(src + (lo + i * VE) * ESZ));
-        const size_t tail = lo + nv * VE;
-        if (tail + tid < hi) st_elem<ESZ>(dst, tail + tid, ld_elem<ESZ>(src, tail + tid));
-    } else {
-        for (size_t e = lo + tid; e < hi; e += stride) st_elem<ESZ>(dst, e, ld_elem<ESZ>(src, e));
-    }
-}
-
-// Uniform all-to-all: recv[j][i*c + t] = send[i][j*c + t].  a.count = c.  The N*N blocks'
-// channel ranges are flattened as p = i*N + j, unit within the range.
+// Uniform all-to-all: recv[j][i*c + t] = send[i][j*c + t].  a.count = c.
 template <int ESZ, bool VEC>
 __global__ void __launch_bounds__(kOnePassThreads)
 k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
-    constexpr int U = VEC ? 16 / ESZ : 1;
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
-    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
     const size_t c = a.count;
-    const size_t lo = min((size_t)ch * a.chanElems, c);
-    const size_t hi = min((size_t)(ch + 1) * a.chanElems, c);
-    const size_t units = (hi - lo + U - 1) / U;
-    const size_t total = units * (size_t)N * (size_t)N;
-    for (size_t j0 = (size_t)cta * blockDim.x + threadIdx.x; j0 < total; j0 += kCopyUnroll * stride) {
-        uint4 v[kCopyUnroll];
-        uint32_t sv[kCopyUnroll];
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; u++) {
-            const size_t jj = j0 + u * stride;
-            if (jj >= total) break;
-            const size_t p = jj / units;
-            const int i = (int)(p / N), j = (int)(p - (size_t)(p / N) * N);
-            const size_t e = lo + (jj - p * units) * U;
-            const char* src = (const char*)a.send[i] + (size_t)j * c * ESZ;
-            if (VEC && e + U <= hi) v[u] = ld_stream(src + e * ESZ);
-            else if (!VEC) sv[u] = ld_elem<ESZ>(src, e);
-        }
-#pragma unroll
-        for (int u = 0; u < kCopyUnroll; u++) {
-            const size_t jj = j0 + u * stride;
-            if (jj >= total) break;
-            const size_t p = jj / units;
-            const int i = (int)(p / N), j = (int)(p - (size_t)(p / N) * N);
-            const size_t e = lo + (jj - p * units) * U;
-            char* dst = (char*)a.recv[j] + (size_t)i * c * ESZ;
-            if (VEC && e + U <= hi) {
-                st_stream(dst + e * ESZ, v[u]);
-            } else if (!VEC) {
-                st_elem<ESZ>(dst, e, sv[u]);
-            } else {
-                const char* src = (const char*)a.send[i] + (size_t)j * c * ESZ;
-                for (size_t x = e; x < hi; x++) st_elem<ESZ>(dst, x, ld_elem<ESZ>(src, x));
-            }
-        }
+    const TileSpan sp = tile_span<ESZ>(a, ch, c);
+    const size_t nTiles = sp.tilesPerBlock * (size_t)N * (size_t)N;
+    for (size_t t = cta; t < nTiles; t += a.ctasPerChannel) {
+        const size_t p = t / sp.tilesPerBlock;
+        const size_t k = t - p * sp.tilesPerBlock;
+        const int i = (int)(p / N), j = (int)(p - (p / N) * N);
+        const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
+        char* dst = (char*)a.recv[j];
+        tile_copy<ESZ, VEC>((const char*)a.send[i] + (size_t)j * c * ESZ, &dst, (size_t)i * c, 1, tlo, thi);
     }
 }
 
@@ -218,8 +162,8 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
         const char* src = (const char*)a.send[i] + (size_t)a.sdispls[p] * ESZ;
         char* dst = (char*)a.recv[j] + (size_t)a.rdispls[j * N + i] * ESZ;
         const bool vec = ((((uintptr_t)src) | ((uintptr_t)dst)) & 15) == 0;
-        if (vec) copy_range<ESZ, true>(src, dst, lo, hi, threadIdx.x, blockDim.x);
-        else copy_range<ESZ, false>(src, dst, lo, hi, threadIdx.x, blockDim.x);
+        if (vec) tile_copy<ESZ, true>(src, &dst, 0, 1, lo, hi);
+        else tile_copy<ESZ, false>(src, &dst, 0, 1, lo, hi);
     }
 }
 

@@ -106,16 +106,21 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         // Round down so the grid never spills into a second, mostly idle wave.
         const int target = 2 * smCount;
         int per = std::max(1, target / q->nChannels);
-        size_t work = 0;    // vectors (or elements) one channel moves per block pass
+        // Never more CTAs than a channel has work items: for the reductions a work item is
+        // one thread's unit (a 16-byte vector of every rank), for the copies a 64 KiB tile.
+        size_t maxPer = 1;
         if (q->coll == vCollAllToAllv) {
-            work = (size_t)1 << 40;
+            maxPer = (size_t)target;
         } else {
             const size_t chElems = std::min(p->channelElems, B);
-            size_t blocks = q->coll == vCollBroadcast ? 1 : (size_t)N;
-            if (q->coll == vCollAllToAll) blocks = (size_t)N * N;
-            work = div_up(chElems, vec ? VE : 1) * (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ? blocks : 1);
+            if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter) {
+                maxPer = div_up(div_up(chElems, vec ? VE : 1) * (size_t)N, (size_t)p->threadsPerCta);
+            } else {
+                size_t blocks = q->coll == vCollBroadcast ? 1 : q->coll == vCollAllGather ? (size_t)N : (size_t)N * N;
+                maxPer = div_up(chElems * esz, (size_t)64 * 1024) * blocks;
+            }
         }
-        const size_t maxPer = std::max<size_t>(1, div_up(work, (size_t)p->threadsPerCta));
+        maxPer = std::max<size_t>(1, maxPer);
         per = (int)std::min<size_t>((size_t)per, maxPer);
         if (q->coll == vCollAllToAllv) { p->nChannels = 1; per = target; }
         p->ctasPerChannel = per;

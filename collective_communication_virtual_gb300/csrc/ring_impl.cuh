@@ -247,13 +247,20 @@ __device__ __forceinline__ void slot_end(const RingArgs& a, RingCtx& c, int kind
     if (kind & kRecv) c.recvSeq++;
 }
 
+// Units per thread whose loads are in flight together; the flag protocols hold more per
+// unit, so they take fewer to stay within 64 registers (two 512-thread CTAs per SM).
+template <int PROTO> struct RingUnroll { static constexpr int value = PROTO == vProtoSimple ? 4 : 2; };
+
 // One slot of m elements.  `in`: user input at the slot's first element (kLocal);
-// `out`: user output at the slot's first element (kOut).
+// `out`: user output at the slot's first element (kOut).  Each thread takes R units at a
+// time and issues all their loads (FIFO data or flags, user data) before
+// combining and storing any of them.
 template <int DT, int OUT, int PROTO>
 __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kind, const char* in,
                                           char* out, size_t m, bool epi) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int OSZ = DTypeOf<OUT>::size;
+    constexpr int R = RingUnroll<PROTO>::value;
     const bool aligned = a.aligned != 0;
     const bool hasScale = a.hasScale != 0;
     if (!slot_begin<PROTO>(a, c, kind)) return false;
@@ -264,17 +271,29 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
         // 16 payload bytes per unit, contiguous in the slot.
         constexpr int UE = 16 / ESZ;
         const size_t units = (m + UE - 1) / UE;
-        for (size_t u = threadIdx.x; u < units; u += blockDim.x) {
-            const int ne = (int)min((size_t)UE, m - u * UE);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (kind & kRecv) v = ld_cg(rs + u * 16);
-            if (kind & kLocal) {
-                const uint4 l = load_unit<ESZ, 16, 16>(in + u * 16, ne, aligned);
-                v = (kind & kRecv) ? op_vec_rt<DT>(a.op, v, l) : l;
+        for (size_t u0 = threadIdx.x; u0 < units; u0 += (size_t)R * blockDim.x) {
+            uint4 v[R], l[R];
+#pragma unroll
+            for (int k = 0; k < R; k++) {
+                const size_t u = u0 + (size_t)k * blockDim.x;
+                v[k] = make_uint4(0u, 0u, 0u, 0u);
+                l[k] = v[k];
+                if (u < units) {
+                    if (kind & kRecv) v[k] = ld_cg(rs + u * 16);
+                    if (kind & kLocal) l[k] = load_unit<ESZ, 16, 16>(in + u * 16, (int)min((size_t)UE, m - u * UE), aligned);
+                }
             }
-            if (kind & kOut)
-                store_unit<DT, OUT, 16, 16>(out + u * UE * OSZ, v, ne, aligned, epi, hasScale, a.scale);
-            if (kind & kSend) st_cg(ss + u * 16, v);
+#pragma unroll
+            for (int k = 0; k < R; k++) {
+                const size_t u = u0 + (size_t)k * blockDim.x;
+                if (u >= units) break;
+                const int ne = (int)min((size_t)UE, m - u * UE);
+                uint4 x = v[k];
+                if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
+                if (kind & kOut)
+                    store_unit<DT, OUT, 16, 16>(out + u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
+                if (kind & kSend) st_cg(ss + u * 16, x);
+            }
         }
     } else if (PROTO == vProtoLL) {
         // 8 payload bytes per unit, stored as two {data, flag} 64-bit words.
@@ -282,22 +301,41 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
         const size_t units = (m + UE - 1) / UE;
         const unsigned int rflag = a.llEpoch | ((c.recvSeq + 1u) & 0xFFFFFFu);
         const unsigned long long sflag = (unsigned long long)(a.llEpoch | ((c.sendSeq + 1u) & 0xFFFFFFu)) << 32;
-        for (size_t u = threadIdx.x; u < units && !fail; u += blockDim.x) {
-            const int ne = (int)min((size_t)UE, m - u * UE);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (kind & kRecv) {
-                uint2 d;
-                if (!wait_ll(a, c, rs + u * 16, rflag, &d, c.recvSeq)) { fail = true; break; }
-                v.x = d.x;
-                v.y = d.y;
+        for (size_t u0 = threadIdx.x; u0 < units && !fail; u0 += (size_t)R * blockDim.x) {
+            unsigned long long w0[R], w1[R];
+            uint4 l[R];
+#pragma unroll
+            for (int k = 0; k < R; k++) {
+                const size_t u = u0 + (size_t)k * blockDim.x;
+                w0[k] = w1[k] = 0ull;
+                l[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (u < units) {
+                    if (kind & kRecv) ld_volatile_u64x2(rs + u * 16, w0[k], w1[k]);
+                    if (kind & kLocal) l[k] = load_unit<ESZ, 8, 8>(in + u * 8, (int)min((size_t)UE, m - u * UE), aligned);
+                }
             }
-            if (kind & kLocal) {
-                const uint4 l = load_unit<ESZ, 8, 8>(in + u * 8, ne, aligned);
-                v = (kind & kRecv) ? op_vec_rt<DT>(a.op, v, l) : l;
+#pragma unroll
+            for (int k = 0; k < R; k++) {
+                const size_t u = u0 + (size_t)k * blockDim.x;
+                if (u >= units || fail) break;
+                const int ne = (int)min((size_t)UE, m - u * UE);
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                if (kind & kRecv) {
+                    if ((unsigned int)(w0[k] >> 32) == rflag && (unsigned int)(w1[k] >> 32) == rflag) {
+                        x.x = (unsigned int)w0[k];
+                        x.y = (unsigned int)w1[k];
+                    } else {
+                        uint2 d;
+                        if (!wait_ll_slow(a, c, rs + u * 16, rflag, &d, c.recvSeq)) { fail = true; break; }
+                        x.x = d.x;
+                        x.y = d.y;
+                    }
+                }
+                if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
+                if (kind & kOut)
+                    store_unit<DT, OUT, 8, 8>(out + u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
+                if (kind & kSend) st_volatile_u64x2(ss + u * 16, sflag | x.x, sflag | x.y);
             }
-            if (kind & kOut)
-                store_unit<DT, OUT, 8, 8>(out + u * UE * OSZ, v, ne, aligned, epi, hasScale, a.scale);
-            if (kind & kSend) st_volatile_u64x2(ss + u * 16, sflag | v.x, sflag | v.y);
         }
     } else {
         // LL128: 128-byte lines of 120 payload bytes + an 8-byte flag.  Eight lanes share a
@@ -318,32 +356,43 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
         }
         if (!__any_sync(0xFFFFFFFFu, fail)) {
             const int pb = t < 7 ? 16 * t : 112;              // payload byte offset in the line
-            for (size_t L = (size_t)warp * 4 + g; L < lines; L += perIter) {
-                const size_t e0 = (L * 120 + pb) / ESZ;           // first element of this lane
-                if (e0 >= m) continue;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (kind & kRecv) {
-                    if (t < 7) v = ld_cg(rs + L * 128 + 16 * t);
-                    else { const uint2 d = ld_cg8(rs + L * 128 + 112); v.x = d.x; v.y = d.y; }
+            const int UEl = t < 7 ? 16 / ESZ : 8 / ESZ;        // elements of this lane
+            for (size_t L0 = (size_t)warp * 4 + g; L0 < lines; L0 += (size_t)R * perIter) {
+                uint4 v[R], l[R];
+#pragma unroll
+                for (int k = 0; k < R; k++) {
+                    const size_t L = L0 + (size_t)k * perIter;
+                    const size_t e0 = (L * 120 + pb) / ESZ;    // first element of this lane
+                    v[k] = make_uint4(0u, 0u, 0u, 0u);
+                    l[k] = v[k];
+                    if (L < lines && e0 < m) {
+                        const int ne = (int)min((size_t)UEl, m - e0);
+                        if (kind & kRecv) {
+                            if (t < 7) v[k] = ld_cg(rs + L * 128 + 16 * t);
+                            else { const uint2 d = ld_cg8(rs + L * 128 + 112); v[k].x = d.x; v[k].y = d.y; }
+                        }
+                        if (kind & kLocal)
+                            l[k] = t < 7 ? load_unit<ESZ, 16, 8>(in + e0 * ESZ, ne, aligned)
+                                         : load_unit<ESZ, 8, 8>(in + e0 * ESZ, ne, aligned);
+                    }
                 }
-                if (t < 7) {
-                    const int ne = (int)min((size_t)(16 / ESZ), m - e0);
-                    if (kind & kLocal) {
-                        const uint4 l = load_unit<ESZ, 16, 8>(in + e0 * ESZ, ne, aligned);
-                        v = (kind & kRecv) ? op_vec_rt<DT>(a.op, v, l) : l;
+#pragma unroll
+                for (int k = 0; k < R; k++) {
+                    const size_t L = L0 + (size_t)k * perIter;
+                    const size_t e0 = (L * 120 + pb) / ESZ;
+                    if (L >= lines || e0 >= m) continue;
+                    const int ne = (int)min((size_t)UEl, m - e0);
+                    uint4 x = v[k];
+                    if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
+                    if (t < 7) {
+                        if (kind & kOut)
+                            store_unit<DT, OUT, 16, 8>(out + e0 * OSZ, x, ne, aligned, epi, hasScale, a.scale);
+                        if (kind & kSend) st_cg(ss + L * 128 + 16 * t, x);
+                    } else {
+                        if (kind & kOut)
+                            store_unit<DT, OUT, 8, 8>(out + e0 * OSZ, x, ne, aligned, epi, hasScale, a.scale);
+                        if (kind & kSend) st_cg8(ss + L * 128 + 112, make_uint2(x.x, x.y));
                     }
-                    if (kind & kOut)
-                        store_unit<DT, OUT, 16, 8>(out + e0 * OSZ, v, ne, aligned, epi, hasScale, a.scale);
-                    if (kind & kSend) st_cg(ss + L * 128 + 16 * t, v);
-                } else {
-                    const int ne = (int)min((size_t)(8 / ESZ), m - e0);
-                    if (kind & kLocal) {
-                        const uint4 l = load_unit<ESZ, 8, 8>(in + e0 * ESZ, ne, aligned);
-                        v = (kind & kRecv) ? op_vec_rt<DT>(a.op, v, l) : l;
-                    }
-                    if (kind & kOut)
-                        store_unit<DT, OUT, 8, 8>(out + e0 * OSZ, v, ne, aligned, epi, hasScale, a.scale);
-                    if (kind & kSend) st_cg8(ss + L * 128 + 112, make_uint2(v.x, v.y));
                 }
             }
             if (kind & kSend) {
@@ -389,7 +438,7 @@ __device__ __forceinline__ size_t seg_len(const RingArgs& a, int ch, int blk, si
 }
 
 template <int DT, int OUT, int PROTO>
-__global__ void __launch_bounds__(kRingThreads) k_ring(const __grid_constant__ RingArgs a) {
+__global__ void __launch_bounds__(kRingThreads, 2) k_ring(const __grid_constant__ RingArgs a) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int OSZ = DTypeOf<OUT>::size;
     const int N = a.nRanks;

@@ -139,7 +139,9 @@ vResult_t vcommSetChunkBytes(vcomm_t comm, size_t chunkBytes);
 vResult_t vcommSetTimeoutMs(vcomm_t comm, int timeoutMs);
 
 /* ------------------------------------------------------------------------------- */
-/* Collectives.  sendbuffs / recvbuffs: host arrays of nRanks device pointers.       */
+/* Collectives.  sendbuffs / recvbuffs: host arrays of nRanks pointers to memory the */
+/* device can access (device allocations, pinned or managed host memory: the kernels */
+/* read and write it directly, so host buffers need no staging copies).              */
 /* Any element-aligned pointer is accepted; when every pointer and the sizes allow   */
 /* 16-byte vectors the vector path runs, otherwise an element-wise path; the output  */
 /* bits are the same.  count == 0 returns vSuccess and launches nothing (NCCL book   */

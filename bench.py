@@ -249,7 +249,7 @@ def run_ours(args):
     recv = [torch.empty_like(s) for s in send]
     comm = V.vcommInit(N_RANKS, 1, V.vProtoSimple)
     V.vcommSetAlgo(comm, "onepass")
-    plan = V.vcommQueryPlan(comm, V.vCollAllReduce, COUNT, torch.float32, True)
+    plan = V.vcommQueryPlan(comm, V.vCollAllReduce, COUNT, torch.float32, 32)
 
     # correctness of the timed configuration: sampled elements against the oracle
     V.vAllReduce(send, recv, COUNT, torch.float32, "sum", comm, stream)
@@ -278,7 +278,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "n_ranks": N_RANKS, "bytes_per_rank": BYTES_PER_RANK,
                        "algo": "onepass", "channels": plan["nChannels"], "grid_ctas": plan["gridCtas"],
-                       "threads_per_cta": plan["threadsPerCta"],
+                       "threads_per_cta": plan["threadsPerCta"], "vector_bytes": plan["vecBytes"],
                        "l2": "inputs larger than L2 (8 x 64 MiB read + 8 x 64 MiB written per step)",
                        "parallelism": f"{world} independent replica(s) of 8 virtual ranks"},
             "hbm_frac": achieved / hbm,

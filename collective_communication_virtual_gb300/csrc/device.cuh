@@ -134,6 +134,47 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// 32-byte accesses (Blackwell's 256-bit global loads and stores): half the instructions
+// of the 16-byte path for the same bytes in flight.  Data streamed once is marked
+// evict-first in L2 so it does not displace lines that are still to be read.
+struct V32 {
+    uint4 lo, hi;
+};
+__device__ __forceinline__ V32 ld_stream32(const void* p) {
+    V32 v;
+    asm("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y),
+          "=r"(v.hi.z), "=r"(v.hi.w)
+        : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream32(void* p, const V32& v) {
+    asm volatile("st.global.L2::evict_first.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(v.lo.x), "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x),
+                    "r"(v.hi.y), "r"(v.hi.z), "r"(v.hi.w)
+                 : "memory");
+}
+template <int DT, int OP>
+__device__ __forceinline__ V32 op_vec(const V32& a, const V32& b) {
+    V32 r;
+    r.lo = op_vec<DT, OP>(a.lo, b.lo);
+    r.hi = op_vec<DT, OP>(a.hi, b.hi);
+    return r;
+}
+
+// Vector of VB bytes (16 or 32) with its load/store.
+template <int VB> struct VecOf;
+template <> struct VecOf<16> {
+    using T = uint4;
+    static __device__ __forceinline__ uint4 ld(const void* p) { return ld_stream(p); }
+    static __device__ __forceinline__ void st(void* p, const uint4& v) { st_stream(p, v); }
+};
+template <> struct VecOf<32> {
+    using T = V32;
+    static __device__ __forceinline__ V32 ld(const void* p) { return ld_stream32(p); }
+    static __device__ __forceinline__ void st(void* p, const V32& v) { st_stream32(p, v); }
+};
+
 // Element loads/stores for the scalar paths (esz = 2 or 4).
 template <int ESZ>
 __device__ __forceinline__ uint32_t ld_elem(const void* base, size_t e) {

@@ -84,16 +84,17 @@ struct RingArgs {
 };
 
 // Launchers (defined in the kernel translation units).  Each returns the launch status.
-cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, bool vec,
+// vb: bytes per vector of the one-pass reductions, 0 (element path), 16 or 32.
+cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, int vb,
                                      int grid, int threads, cudaStream_t s);
 cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
-                                          vDataType_t outType, bool vec, int grid, int threads,
+                                          vDataType_t outType, int vb, int grid, int threads,
                                           cudaStream_t s);
-cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s);
-cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s);
-cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                     int threads, cudaStream_t s);
 cudaError_t launch_alltoallv(const A2AvArgs& a, int grid, int threads, cudaStream_t s);
 

@@ -21,32 +21,37 @@ constexpr size_t kTileBytes = 64 * 1024;   // unit of work dealt to a CTA
 // by one.
 
 // Copy [lo, hi) elements from src to every dst[0..ndst) (ndst = 1 for all-to-all).
-template <int ESZ, bool VEC>
+// VB: bytes per vector (16 or 32; 0 = element by element).  A thread keeps 128 bytes of
+// loads in flight: 8 vectors of 16 bytes or 4 of 32.
+template <int ESZ, int VB>
 __device__ __forceinline__ void tile_copy(const char* src, char* const* dst, size_t dstOff, int ndst,
                                           size_t lo, size_t hi) {
-    if (VEC) {
-        constexpr int VE = 16 / ESZ;
+    if (VB) {
+        constexpr int VBB = VB ? VB : 16;
+        constexpr int VE = VBB / ESZ;
+        constexpr int UN = 128 / VBB;
+        using VT = typename VecOf<VBB>::T;
         const size_t nv = (hi - lo) / VE;
-        for (size_t i0 = threadIdx.x; i0 < nv; i0 += (size_t)kCopyUnroll * blockDim.x) {
-            uint4 v[kCopyUnroll];
+        for (size_t i0 = threadIdx.x; i0 < nv; i0 += (size_t)UN * blockDim.x) {
+            VT v[UN];
 #pragma unroll
-            for (int u = 0; u < kCopyUnroll; u++) {
+            for (int u = 0; u < UN; u++) {
                 const size_t i = i0 + (size_t)u * blockDim.x;
-                if (i < nv) v[u] = ld_stream(src + (lo + i * VE) * ESZ);
+                if (i < nv) v[u] = VecOf<VBB>::ld(src + (lo + i * VE) * ESZ);
             }
             for (int d = 0; d < ndst; d++) {
                 char* o = dst[d] + dstOff * ESZ;
 #pragma unroll
-                for (int u = 0; u < kCopyUnroll; u++) {
+                for (int u = 0; u < UN; u++) {
                     const size_t i = i0 + (size_t)u * blockDim.x;
-                    if (i < nv) st_stream(o + (lo + i * VE) * ESZ, v[u]);
+                    if (i < nv) VecOf<VBB>::st(o + (lo + i * VE) * ESZ, v[u]);
                 }
             }
         }
         const size_t tail = lo + nv * VE;
-        if (tail + threadIdx.x < hi) {
-            const uint32_t w = ld_elem<ESZ>(src, tail + threadIdx.x);
-            for (int d = 0; d < ndst; d++) st_elem<ESZ>(dst[d] + dstOff * ESZ, tail + threadIdx.x, w);
+        for (size_t e = tail + threadIdx.x; e < hi; e += blockDim.x) {
+            const uint32_t w = ld_elem<ESZ>(src, e);
+            for (int d = 0; d < ndst; d++) st_elem<ESZ>(dst[d] + dstOff * ESZ, e, w);
         }
     } else {
         for (size_t e = lo + threadIdx.x; e < hi; e += blockDim.x) {
@@ -72,7 +77,7 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
 }
 
 // All-gather: block s = send[s] lands at recv[r] + s*sc for every r.  a.count = sc.
-template <int ESZ, bool VEC>
+template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads)
 k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
     const int N = a.nRanks;
@@ -85,12 +90,12 @@ k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
         const int s = (int)(t / sp.tilesPerBlock);
         const size_t k = t - (size_t)s * sp.tilesPerBlock;
         const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
-        tile_copy<ESZ, VEC>((const char*)a.send[s], (char* const*)a.recv, (size_t)s * sc, N, tlo, thi);
+        tile_copy<ESZ, VB>((const char*)a.send[s], (char* const*)a.recv, (size_t)s * sc, N, tlo, thi);
     }
 }
 
 // Broadcast: recv[r][t] = send[root][t] for all r.
-template <int ESZ, bool VEC>
+template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads)
 k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
     const int ch = blockIdx.x / a.ctasPerChannel;
@@ -98,12 +103,12 @@ k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
     const TileSpan sp = tile_span<ESZ>(a, ch, a.count);
     for (size_t k = cta; k < sp.tilesPerBlock; k += a.ctasPerChannel) {
         const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
-        tile_copy<ESZ, VEC>((const char*)a.send[a.root], (char* const*)a.recv, 0, a.nRanks, tlo, thi);
+        tile_copy<ESZ, VB>((const char*)a.send[a.root], (char* const*)a.recv, 0, a.nRanks, tlo, thi);
     }
 }
 
 // Uniform all-to-all: recv[j][i*c + t] = send[i][j*c + t].  a.count = c.
-template <int ESZ, bool VEC>
+template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads)
 k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
     const int N = a.nRanks;
@@ -118,7 +123,7 @@ k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
         const int i = (int)(p / N), j = (int)(p - (p / N) * N);
         const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
         char* dst = (char*)a.recv[j];
-        tile_copy<ESZ, VEC>((const char*)a.send[i] + (size_t)j * c * ESZ, &dst, (size_t)i * c, 1, tlo, thi);
+        tile_copy<ESZ, VB>((const char*)a.send[i] + (size_t)j * c * ESZ, &dst, (size_t)i * c, 1, tlo, thi);
     }
 }
 
@@ -126,8 +131,9 @@ k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
 // numbered across all blocks and dealt to CTAs round-robin, so a hot destination's many
 // tiles spread over the whole grid.  Every CTA builds the tile prefix sums in shared
 // memory from the device tables.
+// Three copy widths are inlined here, so the kernel keeps 128 registers: one CTA per SM.
 template <int ESZ>
-__global__ void __launch_bounds__(kOnePassThreads)
+__global__ void __launch_bounds__(kOnePassThreads, 1)
 k_alltoallv(const __grid_constant__ A2AvArgs a) {
     __shared__ unsigned long long tileStart[VCOMM_MAX_RANKS * VCOMM_MAX_RANKS + 1];
     __shared__ int sBad;
@@ -161,39 +167,41 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
         const size_t lo = k * tileElems, hi = min(lo + tileElems, cnt);
         const char* src = (const char*)a.send[i] + (size_t)a.sdispls[p] * ESZ;
         char* dst = (char*)a.recv[j] + (size_t)a.rdispls[j * N + i] * ESZ;
-        const bool vec = ((((uintptr_t)src) | ((uintptr_t)dst)) & 15) == 0;
-        if (vec) tile_copy<ESZ, true>(src, &dst, 0, 1, lo, hi);
-        else tile_copy<ESZ, false>(src, &dst, 0, 1, lo, hi);
+        const uintptr_t al = ((uintptr_t)src | (uintptr_t)dst) & 31;
+        if (al == 0) tile_copy<ESZ, 32>(src, &dst, 0, 1, lo, hi);
+        else if ((al & 15) == 0) tile_copy<ESZ, 16>(src, &dst, 0, 1, lo, hi);
+        else tile_copy<ESZ, 0>(src, &dst, 0, 1, lo, hi);
     }
 }
 
 // ---- dispatch --------------------------------------------------------------------------
 
+#define VC_COPY_LAUNCH_ESZ(KERNEL, E)                                                      \
+    do {                                                                                   \
+        if (vb == 32) KERNEL<E, 32><<<grid, threads, 0, s>>>(a);                           \
+        else if (vb == 16) KERNEL<E, 16><<<grid, threads, 0, s>>>(a);                      \
+        else KERNEL<E, 0><<<grid, threads, 0, s>>>(a);                                     \
+    } while (0)
+
 #define VC_COPY_LAUNCH(KERNEL)                                                             \
     do {                                                                                   \
-        if (elemSize == 4) {                                                               \
-            if (vec) KERNEL<4, true><<<grid, threads, 0, s>>>(a);                          \
-            else KERNEL<4, false><<<grid, threads, 0, s>>>(a);                             \
-        } else if (elemSize == 2) {                                                        \
-            if (vec) KERNEL<2, true><<<grid, threads, 0, s>>>(a);                          \
-            else KERNEL<2, false><<<grid, threads, 0, s>>>(a);                             \
-        } else {                                                                           \
-            return cudaErrorInvalidValue;                                                  \
-        }                                                                                  \
+        if (elemSize == 4) VC_COPY_LAUNCH_ESZ(KERNEL, 4);                                  \
+        else if (elemSize == 2) VC_COPY_LAUNCH_ESZ(KERNEL, 2);                             \
+        else return cudaErrorInvalidValue;                                                 \
         return cudaGetLastError();                                                         \
     } while (0)
 
-cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s) {
     VC_COPY_LAUNCH(k_allgather_onepass);
 }
 
-cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s) {
     VC_COPY_LAUNCH(k_broadcast_onepass);
 }
 
-cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, bool vec, int grid,
+cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                     int threads, cudaStream_t s) {
     VC_COPY_LAUNCH(k_alltoall_onepass);
 }

@@ -18,20 +18,21 @@
 
 namespace vc {
 
-// Load the element vector at element offset `off` of every rank, starting at rank
-// `first` and wrapping, and reduce in that order.  Up to 8 loads are in flight before the
-// first use.
-template <int DT, int OP>
-__device__ __forceinline__ uint4 reduce_vec_ring(const OnePassArgs& a, int first, size_t boff) {
+// Load the VB-byte vector at byte offset `boff` of every rank, starting at rank `first`
+// and wrapping, and reduce in that order.  Up to 8 loads are in flight before the first use.
+template <int DT, int OP, int VB>
+__device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const OnePassArgs& a, int first,
+                                                                size_t boff) {
+    using VT = typename VecOf<VB>::T;
     const int N = a.nRanks;
-    uint4 acc = ld_stream((const char*)a.send[first] + boff);
+    VT acc = VecOf<VB>::ld((const char*)a.send[first] + boff);
     int rk = first + 1 == N ? 0 : first + 1;
     for (int k = 1; k < N; k += 8) {
-        uint4 v[8];
+        VT v[8];
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             if (k + j < N) {
-                v[j] = ld_stream((const char*)a.send[rk] + boff);
+                v[j] = VecOf<VB>::ld((const char*)a.send[rk] + boff);
                 rk = rk + 1 == N ? 0 : rk + 1;
             }
         }
@@ -73,12 +74,14 @@ __device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch
     return s;
 }
 
-// All-reduce.  grid = nChannels * ctasPerChannel.
-template <int DT, int OP, bool VEC>
-__global__ void __launch_bounds__(kOnePassThreads)
+// All-reduce.  grid = nChannels * ctasPerChannel.  VB: 0 (element path), 16 or 32 bytes
+// per vector; the 32-byte kernel keeps twice the registers, so it runs one 512-thread CTA
+// per SM instead of two.
+template <int DT, int OP, int VB>
+__global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
     constexpr int ESZ = DTypeOf<DT>::size;
-    constexpr int U = VEC ? 16 / ESZ : 1;
+    constexpr int U = VB ? VB / ESZ : 1;
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
@@ -94,10 +97,10 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
         const size_t hi = min(base + chEnd, a.count);
         if (e >= hi) continue;
         const int first = b + 1 == N ? 0 : b + 1;
-        if (VEC && e + U <= hi) {
+        if (VB && e + U <= hi) {
             const size_t boff = e * ESZ;
-            const uint4 acc = reduce_vec_ring<DT, OP>(a, first, boff);
-            for (int r = 0; r < N; r++) st_stream((char*)a.recv[r] + boff, acc);
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a, first, boff);
+            for (int r = 0; r < N; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
         } else {
             for (size_t x = e; x < min(e + U, hi); x++) {
                 const uint32_t acc = reduce_elem_ring<DT, OP>(a, first, x);
@@ -141,6 +144,14 @@ __device__ __forceinline__ void store_epilogue_vec(void* outBase, size_t outElem
 }
 
 template <int DT, int OUT>
+__device__ __forceinline__ void store_epilogue_vec(void* outBase, size_t outElem, const V32& acc,
+                                                   bool hasScale, float scale) {
+    constexpr int VE = 16 / DTypeOf<DT>::size;
+    store_epilogue_vec<DT, OUT>(outBase, outElem, acc.lo, hasScale, scale);
+    store_epilogue_vec<DT, OUT>(outBase, outElem + VE, acc.hi, hasScale, scale);
+}
+
+template <int DT, int OUT>
 __device__ __forceinline__ void store_epilogue_elem(void* outBase, size_t outElem, uint32_t acc,
                                                     bool hasScale, float scale) {
     constexpr int OSZ = DTypeOf<OUT>::size;
@@ -154,12 +165,12 @@ __device__ __forceinline__ void store_epilogue_elem(void* outBase, size_t outEle
 }
 
 // Reduce-scatter: block r = [r*rc, (r+1)*rc) of every send buffer lands in recv[r].
-// a.count = N * rc, a.blockElems = rc.  VEC requires rc % (16 / esz) == 0.
-template <int DT, int OP, int OUT, bool VEC>
-__global__ void __launch_bounds__(kOnePassThreads)
+// a.count = N * rc, a.blockElems = rc.  VB > 0 requires rc * esz % VB == 0.
+template <int DT, int OP, int OUT, int VB>
+__global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     constexpr int ESZ = DTypeOf<DT>::size;
-    constexpr int U = VEC ? 16 / ESZ : 1;
+    constexpr int U = VB ? VB / ESZ : 1;
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
@@ -176,8 +187,8 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
         if (t >= chEnd) continue;
         const size_t base = (size_t)r * rc;
         const int first = r + 1 == N ? 0 : r + 1;
-        if (VEC && t + U <= chEnd) {
-            const uint4 acc = reduce_vec_ring<DT, OP>(a, first, (base + t) * ESZ);
+        if (VB && t + U <= chEnd) {
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a, first, (base + t) * ESZ);
             store_epilogue_vec<DT, OUT>(a.recv[r], t, acc, hasScale, a.scale);
         } else {
             for (size_t x = t; x < min(t + U, chEnd); x++) {
@@ -191,70 +202,72 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
 // ---- dispatch --------------------------------------------------------------------------
 
 template <int DT, int OP>
-static cudaError_t ar_dispatch_vec(const OnePassArgs& a, bool vec, int grid, int threads,
+static cudaError_t ar_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
                                    cudaStream_t s) {
-    if (vec) k_allreduce_onepass<DT, OP, true><<<grid, threads, 0, s>>>(a);
-    else k_allreduce_onepass<DT, OP, false><<<grid, threads, 0, s>>>(a);
+    if (vb == 32) k_allreduce_onepass<DT, OP, 32><<<grid, threads, 0, s>>>(a);
+    else if (vb == 16) k_allreduce_onepass<DT, OP, 16><<<grid, threads, 0, s>>>(a);
+    else k_allreduce_onepass<DT, OP, 0><<<grid, threads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 template <int DT>
-static cudaError_t ar_dispatch_op(const OnePassArgs& a, vRedOp_t op, bool vec, int grid, int threads,
+static cudaError_t ar_dispatch_op(const OnePassArgs& a, vRedOp_t op, int vb, int grid, int threads,
                                   cudaStream_t s) {
     switch (op) {
-    case vSum: return ar_dispatch_vec<DT, kSum>(a, vec, grid, threads, s);
-    case vProd: return ar_dispatch_vec<DT, kProd>(a, vec, grid, threads, s);
-    case vMin: return ar_dispatch_vec<DT, kMin>(a, vec, grid, threads, s);
-    case vMax: return ar_dispatch_vec<DT, kMax>(a, vec, grid, threads, s);
+    case vSum: return ar_dispatch_vec<DT, kSum>(a, vb, grid, threads, s);
+    case vProd: return ar_dispatch_vec<DT, kProd>(a, vb, grid, threads, s);
+    case vMin: return ar_dispatch_vec<DT, kMin>(a, vb, grid, threads, s);
+    case vMax: return ar_dispatch_vec<DT, kMax>(a, vb, grid, threads, s);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, bool vec,
+cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, int vb,
                                      int grid, int threads, cudaStream_t s) {
     switch (dt) {
-    case vFloat32: return ar_dispatch_op<kF32>(a, op, vec, grid, threads, s);
-    case vFloat16: return ar_dispatch_op<kF16>(a, op, vec, grid, threads, s);
-    case vBFloat16: return ar_dispatch_op<kBF16>(a, op, vec, grid, threads, s);
-    case vInt32: return ar_dispatch_op<kI32>(a, op, vec, grid, threads, s);
+    case vFloat32: return ar_dispatch_op<kF32>(a, op, vb, grid, threads, s);
+    case vFloat16: return ar_dispatch_op<kF16>(a, op, vb, grid, threads, s);
+    case vBFloat16: return ar_dispatch_op<kBF16>(a, op, vb, grid, threads, s);
+    case vInt32: return ar_dispatch_op<kI32>(a, op, vb, grid, threads, s);
     }
     return cudaErrorInvalidValue;
 }
 
 template <int DT, int OP, int OUT>
-static cudaError_t rs_dispatch_vec(const OnePassArgs& a, bool vec, int grid, int threads,
+static cudaError_t rs_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
                                    cudaStream_t s) {
-    if (vec) k_reduce_scatter_onepass<DT, OP, OUT, true><<<grid, threads, 0, s>>>(a);
-    else k_reduce_scatter_onepass<DT, OP, OUT, false><<<grid, threads, 0, s>>>(a);
+    if (vb == 32) k_reduce_scatter_onepass<DT, OP, OUT, 32><<<grid, threads, 0, s>>>(a);
+    else if (vb == 16) k_reduce_scatter_onepass<DT, OP, OUT, 16><<<grid, threads, 0, s>>>(a);
+    else k_reduce_scatter_onepass<DT, OP, OUT, 0><<<grid, threads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 template <int DT, int OUT>
-static cudaError_t rs_dispatch_op(const OnePassArgs& a, vRedOp_t op, bool vec, int grid,
+static cudaError_t rs_dispatch_op(const OnePassArgs& a, vRedOp_t op, int vb, int grid,
                                   int threads, cudaStream_t s) {
     switch (op) {
-    case vSum: return rs_dispatch_vec<DT, kSum, OUT>(a, vec, grid, threads, s);
-    case vProd: return rs_dispatch_vec<DT, kProd, OUT>(a, vec, grid, threads, s);
-    case vMin: return rs_dispatch_vec<DT, kMin, OUT>(a, vec, grid, threads, s);
-    case vMax: return rs_dispatch_vec<DT, kMax, OUT>(a, vec, grid, threads, s);
+    case vSum: return rs_dispatch_vec<DT, kSum, OUT>(a, vb, grid, threads, s);
+    case vProd: return rs_dispatch_vec<DT, kProd, OUT>(a, vb, grid, threads, s);
+    case vMin: return rs_dispatch_vec<DT, kMin, OUT>(a, vb, grid, threads, s);
+    case vMax: return rs_dispatch_vec<DT, kMax, OUT>(a, vb, grid, threads, s);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
-                                          vDataType_t outType, bool vec, int grid, int threads,
+                                          vDataType_t outType, int vb, int grid, int threads,
                                           cudaStream_t s) {
     const bool toF32 = outType == vFloat32 && dt != vFloat32;
     if (outType != dt && !toF32) return cudaErrorInvalidValue;
     switch (dt) {
-    case vFloat32: return rs_dispatch_op<kF32, kF32>(a, op, vec, grid, threads, s);
+    case vFloat32: return rs_dispatch_op<kF32, kF32>(a, op, vb, grid, threads, s);
     case vFloat16:
-        return toF32 ? rs_dispatch_op<kF16, kF32>(a, op, vec, grid, threads, s)
-                     : rs_dispatch_op<kF16, kF16>(a, op, vec, grid, threads, s);
+        return toF32 ? rs_dispatch_op<kF16, kF32>(a, op, vb, grid, threads, s)
+                     : rs_dispatch_op<kF16, kF16>(a, op, vb, grid, threads, s);
     case vBFloat16:
-        return toF32 ? rs_dispatch_op<kBF16, kF32>(a, op, vec, grid, threads, s)
-                     : rs_dispatch_op<kBF16, kBF16>(a, op, vec, grid, threads, s);
-    case vInt32: return rs_dispatch_op<kI32, kI32>(a, op, vec, grid, threads, s);
+        return toF32 ? rs_dispatch_op<kBF16, kF32>(a, op, vb, grid, threads, s)
+                     : rs_dispatch_op<kBF16, kBF16>(a, op, vb, grid, threads, s);
+    case vInt32: return rs_dispatch_op<kI32, kI32>(a, op, vb, grid, threads, s);
     }
     return cudaErrorInvalidValue;
 }

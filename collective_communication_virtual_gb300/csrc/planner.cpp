@@ -72,13 +72,17 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     }
     p->blockElems = B;
     p->nChannels = q->nChannels;
-    p->channelElems = B ? align_up(div_up(B, (size_t)q->nChannels), VE) : 0;
+    // Channel ranges start on 32 bytes, so either vector width fits inside them.
+    p->channelElems = B ? align_up(div_up(B, (size_t)q->nChannels), 32 / esz) : 0;
 
     // ---- vector path ------------------------------------------------------------------
     bool vec = q->aligned16 != 0;
     if (q->coll == vCollReduceScatter || q->coll == vCollAllGather || q->coll == vCollAllToAll)
         vec = vec && (count % VE == 0);        // block starts r*count must stay 16-byte aligned
     p->vectorized = vec ? 1 : 0;
+    // 32-byte accesses when every block (and so every vector) starts on 32 bytes.
+    const bool v32 = vec && q->aligned32 != 0 && (B * esz) % 32 == 0;
+    p->vecBytes = v32 ? 32 : vec ? 16 : 0;
 
     // ---- algorithm --------------------------------------------------------------------
     bool ring = q->algo == vAlgoRing && N > 1 &&
@@ -103,8 +107,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         // channels; never more CTAs than a channel has vectors to move.
         p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
         p->threadsPerCta = vc::kOnePassThreads;
-        // Round down so the grid never spills into a second, mostly idle wave.
-        const int target = 2 * smCount;
+        // Round down so the grid never spills into a second, mostly idle wave.  The
+        // 32-byte kernels hold twice the registers: one CTA per SM.
+        const int target = (p->vecBytes == 32 ? 1 : 2) * smCount;
         int per = std::max(1, target / q->nChannels);
         // Never more CTAs than a channel has work items: for the reductions a work item is
         // one thread's unit (a 16-byte vector of every rank), for the copies a 64 KiB tile.
@@ -114,7 +119,8 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         } else {
             const size_t chElems = std::min(p->channelElems, B);
             if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter) {
-                maxPer = div_up(div_up(chElems, vec ? VE : 1) * (size_t)N, (size_t)p->threadsPerCta);
+                const size_t unit = p->vecBytes ? p->vecBytes / esz : 1;
+                maxPer = div_up(div_up(chElems, unit) * (size_t)N, (size_t)p->threadsPerCta);
             } else {
                 size_t blocks = q->coll == vCollBroadcast ? 1 : q->coll == vCollAllGather ? (size_t)N : (size_t)N * N;
                 maxPer = div_up(chElems * esz, (size_t)64 * 1024) * blocks;
@@ -122,7 +128,7 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         }
         maxPer = std::max<size_t>(1, maxPer);
         per = (int)std::min<size_t>((size_t)per, maxPer);
-        if (q->coll == vCollAllToAllv) { p->nChannels = 1; per = target; }
+        if (q->coll == vCollAllToAllv) { p->nChannels = 1; per = smCount; }   // 1 CTA per SM
         p->ctasPerChannel = per;
         p->gridCtas = per * p->nChannels;
         (void)total;
@@ -155,6 +161,7 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     p->threadsPerCta = vc::kRingThreads;
     // The 16-byte path of the ring also needs every slot and chunk to start on a vector.
     if (p->slotPayloadElems % VE != 0) p->vectorized = 0;
+    p->vecBytes = p->vectorized ? 16 : 0;
     return vSuccess;
 }
 

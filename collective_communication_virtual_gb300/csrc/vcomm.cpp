@@ -143,24 +143,25 @@ void debug_plan(const vcomm* c, int coll, size_t count, int dt, const vPlanInfo_
 
 bool ptr_aligned(const void* p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-// Common checks of the pointer arrays.  Returns vSuccess and sets *aligned16.
+// Common checks of the pointer arrays.  Returns vSuccess and sets *aligned to the largest
+// power-of-two alignment (up to 32 bytes) that every pointer has.
 vResult_t check_ptrs(const vcomm* c, const void* const* send, void* const* recv, size_t esz,
-                     int root, bool needAllSend, int* aligned16) {
+                     int root, bool needAllSend, int* aligned) {
     if (!send || !recv) return vInvalidArgument;
-    bool a16 = true;
+    uintptr_t bits = 32;
     for (int r = 0; r < c->nRanks; r++) {
         if (needAllSend || r == root) {
             if (!send[r] || !ptr_aligned(send[r], esz)) return vInvalidArgument;
-            a16 = a16 && ptr_aligned(send[r], 16);
+            bits |= (uintptr_t)send[r];
         }
         if (!recv[r] || !ptr_aligned(recv[r], esz)) return vInvalidArgument;
-        a16 = a16 && ptr_aligned(recv[r], 16);
+        bits |= (uintptr_t)recv[r];
     }
-    *aligned16 = a16 ? 1 : 0;
+    *aligned = (int)(bits & (~bits + 1));       // lowest set bit, at most 32
     return vSuccess;
 }
 
-vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned16, vPlanInfo_t* p) {
+vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned, vPlanInfo_t* p) {
     vPlanRequest_t q;
     std::memset(&q, 0, sizeof(q));
     q.nRanks = c->nRanks;
@@ -171,7 +172,8 @@ vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned1
     q.datatype = dt;
     q.count = count;
     q.chunkBytes = c->cfg.chunkBytes;
-    q.aligned16 = aligned16;
+    q.aligned16 = aligned >= 16 ? 1 : 0;
+    q.aligned32 = aligned >= 32 ? 1 : 0;
     q.smCount = c->smCount;
     q.l2Bytes = c->l2Bytes;
     return vPlanCompute(&q, p);
@@ -319,7 +321,7 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
 // Shared front half of every collective.
 struct Front {
     vResult_t res;
-    int aligned16;
+    int aligned;        // common pointer alignment in bytes (up to 32)
 };
 
 Front front(vcomm* c, const void* const* send, void* const* recv, size_t count, int dt, int root,
@@ -334,7 +336,7 @@ Front front(vcomm* c, const void* const* send, void* const* recv, size_t count, 
     const size_t n2 = (size_t)c->nRanks * (size_t)c->nRanks;
     if (count > ((size_t)1 << 62) / (n2 * esz)) { f.res = vInvalidArgument; return f; }
     if (count == 0) return f;
-    f.res = check_ptrs(c, send, recv, esz, root, needAllSend, &f.aligned16);
+    f.res = check_ptrs(c, send, recv, esz, root, needAllSend, &f.aligned);
     return f;
 }
 
@@ -463,10 +465,10 @@ vResult_t vcommTestSetStallRank(vcomm_t c, int rank) {
     return vSuccess;
 }
 
-vResult_t vcommQueryPlan(vcomm_t c, vColl_t coll, size_t count, vDataType_t dt, int aligned16,
+vResult_t vcommQueryPlan(vcomm_t c, vColl_t coll, size_t count, vDataType_t dt, int aligned,
                          vPlanInfo_t* plan) {
     if (!comm_ok(c) || !plan) return vInvalidArgument;
-    return make_plan(c, coll, count, dt, aligned16, plan);
+    return make_plan(c, coll, count, dt, aligned, plan);
 }
 
 vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
@@ -477,14 +479,14 @@ vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, v
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
-    vResult_t r = make_plan(c, vCollAllReduce, count, dt, f.aligned16, &p);
+    vResult_t r = make_plan(c, vCollAllReduce, count, dt, f.aligned, &p);
     if (r != vSuccess) return r;
     debug_plan(c, vCollAllReduce, count, dt, p);
     if (p.algo == vAlgoRing)
         return launch_ring_plan(c, vCollAllReduce, send, recv, count, dt, op, dt, 0, false, 1.0f, p, stream);
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, count);
-    return finish_launch(c, vc::launch_allreduce_onepass(a, dt, op, p.vectorized != 0, p.gridCtas,
+    return finish_launch(c, vc::launch_allreduce_onepass(a, dt, op, p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "allreduce");
 }
 
@@ -500,7 +502,7 @@ static vResult_t reduce_scatter_impl(const void* const* send, void* const* recv,
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
-    vResult_t r = make_plan(c, vCollReduceScatter, rc, dt, f.aligned16, &p);
+    vResult_t r = make_plan(c, vCollReduceScatter, rc, dt, f.aligned, &p);
     if (r != vSuccess) return r;
     debug_plan(c, vCollReduceScatter, rc, dt, p);
     if (p.algo == vAlgoRing)
@@ -510,7 +512,7 @@ static vResult_t reduce_scatter_impl(const void* const* send, void* const* recv,
     fill_onepass(&a, c, send, recv, p, rc * (size_t)c->nRanks);
     a.hasScale = hasScale ? 1 : 0;
     a.scale = scale;
-    return finish_launch(c, vc::launch_reduce_scatter_onepass(a, dt, op, outType, p.vectorized != 0,
+    return finish_launch(c, vc::launch_reduce_scatter_onepass(a, dt, op, outType, p.vecBytes,
                                                               p.gridCtas, p.threadsPerCta, stream),
                          stream, "reduce_scatter");
 }
@@ -535,14 +537,14 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
-    vResult_t r = make_plan(c, vCollAllGather, sendcount, dt, f.aligned16, &p);
+    vResult_t r = make_plan(c, vCollAllGather, sendcount, dt, f.aligned, &p);
     if (r != vSuccess) return r;
     debug_plan(c, vCollAllGather, sendcount, dt, p);
     if (p.algo == vAlgoRing)
         return launch_ring_plan(c, vCollAllGather, send, recv, sendcount, dt, vSum, dt, 0, false, 1.0f, p, stream);
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, sendcount);
-    return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vectorized != 0, p.gridCtas,
+    return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "allgather");
 }
 
@@ -556,7 +558,7 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
-    vResult_t r = make_plan(c, vCollBroadcast, count, dt, f.aligned16, &p);
+    vResult_t r = make_plan(c, vCollBroadcast, count, dt, f.aligned, &p);
     if (r != vSuccess) return r;
     debug_plan(c, vCollBroadcast, count, dt, p);
     if (p.algo == vAlgoRing) {
@@ -567,7 +569,7 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, count);
     a.root = root;
-    return finish_launch(c, vc::launch_broadcast_onepass(a, (int)elem_size(dt), p.vectorized != 0, p.gridCtas,
+    return finish_launch(c, vc::launch_broadcast_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "broadcast");
 }
 
@@ -579,12 +581,12 @@ vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vD
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
-    vResult_t r = make_plan(c, vCollAllToAll, count, dt, f.aligned16, &p);
+    vResult_t r = make_plan(c, vCollAllToAll, count, dt, f.aligned, &p);
     if (r != vSuccess) return r;
     debug_plan(c, vCollAllToAll, count, dt, p);
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, count);
-    return finish_launch(c, vc::launch_alltoall_onepass(a, (int)elem_size(dt), p.vectorized != 0, p.gridCtas,
+    return finish_launch(c, vc::launch_alltoall_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                         p.threadsPerCta, stream), stream, "alltoall");
 }
 
@@ -596,13 +598,13 @@ vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* 
     if (s != vSuccess) return s;
     const size_t esz = elem_size(dt);
     if (esz == 0 || !counts || !sdispls || !rdispls) return vInvalidArgument;
-    int aligned16 = 0;
-    vResult_t r = check_ptrs(c, send, recv, esz, 0, true, &aligned16);
+    int aligned = 0;
+    vResult_t r = check_ptrs(c, send, recv, esz, 0, true, &aligned);
     if (r != vSuccess) return r;
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
-    r = make_plan(c, vCollAllToAllv, 0, dt, aligned16, &p);
+    r = make_plan(c, vCollAllToAllv, 0, dt, aligned, &p);
     if (r != vSuccess) return r;
     debug_plan(c, vCollAllToAllv, 0, dt, p);
     vc::A2AvArgs a;

@@ -43,7 +43,8 @@ class vPlanRequest_t(ctypes.Structure):
     _fields_ = [("nRanks", ctypes.c_int), ("nChannels", ctypes.c_int), ("proto", ctypes.c_int),
                 ("algo", ctypes.c_int), ("coll", ctypes.c_int), ("datatype", ctypes.c_int),
                 ("count", ctypes.c_size_t), ("chunkBytes", ctypes.c_size_t),
-                ("aligned16", ctypes.c_int), ("smCount", ctypes.c_int), ("l2Bytes", ctypes.c_size_t)]
+                ("aligned16", ctypes.c_int), ("smCount", ctypes.c_int), ("l2Bytes", ctypes.c_size_t),
+                ("aligned32", ctypes.c_int)]
 
 
 class vPlanInfo_t(ctypes.Structure):
@@ -54,7 +55,7 @@ class vPlanInfo_t(ctypes.Structure):
                 ("channelElems", ctypes.c_size_t), ("chunkElems", ctypes.c_size_t),
                 ("slotPayloadElems", ctypes.c_size_t), ("slotBytes", ctypes.c_size_t),
                 ("fifoBytes", ctypes.c_size_t), ("minBytes", ctypes.c_double),
-                ("busFactor", ctypes.c_double)]
+                ("busFactor", ctypes.c_double), ("vecBytes", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -208,9 +209,10 @@ def vcommTestSetStallRank(comm, rank: int) -> None:
     _check(lib().vcommTestSetStallRank(comm, rank), "vcommTestSetStallRank")
 
 
-def vcommQueryPlan(comm, coll: int, count: int, datatype, aligned16: bool = True) -> dict:
+def vcommQueryPlan(comm, coll: int, count: int, datatype, aligned: int = 32) -> dict:
+    """The plan for buffers whose pointers share `aligned`-byte alignment (1..32)."""
     info = vPlanInfo_t()
-    _check(lib().vcommQueryPlan(comm, coll, count, _dtype_code(datatype), int(aligned16),
+    _check(lib().vcommQueryPlan(comm, coll, count, _dtype_code(datatype), int(aligned),
                                 ctypes.byref(info)), "vcommQueryPlan")
     return info.as_dict()
 

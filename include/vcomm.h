@@ -235,6 +235,7 @@ typedef struct {
     int aligned16;             /* 1 if every buffer pointer is 16-byte aligned */
     int smCount;               /* streaming multiprocessors of the device */
     size_t l2Bytes;            /* L2 cache size of the device */
+    int aligned32;             /* 1 if every buffer pointer is 32-byte aligned */
 } vPlanRequest_t;
 
 typedef struct {
@@ -254,6 +255,7 @@ typedef struct {
     size_t fifoBytes;          /* ring: bytes of one (channel, rank) FIFO, 8 slots */
     double minBytes;           /* algorithmic minimum HBM bytes read + written */
     double busFactor;          /* busBW = algBW * busFactor (nSteps / nRanks) */
+    int vecBytes;              /* bytes per vector access of the one-pass kernels: 0, 16, 32 */
 } vPlanInfo_t;
 
 /* Compute the plan a collective with these parameters would run.  Pure host
@@ -271,9 +273,10 @@ vResult_t vPlanChannelRange(const vPlanInfo_t* plan, size_t count, int channel, 
  * transfer ends with the sticky error vTimeout.  -1 turns the hook off. */
 vResult_t vcommTestSetStallRank(vcomm_t comm, int rank);
 
-/* vPlanCompute for this communicator's device and settings. */
+/* vPlanCompute for this communicator's device and settings.  `aligned` is the largest
+ * power-of-two alignment (in bytes, up to 32) shared by every buffer pointer. */
 vResult_t vcommQueryPlan(vcomm_t comm, vColl_t coll, size_t count, vDataType_t datatype,
-                         int aligned16, vPlanInfo_t* plan);
+                         int aligned, vPlanInfo_t* plan);
 
 #ifdef __cplusplus
 }

@@ -107,6 +107,9 @@ def test_allreduce_unaligned_and_inplace(comms, variant):
         xs = inputs.uniform_ranks(8, 50_001, dtype, 7)
         want = oracle.allreduce(xs, "sum")
         assert_bits_equal(run_allreduce(comms, xs, "sum", algo, proto, pad=1), want, "unaligned")
+        # 16-byte but not 32-byte aligned buffers take the 16-byte vector path
+        assert_bits_equal(run_allreduce(comms, xs, "sum", algo, proto, pad=16 // xs[0].element_size()),
+                          want, "16-byte aligned")
         assert_bits_equal(run_allreduce(comms, xs, "sum", algo, proto, inplace=True), want, "in place")
 
 

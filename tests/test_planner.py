@@ -18,7 +18,7 @@ def _lib():
 def plan(**kw):
     req = dict(nRanks=8, nChannels=1, proto=V.vProtoSimple, algo=V.vAlgoAuto, coll=V.vCollAllReduce,
                datatype=V.vFloat32, count=1024, chunkBytes=0, aligned16=1, smCount=152,
-               l2Bytes=126 << 20)
+               l2Bytes=126 << 20, aligned32=0)
     req.update(kw)
     return V.vPlanCompute(**req)
 
@@ -117,6 +117,22 @@ def test_traffic_and_bus_factor():
     assert p.minBytes == S + n * S
     p = plan(nRanks=n, count=count, coll=V.vCollAllToAll)
     assert p.minBytes == 2 * n * n * S
+
+
+def test_32_byte_vectors_when_blocks_and_pointers_allow():
+    # B = 2M fp32 elements (8 MiB): a multiple of 32 bytes
+    p = plan(count=16 << 20, aligned32=1)
+    assert p.vecBytes == 32 and p.gridCtas == 152          # one 512-thread CTA per SM
+    assert plan(count=16 << 20, aligned32=0).vecBytes == 16
+    # B = alignUp(513, 4) = 516 elements = 2064 bytes: 16-byte blocks only
+    assert plan(count=4099, aligned32=1).vecBytes == 16
+    assert plan(count=4099, aligned16=0, aligned32=0).vecBytes == 0
+    assert plan(coll=V.vCollReduceScatter, count=4096, aligned32=1).vecBytes == 32
+    assert plan(coll=V.vCollAllGather, count=4096, aligned32=1).vecBytes == 32
+    assert plan(coll=V.vCollAllGather, count=4100, aligned32=1).vecBytes == 16
+    for n, count, nch in [(8, 16 << 20, 32), (3, 100_003, 5)]:
+        p = plan(nRanks=n, nChannels=nch, count=count)
+        assert (p.channelElems * 4) % 32 == 0
 
 
 def test_grid_is_about_two_ctas_per_sm_and_never_idle():

@@ -108,8 +108,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
         p->threadsPerCta = vc::kOnePassThreads;
         // Round down so the grid never spills into a second, mostly idle wave.  The
-        // 32-byte kernels hold twice the registers: one CTA per SM.
-        const int target = (p->vecBytes == 32 ? 1 : 2) * smCount;
+        // 32-byte reduction kernels hold 128 registers: one CTA per SM; the copies two.
+        const bool wide = p->vecBytes == 32 && (q->coll == vCollAllReduce || q->coll == vCollReduceScatter);
+        const int target = (wide ? 1 : 2) * smCount;
         int per = std::max(1, target / q->nChannels);
         // Never more CTAs than a channel has work items: for the reductions a work item is
         // one thread's unit (a 16-byte vector of every rank), for the copies a 64 KiB tile.

@@ -129,6 +129,7 @@ def test_32_byte_vectors_when_blocks_and_pointers_allow():
     assert plan(count=4099, aligned16=0, aligned32=0).vecBytes == 0
     assert plan(coll=V.vCollReduceScatter, count=4096, aligned32=1).vecBytes == 32
     assert plan(coll=V.vCollAllGather, count=4096, aligned32=1).vecBytes == 32
+    assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1).gridCtas == 2 * 152
     assert plan(coll=V.vCollAllGather, count=4100, aligned32=1).vecBytes == 16
     for n, count, nch in [(8, 16 << 20, 32), (3, 100_003, 5)]:
         p = plan(nRanks=n, nChannels=nch, count=count)

@@ -53,6 +53,9 @@ def lib() -> ctypes.CDLL:
             "orc_broadcast": [sz, i32, sz, i32, pp, pp],
             "orc_alltoall": [sz, i32, sz, pp, pp],
             "orc_alltoallv": [sz, i32, ip, ip, ip, pp, pp],
+            "orc_reduce": [i32, i32, i32, sz, i32, pp, pp, i32],
+            "orc_gather": [sz, i32, sz, i32, pp, pp],
+            "orc_scatter": [sz, i32, sz, i32, pp, pp],
         }.items():
             f = getattr(L, name)
             f.argtypes, f.restype = args, ctypes.c_int
@@ -118,6 +121,40 @@ def reduce_scatter_scale(xs, op: str, scale: float, out_dtype=torch.float32, nth
     _ok(lib().orc_reduce_scatter_scale(DTYPE_CODE[xs[0].dtype], OP_CODE[op], n, rc,
                                        DTYPE_CODE[out_dtype], ctypes.c_float(scale), _ptrs(xs),
                                        _ptrs(out), nthreads), "reduce_scatter_scale")
+    return out
+
+
+def reduce(xs, op: str = "sum", root: int = 0, nthreads: int = 1):
+    """Reduce to root; returns the root's result (one tensor)."""
+    _check(xs)
+    n, count = len(xs), xs[0].numel()
+    out = [None] * n
+    out[root] = torch.empty_like(xs[0])
+    _ok(lib().orc_reduce(DTYPE_CODE[xs[0].dtype], OP_CODE[op], n, count, root, _ptrs(xs), _ptrs(out),
+                         nthreads), "reduce")
+    return out[root]
+
+
+def gather(xs, root: int = 0):
+    """Gather to root; returns the root's buffer (N * sendcount elements)."""
+    _check(xs)
+    n, sc = len(xs), xs[0].numel()
+    out = [None] * n
+    out[root] = torch.empty(n * sc, dtype=xs[0].dtype)
+    _ok(lib().orc_gather(xs[0].element_size(), n, sc, root, _ptrs(xs), _ptrs(out)), "gather")
+    return out[root]
+
+
+def scatter(src, n: int, root: int = 0):
+    """Scatter the root's buffer (n blocks) to n ranks; returns the n receive buffers."""
+    _check([src])
+    if src.numel() % n:
+        raise ValueError("scatter source must hold n equal blocks")
+    rc = src.numel() // n
+    send = [None] * n
+    send[root] = src
+    out = [torch.empty(rc, dtype=src.dtype) for _ in range(n)]
+    _ok(lib().orc_scatter(src.element_size(), n, rc, root, _ptrs(send), _ptrs(out)), "scatter")
     return out
 
 

@@ -30,6 +30,11 @@
  *    counts and displacements per (sender, receiver).
  *  - Non-reducing collectives are byte copies whatever the data type (NCCL book,
  *    chapter 6, taskAppend: AllGather/Broadcast run as ncclInt8).
+ *  - Reduce (to root): recv_root = the reduction of all ranks, every element in the
+ *    ring order root+1, ..., root -- the order of a ring chain that ends at the root
+ *    (collective table, reduce row; NCCL runs Reduce as such a chain).  Gather:
+ *    recv_root = concat over s of send_s.  Scatter: recv_r = block r of send_root
+ *    (collective table, gather and scatter rows).
  *  - Special cases: count 0 does nothing; N = 1 is a plain copy (taskAppend:
  *    count==0 returns at once, nRanks==1 runs a local one-rank reduction).
  *
@@ -213,9 +218,11 @@ static uint32_t ring_reduce(int dt, int op, int n, const void* const* x, size_t 
 }
 
 typedef struct {
-    int kind;                 /* 0 all-reduce, 1 reduce-scatter, 2 reduce-scatter + epilogue */
+    int kind;                 /* 0 all-reduce, 1 reduce-scatter, 2 reduce-scatter + epilogue,
+                                 3 reduce to root */
     int dt, op, n, outdt;
     size_t count, recvcount, block;
+    int root;
     float scale;
     const void* const* send;
     void* const* recv;
@@ -229,6 +236,12 @@ static void run_job(const job_t* j) {
             uint32_t acc = ring_reduce(j->dt, j->op, j->n, j->send, esz, e, e / j->block);
             for (int r = 0; r < j->n; r++) store_bits(j->recv[r], esz, e, acc);
         }
+        return;
+    }
+    if (j->kind == 3) {
+        for (size_t e = j->lo; e < j->hi; e++)
+            store_bits(j->recv[j->root], esz, e,
+                       ring_reduce(j->dt, j->op, j->n, j->send, esz, e, (size_t)j->root));
         return;
     }
     /* reduce-scatter: flat index e = r * recvcount + t, block r lands in recv[r][t] */
@@ -299,6 +312,18 @@ int orc_reduce_scatter(int dt, int op, int n, size_t recvcount, const void* cons
     return run_split(j, recvcount * (size_t)n, nthreads);
 }
 
+/* Reduce to root: only recv[root] is written. */
+int orc_reduce(int dt, int op, int n, size_t count, int root, const void* const* send,
+               void* const* recv, int nthreads) {
+    if (!valid_dt_op(dt, op) || n < 1 || root < 0 || root >= n) return -1;
+    if (count == 0) return 0;
+    if (!send || !recv || !recv[root]) return -2;
+    job_t j; memset(&j, 0, sizeof j);
+    j.kind = 3; j.dt = dt; j.op = op; j.n = n; j.count = count; j.root = root;
+    j.send = send; j.recv = recv;
+    return run_split(j, count, nthreads);
+}
+
 /* Reduce-scatter whose output element is (float)acc * scale, stored as outdt
  * (fp32, or the input type itself). */
 int orc_reduce_scatter_scale(int dt, int op, int n, size_t recvcount, int outdt, float scale,
@@ -331,6 +356,24 @@ int orc_broadcast(size_t esz, int n, size_t count, int root, const void* const* 
     if (n < 1 || esz == 0 || root < 0 || root >= n) return -1;
     if (count == 0) return 0;
     for (int r = 0; r < n; r++) memmove(recv[r], send[root], count * esz);
+    return 0;
+}
+
+int orc_gather(size_t esz, int n, size_t sendcount, int root, const void* const* send,
+               void* const* recv) {
+    if (n < 1 || esz == 0 || root < 0 || root >= n) return -1;
+    if (sendcount == 0) return 0;
+    size_t bytes = sendcount * esz;
+    for (int s = 0; s < n; s++) memcpy((char*)recv[root] + (size_t)s * bytes, send[s], bytes);
+    return 0;
+}
+
+int orc_scatter(size_t esz, int n, size_t recvcount, int root, const void* const* send,
+                void* const* recv) {
+    if (n < 1 || esz == 0 || root < 0 || root >= n) return -1;
+    if (recvcount == 0) return 0;
+    size_t bytes = recvcount * esz;
+    for (int r = 0; r < n; r++) memcpy(recv[r], (const char*)send[root] + (size_t)r * bytes, bytes);
     return 0;
 }
 

@@ -119,3 +119,13 @@ def ring_allgather(xs):
     for r in range(n):
         bufs[r][r * sc:(r + 1) * sc] = xs[r]
     return ring_allgather_chunks(bufs, [(s * sc, (s + 1) * sc) for s in range(n)])
+
+
+def ring_reduce_chain(xs, op: str, root: int):
+    """Reduce to root as a ring chain: rank root+1 sends its whole buffer to root+2, which
+    combines it with its own and passes it on, ..., until the root combines the last hop."""
+    n = len(xs)
+    partial = xs[(root + 1) % n].clone()
+    for k in range(2, n + 1):
+        partial = combine(op, partial, xs[(root + k) % n])
+    return partial

@@ -340,3 +340,49 @@ def test_threads_do_not_change_bits():
     a = oracle.allreduce(xs, "sum", nthreads=1)
     b = oracle.allreduce(xs, "sum", nthreads=7)
     assert all(_same_bits(x, y) for x, y in zip(a, b))
+
+
+# ---------------------------------------------------------------------------------------
+# Rooted collectives: reduce, gather, scatter
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=lambda d: str(d).split(".")[1])
+@pytest.mark.parametrize("op", OPS)
+def test_reduce_matches_ring_chain(dtype, op):
+    for n in (1, 2, 3, 5, 8):
+        for count in (0, 1, 7, 33, 1000):
+            xs = _inputs(n, count, dtype, seed=17 * n + count)
+            for root in {0, n - 1, n // 2}:
+                got = oracle.reduce(xs, op, root)
+                assert _same_bits(got, ring_sim.ring_reduce_chain(xs, op, root)), (n, count, root)
+
+
+def test_reduce_order_is_the_roots_block_order():
+    """Reduce to root r reduces in the order that block r of an all-reduce uses."""
+    xs = inputs.uniform_ranks(8, 4096, torch.float32, 5)
+    B = oracle.block_elems(4096, 8, 4)
+    ar = oracle.allreduce(xs, "sum")[0]
+    for root in range(8):
+        got = oracle.reduce(xs, "sum", root)
+        assert _same_bits(got[root * B:(root + 1) * B], ar[root * B:(root + 1) * B])
+
+
+def test_reduce_min_max_int_are_library_reductions():
+    xs = inputs.uniform_ranks(6, 999, torch.int32, 8)
+    s64 = torch.stack([x.to(torch.int64) for x in xs])
+    assert torch.equal(oracle.reduce(xs, "max", 2), s64.amax(0).to(torch.int32))
+    assert torch.equal(oracle.reduce(xs, "sum", 4), ring_sim._wrap32(s64.sum(0)))
+
+
+def test_gather_and_scatter_are_cat_and_chunk():
+    n = 6
+    xs = inputs.uniform_ranks(n, 77, torch.float16, 3)
+    for root in (0, 5):
+        assert _same_bits(oracle.gather(xs, root), torch.cat(xs))
+    src = inputs.uniform_ranks(1, n * 13, torch.bfloat16, 4)[0]
+    for root in (0, 3):
+        out = oracle.scatter(src, n, root)
+        assert all(_same_bits(o, c) for o, c in zip(out, src.chunk(n)))
+    # scatter of a gather gives every rank its own buffer back
+    back = oracle.scatter(oracle.gather(xs, 2), n, 2)
+    assert all(_same_bits(a, b) for a, b in zip(back, xs))

@@ -32,7 +32,10 @@ struct OnePassArgs {
     void* recv[VCOMM_MAX_RANKS];
     int nRanks;
     int ctasPerChannel;
-    int root;                        // broadcast
+    int root;                        // broadcast, scatter
+    int orderRoot;                   // >= 0: every element reduced in the order of block
+                                     // orderRoot (reduce to root); -1: per block
+    int outRoot;                     // >= 0: only recv[outRoot] is written (reduce, gather)
     int hasScale;                    // reduce-scatter epilogue
     float scale;
     size_t count;                    // AR: count; RS: N*recvcount; AG: sendcount; BC: count; A2A: block
@@ -96,6 +99,8 @@ cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb,
                                      int threads, cudaStream_t s);
 cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                     int threads, cudaStream_t s);
+cudaError_t launch_scatter_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
+                                   int threads, cudaStream_t s);
 cudaError_t launch_alltoallv(const A2AvArgs& a, int grid, int threads, cudaStream_t s);
 
 // Cooperative launch of the staged ring (all CTAs co-resident or the launch fails).

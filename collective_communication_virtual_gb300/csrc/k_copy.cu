@@ -77,6 +77,7 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
 }
 
 // All-gather: block s = send[s] lands at recv[r] + s*sc for every r.  a.count = sc.
+// Gather (a.outRoot = root) writes recv[root] only.
 template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads)
 k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
@@ -90,7 +91,11 @@ k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
         const int s = (int)(t / sp.tilesPerBlock);
         const size_t k = t - (size_t)s * sp.tilesPerBlock;
         const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
-        tile_copy<ESZ, VB>((const char*)a.send[s], (char* const*)a.recv, (size_t)s * sc, N, tlo, thi);
+        if (a.outRoot >= 0)
+            tile_copy<ESZ, VB>((const char*)a.send[s], (char* const*)&a.recv[a.outRoot], (size_t)s * sc, 1,
+                               tlo, thi);
+        else
+            tile_copy<ESZ, VB>((const char*)a.send[s], (char* const*)a.recv, (size_t)s * sc, N, tlo, thi);
     }
 }
 
@@ -124,6 +129,25 @@ k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
         const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
         char* dst = (char*)a.recv[j];
         tile_copy<ESZ, VB>((const char*)a.send[i] + (size_t)j * c * ESZ, &dst, (size_t)i * c, 1, tlo, thi);
+    }
+}
+
+// Scatter: block j of send[root] lands in recv[j].  a.count = recvcount.
+template <int ESZ, int VB>
+__global__ void __launch_bounds__(kOnePassThreads)
+k_scatter_onepass(const __grid_constant__ OnePassArgs a) {
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t c = a.count;
+    const TileSpan sp = tile_span<ESZ>(a, ch, c);
+    const size_t nTiles = sp.tilesPerBlock * (size_t)N;
+    for (size_t t = cta; t < nTiles; t += a.ctasPerChannel) {
+        const int j = (int)(t / sp.tilesPerBlock);
+        const size_t k = t - (size_t)j * sp.tilesPerBlock;
+        const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
+        char* dst = (char*)a.recv[j];
+        tile_copy<ESZ, VB>((const char*)a.send[a.root] + (size_t)j * c * ESZ, &dst, 0, 1, tlo, thi);
     }
 }
 
@@ -204,6 +228,11 @@ cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb,
 cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                     int threads, cudaStream_t s) {
     VC_COPY_LAUNCH(k_alltoall_onepass);
+}
+
+cudaError_t launch_scatter_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
+                                   int threads, cudaStream_t s) {
+    VC_COPY_LAUNCH(k_scatter_onepass);
 }
 
 cudaError_t launch_alltoallv(const A2AvArgs& a, int grid, int threads, cudaStream_t s) {

@@ -74,9 +74,10 @@ __device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch
     return s;
 }
 
-// All-reduce.  grid = nChannels * ctasPerChannel.  VB: 0 (element path), 16 or 32 bytes
-// per vector; the 32-byte kernel keeps twice the registers, so it runs one 512-thread CTA
-// per SM instead of two.
+// All-reduce, and reduce to root.  grid = nChannels * ctasPerChannel.  VB: 0 (element
+// path), 16 or 32 bytes per vector; the 32-byte kernel keeps twice the registers, so it
+// runs one 512-thread CTA per SM instead of two.  Reduce to root (a.orderRoot = a.outRoot
+// = root) reduces every block in the root's order and writes only recv[root].
 template <int DT, int OP, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
@@ -96,15 +97,18 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
         const size_t e = base + sp.lo + i * U;
         const size_t hi = min(base + chEnd, a.count);
         if (e >= hi) continue;
-        const int first = b + 1 == N ? 0 : b + 1;
+        const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
+        const int first = ob + 1 == N ? 0 : ob + 1;
+        const int r0 = a.outRoot >= 0 ? a.outRoot : 0;
+        const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
         if (VB && e + U <= hi) {
             const size_t boff = e * ESZ;
             const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a, first, boff);
-            for (int r = 0; r < N; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
+            for (int r = r0; r < r1; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
         } else {
             for (size_t x = e; x < min(e + U, hi); x++) {
                 const uint32_t acc = reduce_elem_ring<DT, OP>(a, first, x);
-                for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], x, acc);
+                for (int r = r0; r < r1; r++) st_elem<ESZ>(a.recv[r], x, acc);
             }
         }
     }

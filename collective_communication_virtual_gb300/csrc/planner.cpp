@@ -46,7 +46,7 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     const int N = q->nRanks;
     if (N < 1 || N > VCOMM_MAX_RANKS) return vInvalidArgument;
     if (q->nChannels < 1 || q->nChannels > VCOMM_MAX_CHANNELS) return vInvalidArgument;
-    if (q->coll < vCollAllReduce || q->coll > vCollAllToAllv) return vInvalidArgument;
+    if (q->coll < vCollAllReduce || q->coll > vCollScatter) return vInvalidArgument;
     if (q->proto < vProtoSimple || q->proto > vProtoAuto) return vInvalidArgument;
     if (q->algo < vAlgoAuto || q->algo > vAlgoRing) return vInvalidArgument;
     const size_t esz = elem_size(q->datatype);
@@ -69,6 +69,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     case vCollBroadcast: B = count; total = count; break;
     case vCollAllToAll: B = count; total = count * (size_t)N * (size_t)N; break;
     case vCollAllToAllv: B = 0; total = 0; break;
+    case vCollReduce: B = align_up(div_up(count, (size_t)N), VE); total = count; break;
+    case vCollGather: B = count; total = count * (size_t)N; break;
+    case vCollScatter: B = count; total = count * (size_t)N; break;
     }
     p->blockElems = B;
     p->nChannels = q->nChannels;
@@ -77,7 +80,8 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
 
     // ---- vector path ------------------------------------------------------------------
     bool vec = q->aligned16 != 0;
-    if (q->coll == vCollReduceScatter || q->coll == vCollAllGather || q->coll == vCollAllToAll)
+    if (q->coll == vCollReduceScatter || q->coll == vCollAllGather || q->coll == vCollAllToAll ||
+        q->coll == vCollGather || q->coll == vCollScatter)
         vec = vec && (count % VE == 0);        // block starts r*count must stay 16-byte aligned
     p->vectorized = vec ? 1 : 0;
     // 32-byte accesses when every block (and so every vector) starts on 32 bytes.
@@ -99,6 +103,8 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     case vCollAllGather: p->minBytes = (double)N * S + (double)N * N * S; p->busFactor = (double)(N - 1) / N; break;
     case vCollBroadcast: p->minBytes = S + (double)N * S; p->busFactor = (double)(N - 1) / N; break;
     case vCollAllToAll: p->minBytes = 2.0 * N * N * S; p->busFactor = (double)(N - 1) / N; break;
+    case vCollReduce: p->minBytes = (double)N * S + S; p->busFactor = (double)(N - 1) / N; break;
+    case vCollGather: case vCollScatter: p->minBytes = 2.0 * N * S; p->busFactor = (double)(N - 1) / N; break;
     default: p->minBytes = 0; p->busFactor = (double)(N - 1) / N; break;
     }
 
@@ -109,7 +115,8 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         p->threadsPerCta = vc::kOnePassThreads;
         // Round down so the grid never spills into a second, mostly idle wave.  The
         // 32-byte reduction kernels hold 128 registers: one CTA per SM; the copies two.
-        const bool wide = p->vecBytes == 32 && (q->coll == vCollAllReduce || q->coll == vCollReduceScatter);
+        const bool wide = p->vecBytes == 32 && (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ||
+                                                q->coll == vCollReduce);
         const int target = (wide ? 1 : 2) * smCount;
         int per = std::max(1, target / q->nChannels);
         // Never more CTAs than a channel has work items: for the reductions a work item is
@@ -119,11 +126,11 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
             maxPer = (size_t)target;
         } else {
             const size_t chElems = std::min(p->channelElems, B);
-            if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter) {
+            if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter || q->coll == vCollReduce) {
                 const size_t unit = p->vecBytes ? p->vecBytes / esz : 1;
                 maxPer = div_up(div_up(chElems, unit) * (size_t)N, (size_t)p->threadsPerCta);
             } else {
-                size_t blocks = q->coll == vCollBroadcast ? 1 : q->coll == vCollAllGather ? (size_t)N : (size_t)N * N;
+                size_t blocks = q->coll == vCollBroadcast ? 1 : q->coll == vCollAllToAll ? (size_t)N * N : (size_t)N;
                 maxPer = div_up(chElems * esz, (size_t)64 * 1024) * blocks;
             }
         }

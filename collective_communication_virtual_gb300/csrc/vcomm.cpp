@@ -127,8 +127,9 @@ void free_comm(vcomm* c) {
 }
 
 const char* coll_name(int coll) {
-    static const char* n[] = {"AllReduce", "ReduceScatter", "AllGather", "Broadcast", "AllToAll", "AllToAllv"};
-    return (coll >= 0 && coll <= 5) ? n[coll] : "?";
+    static const char* n[] = {"AllReduce", "ReduceScatter", "AllGather", "Broadcast", "AllToAll",
+                              "AllToAllv", "Reduce", "Gather", "Scatter"};
+    return (coll >= 0 && coll <= 8) ? n[coll] : "?";
 }
 
 void debug_plan(const vcomm* c, int coll, size_t count, int dt, const vPlanInfo_t& p) {
@@ -146,7 +147,7 @@ bool ptr_aligned(const void* p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0
 // Common checks of the pointer arrays.  Returns vSuccess and sets *aligned to the largest
 // power-of-two alignment (up to 32 bytes) that every pointer has.
 vResult_t check_ptrs(const vcomm* c, const void* const* send, void* const* recv, size_t esz,
-                     int root, bool needAllSend, int* aligned) {
+                     int root, bool needAllSend, int* aligned, bool needAllRecv = true) {
     if (!send || !recv) return vInvalidArgument;
     uintptr_t bits = 32;
     for (int r = 0; r < c->nRanks; r++) {
@@ -154,8 +155,10 @@ vResult_t check_ptrs(const vcomm* c, const void* const* send, void* const* recv,
             if (!send[r] || !ptr_aligned(send[r], esz)) return vInvalidArgument;
             bits |= (uintptr_t)send[r];
         }
-        if (!recv[r] || !ptr_aligned(recv[r], esz)) return vInvalidArgument;
-        bits |= (uintptr_t)recv[r];
+        if (needAllRecv || r == root) {
+            if (!recv[r] || !ptr_aligned(recv[r], esz)) return vInvalidArgument;
+            bits |= (uintptr_t)recv[r];
+        }
     }
     *aligned = (int)(bits & (~bits + 1));       // lowest set bit, at most 32
     return vSuccess;
@@ -207,6 +210,8 @@ void fill_onepass(vc::OnePassArgs* a, const vcomm* c, const void* const* send, v
         a->send[r] = send ? send[r] : nullptr;
         a->recv[r] = recv[r];
     }
+    a->orderRoot = -1;
+    a->outRoot = -1;
     a->nRanks = c->nRanks;
     a->ctasPerChannel = p.ctasPerChannel;
     a->count = count;
@@ -325,7 +330,7 @@ struct Front {
 };
 
 Front front(vcomm* c, const void* const* send, void* const* recv, size_t count, int dt, int root,
-            bool needAllSend) {
+            bool needAllSend, bool needAllRecv = true) {
     Front f{vSuccess, 0};
     if (!comm_ok(c)) { f.res = vInvalidArgument; return f; }
     vResult_t s = sticky(c);
@@ -336,7 +341,7 @@ Front front(vcomm* c, const void* const* send, void* const* recv, size_t count, 
     const size_t n2 = (size_t)c->nRanks * (size_t)c->nRanks;
     if (count > ((size_t)1 << 62) / (n2 * esz)) { f.res = vInvalidArgument; return f; }
     if (count == 0) return f;
-    f.res = check_ptrs(c, send, recv, esz, root, needAllSend, &f.aligned);
+    f.res = check_ptrs(c, send, recv, esz, root, needAllSend, &f.aligned, needAllRecv);
     return f;
 }
 
@@ -588,6 +593,64 @@ vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vD
     fill_onepass(&a, c, send, recv, p, count);
     return finish_launch(c, vc::launch_alltoall_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                         p.threadsPerCta, stream), stream, "alltoall");
+}
+
+vResult_t vReduce(const void* const* send, void* const* recv, size_t count, vDataType_t dt, vRedOp_t op,
+                  int root, vcomm_t c, cudaStream_t stream) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    if (root < 0 || root >= c->nRanks || !valid_op(op)) return vInvalidArgument;
+    Front f = front(c, send, recv, count, dt, root, true, false);
+    if (f.res != vSuccess || count == 0) return f.res;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollReduce, count, dt, f.aligned, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollReduce, count, dt, p);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, count);
+    a.orderRoot = root;
+    a.outRoot = root;
+    return finish_launch(c, vc::launch_allreduce_onepass(a, dt, op, p.vecBytes, p.gridCtas, p.threadsPerCta,
+                                                         stream), stream, "reduce");
+}
+
+vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, vDataType_t dt, int root,
+                  vcomm_t c, cudaStream_t stream) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    if (root < 0 || root >= c->nRanks) return vInvalidArgument;
+    Front f = front(c, send, recv, sendcount, dt, root, true, false);
+    if (f.res != vSuccess || sendcount == 0) return f.res;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollGather, sendcount, dt, f.aligned, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollGather, sendcount, dt, p);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, sendcount);
+    a.outRoot = root;
+    return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
+                                                         p.threadsPerCta, stream), stream, "gather");
+}
+
+vResult_t vScatter(const void* const* send, void* const* recv, size_t recvcount, vDataType_t dt, int root,
+                   vcomm_t c, cudaStream_t stream) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    if (root < 0 || root >= c->nRanks) return vInvalidArgument;
+    Front f = front(c, send, recv, recvcount, dt, root, false, true);
+    if (f.res != vSuccess || recvcount == 0) return f.res;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vPlanInfo_t p;
+    vResult_t r = make_plan(c, vCollScatter, recvcount, dt, f.aligned, &p);
+    if (r != vSuccess) return r;
+    debug_plan(c, vCollScatter, recvcount, dt, p);
+    vc::OnePassArgs a;
+    fill_onepass(&a, c, send, recv, p, recvcount);
+    a.root = root;
+    return finish_launch(c, vc::launch_scatter_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
+                                                       p.threadsPerCta, stream), stream, "scatter");
 }
 
 vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* counts,

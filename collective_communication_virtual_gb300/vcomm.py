@@ -23,6 +23,7 @@ vProtoSimple, vProtoLL, vProtoLL128, vProtoAuto = 0, 1, 2, 3
 vAlgoAuto, vAlgoOnePass, vAlgoRing = 0, 1, 2
 vCollAllReduce, vCollReduceScatter, vCollAllGather = 0, 1, 2
 vCollBroadcast, vCollAllToAll, vCollAllToAllv = 3, 4, 5
+vCollReduce, vCollGather, vCollScatter = 6, 7, 8
 VCOMM_MAX_RANKS = 64
 
 RESULT_NAMES = {0: "vSuccess", 1: "vUnhandledCudaError", 2: "vSystemError", 3: "vInternalError",
@@ -93,6 +94,12 @@ _SIGNATURES = {
                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vAllToAllv": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vReduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                 ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vGather": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                 ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vScatter": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vAllReduceNoAlloc": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
 }
@@ -264,6 +271,21 @@ def vBroadcast(sendbuffs, recvbuffs, count: int, datatype, op, root: int, comm, 
 def vAllToAll(sendbuffs, recvbuffs, count: int, datatype, op, comm, stream=None) -> None:
     _check(lib().vAllToAll(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
                            _op_code(op), comm, _stream(stream)), "vAllToAll")
+
+
+def vReduce(sendbuffs, recvbuffs, count: int, datatype, op, root: int, comm, stream=None) -> None:
+    _check(lib().vReduce(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+                         _op_code(op), root, comm, _stream(stream)), "vReduce")
+
+
+def vGather(sendbuffs, recvbuffs, sendcount: int, datatype, root: int, comm, stream=None) -> None:
+    _check(lib().vGather(_ptr_array(sendbuffs), _ptr_array(recvbuffs), sendcount, _dtype_code(datatype),
+                         root, comm, _stream(stream)), "vGather")
+
+
+def vScatter(sendbuffs, recvbuffs, recvcount: int, datatype, root: int, comm, stream=None) -> None:
+    _check(lib().vScatter(_ptr_array(sendbuffs), _ptr_array(recvbuffs), recvcount, _dtype_code(datatype),
+                          root, comm, _stream(stream)), "vScatter")
 
 
 def vAllToAllv(sendbuffs, recvbuffs, counts, sdispls, rdispls, datatype, comm, stream=None) -> None:

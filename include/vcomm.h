@@ -94,7 +94,8 @@ typedef enum { vAlgoAuto = 0, vAlgoOnePass = 1, vAlgoRing = 2 } vAlgo_t;
 
 typedef enum {
     vCollAllReduce = 0, vCollReduceScatter = 1, vCollAllGather = 2,
-    vCollBroadcast = 3, vCollAllToAll = 4, vCollAllToAllv = 5
+    vCollBroadcast = 3, vCollAllToAll = 4, vCollAllToAllv = 5,
+    vCollReduce = 6, vCollGather = 7, vCollScatter = 8
 } vColl_t;
 
 /* ------------------------------------------------------------------------------- */
@@ -199,6 +200,25 @@ vResult_t vAllToAllv(const void* const* sendbuffs, void* const* recvbuffs, const
                      const int32_t* sdispls, const int32_t* rdispls, vDataType_t datatype,
                      vcomm_t comm, cudaStream_t stream);
 
+/* Rooted collectives ("AI Systems Performance Engineering (3)", collective table:
+ * reduce, gather and scatter rows).  root in [0, nRanks); recvbuffs / sendbuffs entries
+ * that the call does not use may be NULL.
+ *
+ * vReduce: recvbuffs[root][e] = the reduction of sendbuffs[.][e] for e < count, every
+ * element in the order of a ring chain that ends at the root: ranks root+1, ..., root
+ * (the order block `root` of vAllReduce uses).  In place: recvbuffs[root] ==
+ * sendbuffs[root].
+ * vGather: recvbuffs[root][s * sendcount + t] = sendbuffs[s][t].  In place:
+ * sendbuffs[root] == recvbuffs[root] + root * sendcount.
+ * vScatter: recvbuffs[r][t] = sendbuffs[root][r * recvcount + t].  In place:
+ * recvbuffs[root] == sendbuffs[root] + root * recvcount. */
+vResult_t vReduce(const void* const* sendbuffs, void* const* recvbuffs, size_t count,
+                  vDataType_t datatype, vRedOp_t op, int root, vcomm_t comm, cudaStream_t stream);
+vResult_t vGather(const void* const* sendbuffs, void* const* recvbuffs, size_t sendcount,
+                  vDataType_t datatype, int root, vcomm_t comm, cudaStream_t stream);
+vResult_t vScatter(const void* const* sendbuffs, void* const* recvbuffs, size_t recvcount,
+                   vDataType_t datatype, int root, vcomm_t comm, cudaStream_t stream);
+
 /* Ring all-reduce for callers that cannot allocate device memory.  The pages have no
  * counterpart to this call; it exists for code that must not call cudaMalloc (code
  * running during CUDA graph capture, allocator or memory-pool callbacks, runtimes that
@@ -230,7 +250,8 @@ typedef struct {
     int algo;                  /* vAlgo_t requested */
     int coll;                  /* vColl_t */
     int datatype;              /* vDataType_t */
-    size_t count;              /* elements: AR/BC count, RS recvcount, AG sendcount, A2A block */
+    size_t count;              /* elements: AR/BC/Reduce count, RS/Scatter recvcount,
+                                  AG/Gather sendcount, A2A block */
     size_t chunkBytes;         /* ring chunk bytes per rank (0 = default) */
     int aligned16;             /* 1 if every buffer pointer is 16-byte aligned */
     int smCount;               /* streaming multiprocessors of the device */

@@ -31,6 +31,7 @@ def test_header_declares_the_collectives():
     names = declared_functions()
     for n in ["vcommInit", "vcommDestroy", "vcommGetAsyncError", "vAllReduce", "vReduceScatter",
               "vReduceScatterScaleCast", "vAllGather", "vBroadcast", "vAllToAll", "vAllToAllv",
+              "vReduce", "vGather", "vScatter",
               "vPlanCompute"]:
         assert n in names
 
@@ -77,6 +78,9 @@ def test_null_or_garbage_comm_is_refused(lib):
         assert lib.vBroadcast(arr, arr, 16, 0, 0, 0, comm, None) == V.vInvalidArgument
         assert lib.vAllToAll(arr, arr, 16, 0, 0, comm, None) == V.vInvalidArgument
         assert lib.vAllToAllv(arr, arr, None, None, None, 0, comm, None) == V.vInvalidArgument
+        assert lib.vReduce(arr, arr, 16, 0, 0, 0, comm, None) == V.vInvalidArgument
+        assert lib.vGather(arr, arr, 16, 0, 0, comm, None) == V.vInvalidArgument
+        assert lib.vScatter(arr, arr, 16, 0, 0, comm, None) == V.vInvalidArgument
         assert lib.vcommDestroy(comm) == V.vInvalidArgument
         assert lib.vcommAbort(comm) == V.vInvalidArgument
         err = ctypes.c_int()

@@ -117,6 +117,11 @@ def test_traffic_and_bus_factor():
     assert p.minBytes == S + n * S
     p = plan(nRanks=n, count=count, coll=V.vCollAllToAll)
     assert p.minBytes == 2 * n * n * S
+    p = plan(nRanks=n, count=count, coll=V.vCollReduce)
+    assert p.minBytes == n * S + S and p.blockElems == oracle.block_elems(count, n, 4)
+    assert plan(nRanks=n, count=count, coll=V.vCollGather).minBytes == 2 * n * S
+    assert plan(nRanks=n, count=count, coll=V.vCollScatter).minBytes == 2 * n * S
+    assert plan(nRanks=n, count=count, coll=V.vCollReduce, algo=V.vAlgoRing).algo == V.vAlgoOnePass
 
 
 def test_32_byte_vectors_when_blocks_and_pointers_allow():
@@ -148,7 +153,7 @@ def test_grid_is_about_two_ctas_per_sm_and_never_idle():
 
 def test_bad_requests():
     for kw in [dict(nRanks=0), dict(nRanks=65), dict(nChannels=0), dict(nChannels=65), dict(coll=9),
-               dict(datatype=7), dict(proto=5), dict(algo=4), dict(chunkBytes=1000),
+               dict(datatype=7), dict(proto=5), dict(algo=4), dict(chunkBytes=1000), dict(coll=10),
                dict(chunkBytes=3 << 20)]:
         with pytest.raises(V.VcommError) as e:
             plan(**kw)

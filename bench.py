@@ -445,6 +445,41 @@ def other_workloads(torch, V, dev, stream, hbm):
     rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
     t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
     rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    # group batching: 64 gradient buckets of 64 KiB fp32, separate calls vs one group
+    nb, bc = 64, 16384
+    bx = [[torch.rand(bc, device=dev) for _ in range(n)] for _ in range(nb)]
+    by = [[torch.empty(bc, device=dev) for _ in range(n)] for _ in range(nb)]
+
+    def separate(s=stream):
+        for i in range(nb):
+            V.vAllReduce(bx[i], by[i], bc, torch.float32, "sum", comm, s)
+
+    t_eager = tm(separate, 10)
+    # device time of the 64 separate launches: replayed from a CUDA graph (no host gaps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        separate(torch.cuda.current_stream())
+    t_graph = tm(g.replay, 10)
+    # device time of the group: the recording happens on the host before the timed region,
+    # vcommGroupEnd then uploads the work table and launches one fused kernel
+    ts = []
+    for rep in range(13):
+        V.vcommGroupStart(comm)
+        separate()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        V.vcommGroupEnd(comm)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            ts.append(a.elapsed_time(b) / 1e3)
+    t_grp = sum(ts) / len(ts)
+    out["ddp_64_buckets_64KiB_fp32"] = {"separate_eager_us": t_eager * 1e6,
+                                        "separate_graph_replay_us": t_graph * 1e6,
+                                        "grouped_us": t_grp * 1e6, "launches_separate": nb,
+                                        "launches_grouped": 1,
+                                        "min_bytes": 2 * n * nb * bc * 4}
     V.vcommDestroy(comm)
     return out
 

@@ -86,6 +86,26 @@ struct RingArgs {
     int testStallRank;               // test hook: this rank never posts data (-1 = off)
 };
 
+// A batch of all-reduces of one type and op run by one launch (group batching).  The
+// work table lives in device memory: items[i] describes all-reduce i, whose 2*N rank
+// pointers are ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).
+constexpr int kMaxGroupItems = 1024;
+struct GroupItem {
+    unsigned long long unitStart;    // first flat work unit of this item
+    unsigned long long count;        // elements per rank
+    unsigned long long blockElems;   // B of this all-reduce
+    unsigned long long unitsPerBlock;
+    int ptrOff;
+    int pad;
+};
+struct GroupArgs {
+    const GroupItem* items;
+    const void* const* ptrs;
+    int nItems;
+    int nRanks;
+    unsigned long long totalUnits;
+};
+
 // Launchers (defined in the kernel translation units).  Each returns the launch status.
 // vb: bytes per vector of the one-pass reductions, 0 (element path), 16 or 32.
 cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, int vb,
@@ -93,6 +113,8 @@ cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedO
 cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
                                           vDataType_t outType, int vb, int grid, int threads,
                                           cudaStream_t s);
+cudaError_t launch_allreduce_group(const GroupArgs& a, vDataType_t dt, vRedOp_t op, int vb, int grid,
+                                   int threads, cudaStream_t s);
 cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s);
 cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,

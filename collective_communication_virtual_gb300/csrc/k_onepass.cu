@@ -21,18 +21,17 @@ namespace vc {
 // Load the VB-byte vector at byte offset `boff` of every rank, starting at rank `first`
 // and wrapping, and reduce in that order.  Up to 8 loads are in flight before the first use.
 template <int DT, int OP, int VB>
-__device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const OnePassArgs& a, int first,
-                                                                size_t boff) {
+__device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const void* const* send, int N,
+                                                                int first, size_t boff) {
     using VT = typename VecOf<VB>::T;
-    const int N = a.nRanks;
-    VT acc = VecOf<VB>::ld((const char*)a.send[first] + boff);
+    VT acc = VecOf<VB>::ld((const char*)send[first] + boff);
     int rk = first + 1 == N ? 0 : first + 1;
     for (int k = 1; k < N; k += 8) {
         VT v[8];
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             if (k + j < N) {
-                v[j] = VecOf<VB>::ld((const char*)a.send[rk] + boff);
+                v[j] = VecOf<VB>::ld((const char*)send[rk] + boff);
                 rk = rk + 1 == N ? 0 : rk + 1;
             }
         }
@@ -44,13 +43,12 @@ __device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const OnePassAr
 }
 
 template <int DT, int OP>
-__device__ __forceinline__ uint32_t reduce_elem_ring(const OnePassArgs& a, int first, size_t e) {
+__device__ __forceinline__ uint32_t reduce_elem_ring(const void* const* send, int N, int first, size_t e) {
     constexpr int ESZ = DTypeOf<DT>::size;
-    const int N = a.nRanks;
-    uint32_t acc = ld_elem<ESZ>(a.send[first], e);
+    uint32_t acc = ld_elem<ESZ>(send[first], e);
     int rk = first + 1 == N ? 0 : first + 1;
     for (int k = 1; k < N; k++) {
-        acc = op_elem<DT, OP>(acc, ld_elem<ESZ>(a.send[rk], e));
+        acc = op_elem<DT, OP>(acc, ld_elem<ESZ>(send[rk], e));
         rk = rk + 1 == N ? 0 : rk + 1;
     }
     return acc;
@@ -103,11 +101,11 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
         const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
         if (VB && e + U <= hi) {
             const size_t boff = e * ESZ;
-            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a, first, boff);
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a.send, N, first, boff);
             for (int r = r0; r < r1; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
         } else {
             for (size_t x = e; x < min(e + U, hi); x++) {
-                const uint32_t acc = reduce_elem_ring<DT, OP>(a, first, x);
+                const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, x);
                 for (int r = r0; r < r1; r++) st_elem<ESZ>(a.recv[r], x, acc);
             }
         }
@@ -192,12 +190,56 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
         const size_t base = (size_t)r * rc;
         const int first = r + 1 == N ? 0 : r + 1;
         if (VB && t + U <= chEnd) {
-            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a, first, (base + t) * ESZ);
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a.send, N, first, (base + t) * ESZ);
             store_epilogue_vec<DT, OUT>(a.recv[r], t, acc, hasScale, a.scale);
         } else {
             for (size_t x = t; x < min(t + U, chEnd); x++) {
-                const uint32_t acc = reduce_elem_ring<DT, OP>(a, first, base + x);
+                const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, base + x);
                 store_epilogue_elem<DT, OUT>(a.recv[r], x, acc, hasScale, a.scale);
+            }
+        }
+    }
+}
+
+// Batched all-reduces (group batching, NCCL book chapter 6: ncclPrepareTasks aggregates
+// collectives of the same function, op and type into one launch).  Every item keeps its
+// own block partition and ring order, so its bits equal a separate vAllReduce.  The work
+// units of all items form one flat index space; a thread finds its item by binary search
+// over the items' first units, held in shared memory.
+template <int DT, int OP, int VB>
+__global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
+k_allreduce_group(const __grid_constant__ GroupArgs a) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    constexpr int U = VB ? VB / ESZ : 1;
+    __shared__ unsigned long long sStart[kMaxGroupItems];
+    for (int i = threadIdx.x; i < a.nItems; i += blockDim.x) sStart[i] = a.items[i].unitStart;
+    __syncthreads();
+    const int N = a.nRanks;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t j = (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < a.totalUnits; j += stride) {
+        int lo = 0, hi = a.nItems - 1;                   // last item with unitStart <= j
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sStart[mid] <= j) lo = mid;
+            else hi = mid - 1;
+        }
+        const GroupItem it = a.items[lo];
+        const void* const* send = a.ptrs + it.ptrOff;
+        void* const* recv = (void* const*)(a.ptrs + it.ptrOff + N);
+        const size_t u = j - it.unitStart;
+        const int b = (int)(u / it.unitsPerBlock);
+        const size_t e = (size_t)b * it.blockElems + (u - (size_t)b * it.unitsPerBlock) * U;
+        const size_t bend = min((size_t)((b + 1) * it.blockElems), (size_t)it.count);
+        if (e >= bend) continue;
+        const int first = b + 1 == N ? 0 : b + 1;
+        if (VB && e + U <= bend) {
+            const size_t boff = e * ESZ;
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(send, N, first, boff);
+            for (int r = 0; r < N; r++) VecOf<VB ? VB : 16>::st((char*)recv[r] + boff, acc);
+        } else {
+            for (size_t x = e; x < min(e + U, bend); x++) {
+                const uint32_t acc = reduce_elem_ring<DT, OP>(send, N, first, x);
+                for (int r = 0; r < N; r++) st_elem<ESZ>(recv[r], x, acc);
             }
         }
     }
@@ -233,6 +275,37 @@ cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedO
     case vFloat16: return ar_dispatch_op<kF16>(a, op, vb, grid, threads, s);
     case vBFloat16: return ar_dispatch_op<kBF16>(a, op, vb, grid, threads, s);
     case vInt32: return ar_dispatch_op<kI32>(a, op, vb, grid, threads, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int DT, int OP>
+static cudaError_t group_dispatch_vec(const GroupArgs& a, int vb, int grid, int threads, cudaStream_t s) {
+    if (vb == 32) k_allreduce_group<DT, OP, 32><<<grid, threads, 0, s>>>(a);
+    else if (vb == 16) k_allreduce_group<DT, OP, 16><<<grid, threads, 0, s>>>(a);
+    else k_allreduce_group<DT, OP, 0><<<grid, threads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t group_dispatch_op(const GroupArgs& a, vRedOp_t op, int vb, int grid, int threads,
+                                     cudaStream_t s) {
+    switch (op) {
+    case vSum: return group_dispatch_vec<DT, kSum>(a, vb, grid, threads, s);
+    case vProd: return group_dispatch_vec<DT, kProd>(a, vb, grid, threads, s);
+    case vMin: return group_dispatch_vec<DT, kMin>(a, vb, grid, threads, s);
+    case vMax: return group_dispatch_vec<DT, kMax>(a, vb, grid, threads, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_allreduce_group(const GroupArgs& a, vDataType_t dt, vRedOp_t op, int vb, int grid,
+                                   int threads, cudaStream_t s) {
+    switch (dt) {
+    case vFloat32: return group_dispatch_op<kF32>(a, op, vb, grid, threads, s);
+    case vFloat16: return group_dispatch_op<kF16>(a, op, vb, grid, threads, s);
+    case vBFloat16: return group_dispatch_op<kBF16>(a, op, vb, grid, threads, s);
+    case vInt32: return group_dispatch_op<kI32>(a, op, vb, grid, threads, s);
     }
     return cudaErrorInvalidValue;
 }

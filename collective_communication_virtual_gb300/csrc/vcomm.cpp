@@ -11,9 +11,13 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <new>
+#include <vector>
 
 #include "internal.h"
+
+#include <algorithm>
 
 namespace {
 
@@ -24,6 +28,20 @@ struct Config {
     size_t chunkBytes = 0;           // 0: planner default
     int timeoutMs = 2000;
     bool debug = false;
+};
+
+// One call recorded between vcommGroupStart and vcommGroupEnd.
+struct GroupRec {
+    bool fusable = false;            // a one-pass all-reduce (fused with its peers)
+    std::vector<const void*> send;
+    std::vector<void*> recv;
+    size_t count = 0;
+    vDataType_t dt = vFloat32;
+    vRedOp_t op = vSum;
+    cudaStream_t stream = nullptr;
+    int vecBytes = 0;
+    size_t blockElems = 0;
+    std::function<vResult_t()> launch; // every other call
 };
 
 }  // namespace
@@ -54,6 +72,14 @@ struct vcomm {
     int testStallRank;
     cudaEvent_t lastEvent;
     bool eventRecorded;
+    // group batching
+    int groupDepth;
+    std::vector<GroupRec>* group;
+    char* groupTable[2];             // device work tables (items, then rank pointers)
+    char* groupStage[2];             // pinned staging of the tables
+    cudaEvent_t groupEv[2];
+    bool groupEvRecorded[2];
+    unsigned groupSlot;
     unsigned long long endMagic;
 };
 
@@ -115,6 +141,12 @@ void read_env(Config* cfg) {
 }
 
 void free_comm(vcomm* c) {
+    delete c->group;
+    for (int k = 0; k < 2; k++) {
+        if (c->groupEv[k]) cudaEventDestroy(c->groupEv[k]);
+        if (c->groupTable[k]) cudaFree(c->groupTable[k]);
+        if (c->groupStage[k]) cudaFreeHost(c->groupStage[k]);
+    }
     if (c->lastEvent) cudaEventDestroy(c->lastEvent);
     if (c->fifo) cudaFree(c->fifo);
     if (c->ctrl) cudaFree(c->ctrl);
@@ -323,6 +355,74 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
     return finish_launch(c, e, stream, "ring launch");
 }
 
+size_t group_table_bytes(int nRanks) {
+    return (size_t)vc::kMaxGroupItems * sizeof(vc::GroupItem) +
+           (size_t)vc::kMaxGroupItems * 2 * (size_t)nRanks * sizeof(void*);
+}
+
+// One launch for up to kMaxGroupItems recorded all-reduces of one type, op, stream and
+// vector width.  The work table goes through one of two pinned staging buffers, each
+// reused only after the launch that last read it has finished.
+vResult_t launch_group_batch(vcomm* c, const std::vector<const GroupRec*>& items) {
+    const int N = c->nRanks;
+    const GroupRec& r0 = *items[0];
+    const size_t tableBytes = group_table_bytes(N);
+    if (!c->groupTable[0]) {
+        for (int k = 0; k < 2; k++) {
+            cudaError_t e = cudaMalloc(&c->groupTable[k], tableBytes);
+            if (e == cudaSuccess) e = cudaHostAlloc(&c->groupStage[k], tableBytes, cudaHostAllocDefault);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->groupEv[k], cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(c, e, "group buffers");
+        }
+    }
+    const int k = (int)(c->groupSlot++ & 1u);
+    if (c->groupEvRecorded[k]) cudaEventSynchronize(c->groupEv[k]);
+    // Table: the batch's items, then their rank pointers right after them, so one copy
+    // uploads both.
+    const size_t n = items.size();
+    const size_t itemBytes = (n * sizeof(vc::GroupItem) + 15) / 16 * 16;
+    const size_t tableUsed = itemBytes + n * 2 * (size_t)N * sizeof(void*);
+    vc::GroupItem* it = reinterpret_cast<vc::GroupItem*>(c->groupStage[k]);
+    const void** ptrs = reinterpret_cast<const void**>(c->groupStage[k] + itemBytes);
+    const size_t esz = elem_size(r0.dt);
+    const size_t U = r0.vecBytes ? (size_t)r0.vecBytes / esz : 1;
+    unsigned long long units = 0;
+    for (size_t i = 0; i < n; i++) {
+        const GroupRec& g = *items[i];
+        it[i].unitStart = units;
+        it[i].count = g.count;
+        it[i].blockElems = g.blockElems;
+        it[i].unitsPerBlock = (g.blockElems + U - 1) / U;
+        it[i].ptrOff = (int)(i * 2 * N);
+        it[i].pad = 0;
+        for (int r = 0; r < N; r++) {
+            ptrs[i * 2 * N + r] = g.send[r];
+            ptrs[i * 2 * N + N + r] = g.recv[r];
+        }
+        units += it[i].unitsPerBlock * (unsigned long long)N;
+    }
+    (void)tableBytes;
+    cudaError_t e = cudaMemcpyAsync(c->groupTable[k], c->groupStage[k], tableUsed, cudaMemcpyHostToDevice,
+                                    r0.stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "group table upload");
+    vc::GroupArgs a;
+    a.items = reinterpret_cast<const vc::GroupItem*>(c->groupTable[k]);
+    a.ptrs = reinterpret_cast<const void* const*>(c->groupTable[k] + itemBytes);
+    a.nItems = (int)n;
+    a.nRanks = N;
+    a.totalUnits = units;
+    const int perSm = r0.vecBytes == 32 ? 1 : 2;
+    const unsigned long long need = (units + vc::kOnePassThreads - 1) / vc::kOnePassThreads;
+    const int grid = (int)std::min<unsigned long long>((unsigned long long)perSm * c->smCount, std::max(1ull, need));
+    e = vc::launch_allreduce_group(a, r0.dt, r0.op, r0.vecBytes, grid, vc::kOnePassThreads, r0.stream);
+    if (e != cudaSuccess) {
+        c->hostError = vUnhandledCudaError;
+        return cuda_fail(c, e, "group launch");
+    }
+    if (cudaEventRecord(c->groupEv[k], r0.stream) == cudaSuccess) c->groupEvRecorded[k] = true;
+    return finish_launch(c, cudaSuccess, r0.stream, "group");
+}
+
 // Shared front half of every collective.
 struct Front {
     vResult_t res;
@@ -346,6 +446,25 @@ Front front(vcomm* c, const void* const* send, void* const* recv, size_t count, 
 }
 
 bool valid_op(int op) { return op >= vSum && op <= vMax; }
+
+std::vector<const void*> copy_ptrs(const void* const* p, int n) {
+    return p ? std::vector<const void*>(p, p + n) : std::vector<const void*>(n, nullptr);
+}
+std::vector<void*> copy_ptrs(void* const* p, int n) {
+    return p ? std::vector<void*>(p, p + n) : std::vector<void*>(n, nullptr);
+}
+
+// Inside a group every call is recorded (its pointer arrays copied) and runs at
+// vcommGroupEnd.
+#define VC_GROUP_RECORD(c, CALL)                                                           \
+    do {                                                                                   \
+        if ((c)->groupDepth > 0) {                                                         \
+            GroupRec rec;                                                                  \
+            rec.launch = CALL;                                                             \
+            (c)->group->push_back(std::move(rec));                                         \
+            return vSuccess;                                                               \
+        }                                                                                  \
+    } while (0)
 
 }  // namespace
 
@@ -387,6 +506,11 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
     c->testStallRank = -1;
     c->hostError = vSuccess;
     c->epoch = 1;                    // eager ring launches use epochs >= 2
+    c->group = new (std::nothrow) std::vector<GroupRec>();
+    if (!c->group) {
+        free_comm(c);
+        return vSystemError;
+    }
     int v = 0;
     if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) goto fail;
     c->smCount = v;
@@ -437,6 +561,60 @@ vResult_t vcommAbort(vcomm_t c) {
     return vSuccess;
 }
 
+vResult_t vcommGroupStart(vcomm_t c) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    c->groupDepth++;
+    return vSuccess;
+}
+
+vResult_t vcommGroupEnd(vcomm_t c) {
+    if (!comm_ok(c)) return vInvalidArgument;
+    if (c->groupDepth == 0) return vInvalidUsage;
+    if (--c->groupDepth > 0) return vSuccess;
+    std::vector<GroupRec> recs;
+    recs.swap(*c->group);
+    vResult_t s = sticky(c);
+    if (s != vSuccess) return s;
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
+    vResult_t first = vSuccess;
+    // Fused all-reduces: batches of one (type, op, stream, vector width), in order of
+    // their first call; a batch of one, or one on a capturing stream, runs on its own.
+    std::vector<bool> done(recs.size(), false);
+    for (size_t i = 0; i < recs.size(); i++) {
+        if (!recs[i].fusable || done[i]) continue;
+        std::vector<const GroupRec*> batch;
+        for (size_t j = i; j < recs.size(); j++) {
+            const GroupRec& a = recs[i];
+            const GroupRec& b = recs[j];
+            if (!b.fusable || done[j] || b.dt != a.dt || b.op != a.op || b.stream != a.stream ||
+                b.vecBytes != a.vecBytes)
+                continue;
+            batch.push_back(&b);
+            done[j] = true;
+        }
+        const bool single = batch.size() == 1 || stream_capturing(recs[i].stream);
+        for (size_t k = 0; k < batch.size(); k += (single ? 1 : vc::kMaxGroupItems)) {
+            vResult_t r;
+            if (single) {
+                const GroupRec& b = *batch[k];
+                r = vAllReduce(b.send.data(), b.recv.data(), b.count, b.dt, b.op, c, b.stream);
+            } else {
+                std::vector<const GroupRec*> part(batch.begin() + k,
+                                                  batch.begin() + std::min(batch.size(), k + vc::kMaxGroupItems));
+                r = launch_group_batch(c, part);
+            }
+            if (r != vSuccess && first == vSuccess) first = r;
+        }
+    }
+    for (auto& rec : recs) {
+        if (rec.fusable) continue;
+        const vResult_t r = rec.launch();
+        if (r != vSuccess && first == vSuccess) first = r;
+    }
+    return first;
+}
+
 vResult_t vcommSetAlgo(vcomm_t c, vAlgo_t algo) {
     if (!comm_ok(c) || algo < vAlgoAuto || algo > vAlgoRing) return vInvalidArgument;
     c->cfg.algo = algo;
@@ -481,11 +659,30 @@ vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, v
     Front f = front(c, send, recv, count, dt, 0, true);
     if (f.res != vSuccess || count == 0) return f.res;
     if (!valid_op(op)) return vInvalidArgument;
-    DeviceGuard g(c->device);
-    if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollAllReduce, count, dt, f.aligned, &p);
     if (r != vSuccess) return r;
+    if (c->groupDepth > 0) {
+        GroupRec rec;
+        rec.send = copy_ptrs(send, c->nRanks);
+        rec.recv = copy_ptrs(recv, c->nRanks);
+        rec.count = count;
+        rec.dt = dt;
+        rec.op = op;
+        rec.stream = stream;
+        rec.vecBytes = p.vecBytes;
+        rec.blockElems = p.blockElems;
+        rec.fusable = p.algo == vAlgoOnePass;
+        if (!rec.fusable) {
+            auto s_ = rec.send;
+            auto r_ = rec.recv;
+            rec.launch = [=]() { return vAllReduce(s_.data(), r_.data(), count, dt, op, c, stream); };
+        }
+        c->group->push_back(std::move(rec));
+        return vSuccess;
+    }
+    DeviceGuard g(c->device);
+    if (!g.ok) return vUnhandledCudaError;
     debug_plan(c, vCollAllReduce, count, dt, p);
     if (p.algo == vAlgoRing)
         return launch_ring_plan(c, vCollAllReduce, send, recv, count, dt, op, dt, 0, false, 1.0f, p, stream);
@@ -498,6 +695,11 @@ vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, v
 static vResult_t reduce_scatter_impl(const void* const* send, void* const* recv, size_t rc,
                                      vDataType_t dt, vRedOp_t op, vDataType_t outType, bool hasScale,
                                      float scale, vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return reduce_scatter_impl(s_.data(), r_.data(), rc, dt, op, outType, hasScale, scale, c, stream); });
+    }
     Front f = front(c, send, recv, rc, dt, 0, true);
     if (f.res != vSuccess || rc == 0) return f.res;
     if (!valid_op(op)) return vInvalidArgument;
@@ -536,6 +738,11 @@ vResult_t vReduceScatterScaleCast(const void* const* send, void* const* recv, si
 
 vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcount, vDataType_t dt,
                      vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vAllGather(s_.data(), r_.data(), sendcount, dt, op, c, stream); });
+    }
     (void)op;
     Front f = front(c, send, recv, sendcount, dt, 0, true);
     if (f.res != vSuccess || sendcount == 0) return f.res;
@@ -555,6 +762,11 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
 
 vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
                      vRedOp_t op, int root, vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vBroadcast(s_.data(), r_.data(), count, dt, op, root, c, stream); });
+    }
     (void)op;
     if (!comm_ok(c)) return vInvalidArgument;
     if (root < 0 || root >= c->nRanks) return vInvalidArgument;
@@ -580,6 +792,11 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
 
 vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
                     vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vAllToAll(s_.data(), r_.data(), count, dt, op, c, stream); });
+    }
     (void)op;
     Front f = front(c, send, recv, count, dt, 0, true);
     if (f.res != vSuccess || count == 0) return f.res;
@@ -597,6 +814,11 @@ vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vD
 
 vResult_t vReduce(const void* const* send, void* const* recv, size_t count, vDataType_t dt, vRedOp_t op,
                   int root, vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vReduce(s_.data(), r_.data(), count, dt, op, root, c, stream); });
+    }
     if (!comm_ok(c)) return vInvalidArgument;
     if (root < 0 || root >= c->nRanks || !valid_op(op)) return vInvalidArgument;
     Front f = front(c, send, recv, count, dt, root, true, false);
@@ -617,6 +839,11 @@ vResult_t vReduce(const void* const* send, void* const* recv, size_t count, vDat
 
 vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, vDataType_t dt, int root,
                   vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vGather(s_.data(), r_.data(), sendcount, dt, root, c, stream); });
+    }
     if (!comm_ok(c)) return vInvalidArgument;
     if (root < 0 || root >= c->nRanks) return vInvalidArgument;
     Front f = front(c, send, recv, sendcount, dt, root, true, false);
@@ -636,6 +863,11 @@ vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, 
 
 vResult_t vScatter(const void* const* send, void* const* recv, size_t recvcount, vDataType_t dt, int root,
                    vcomm_t c, cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vScatter(s_.data(), r_.data(), recvcount, dt, root, c, stream); });
+    }
     if (!comm_ok(c)) return vInvalidArgument;
     if (root < 0 || root >= c->nRanks) return vInvalidArgument;
     Front f = front(c, send, recv, recvcount, dt, root, false, true);
@@ -656,6 +888,11 @@ vResult_t vScatter(const void* const* send, void* const* recv, size_t recvcount,
 vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* counts,
                      const int32_t* sdispls, const int32_t* rdispls, vDataType_t dt, vcomm_t c,
                      cudaStream_t stream) {
+    if (comm_ok(c) && c->groupDepth > 0) {
+        auto s_ = copy_ptrs(send, c->nRanks);
+        auto r_ = copy_ptrs(recv, c->nRanks);
+        VC_GROUP_RECORD(c, [=]() { return vAllToAllv(s_.data(), r_.data(), counts, sdispls, rdispls, dt, c, stream); });
+    }
     if (!comm_ok(c)) return vInvalidArgument;
     vResult_t s = sticky(c);
     if (s != vSuccess) return s;

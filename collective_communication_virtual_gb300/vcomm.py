@@ -71,6 +71,8 @@ _SIGNATURES = {
     "vcommAbort": ([ctypes.c_void_p], ctypes.c_int),
     "vcommGetErrorString": ([ctypes.c_int], ctypes.c_char_p),
     "vcommSetAlgo": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
+    "vcommGroupStart": ([ctypes.c_void_p], ctypes.c_int),
+    "vcommGroupEnd": ([ctypes.c_void_p], ctypes.c_int),
     "vcommSetProtocol": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "vcommSetChunkBytes": ([ctypes.c_void_p, ctypes.c_size_t], ctypes.c_int),
     "vcommSetTimeoutMs": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
@@ -193,6 +195,14 @@ def vcommAbort(comm) -> None:
 
 def vcommGetErrorString(code: int) -> str:
     return lib().vcommGetErrorString(code).decode()
+
+
+def vcommGroupStart(comm) -> None:
+    _check(lib().vcommGroupStart(comm), "vcommGroupStart")
+
+
+def vcommGroupEnd(comm) -> None:
+    _check(lib().vcommGroupEnd(comm), "vcommGroupEnd")
 
 
 def vcommSetAlgo(comm, algo) -> None:

@@ -129,6 +129,21 @@ vResult_t vcommAbort(vcomm_t comm);
 
 const char* vcommGetErrorString(vResult_t result);
 
+/* Group batching (NCCL book chapter 6 ncclPrepareTasks and chapter 7 ncclGroupStart /
+ * ncclGroupEnd).  Between vcommGroupStart and vcommGroupEnd every collective call on
+ * this communicator is checked and recorded (its pointer arrays copied) and returns
+ * vSuccess; nothing is enqueued.  vcommGroupEnd enqueues them: one-pass all-reduces of
+ * the same type, op, stream and vector width are fused into one kernel launch (up to
+ * 1024 per launch, each keeping its own block order, so the bits equal separate calls);
+ * every other call is enqueued as its own launch, in call order.  Calls in one group
+ * must not depend on each other's results.  Groups nest; only the outermost end
+ * enqueues.  vcommGroupEnd returns the first error of the recorded calls, or
+ * vInvalidUsage without a matching start.  On a stream being captured into a CUDA
+ * graph the all-reduces are enqueued one by one.  The communicator keeps two small
+ * device work tables and their pinned staging copies for the fused launches. */
+vResult_t vcommGroupStart(vcomm_t comm);
+vResult_t vcommGroupEnd(vcomm_t comm);
+
 /* Tuning knobs (host only, take effect for later calls).  chunkBytes is the ring
  * path's bytes per rank per chunk (one chunk = 4 FIFO slots, one slice = 2 slots;
  * NCCL book chapter 6, ALLREDUCE_CHUNKSTEPS / ALLREDUCE_SLICESTEPS); it must be a

@@ -81,6 +81,8 @@ def test_null_or_garbage_comm_is_refused(lib):
         assert lib.vReduce(arr, arr, 16, 0, 0, 0, comm, None) == V.vInvalidArgument
         assert lib.vGather(arr, arr, 16, 0, 0, comm, None) == V.vInvalidArgument
         assert lib.vScatter(arr, arr, 16, 0, 0, comm, None) == V.vInvalidArgument
+        assert lib.vcommGroupStart(comm) == V.vInvalidArgument
+        assert lib.vcommGroupEnd(comm) == V.vInvalidArgument
         assert lib.vcommDestroy(comm) == V.vInvalidArgument
         assert lib.vcommAbort(comm) == V.vInvalidArgument
         err = ctypes.c_int()

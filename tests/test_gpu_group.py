@@ -1,0 +1,111 @@
+"""Group batching: calls between vcommGroupStart and vcommGroupEnd run at the end, with
+one-pass all-reduces of one type/op/stream fused into one launch.  Results must equal
+the oracle (and so separate calls) bit for bit."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import oracle
+from collective_communication_virtual_gb300 import inputs
+from collective_communication_virtual_gb300 import vcomm as V
+from tests.gpu_util import DEV, assert_bits_equal, empty_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture()
+def comm():
+    c = V.vcommInit(8, 2, V.vProtoSimple)
+    yield c
+    V.vcommDestroy(c)
+
+
+def test_group_of_mixed_all_reduces_matches_oracle(comm):
+    n = 8
+    cases = []
+    V.vcommGroupStart(comm)
+    for i, (count, dtype, op) in enumerate([(1, torch.float32, "sum"), (4099, torch.float32, "sum"),
+                                            (100_003, torch.float32, "sum"), (65_536, torch.bfloat16, "max"),
+                                            (7, torch.bfloat16, "max"), (33_333, torch.int32, "prod"),
+                                            (12_345, torch.float32, "sum"), (1 << 20, torch.float16, "sum")]):
+        xs = inputs.uniform_ranks(n, count, dtype, seed=i)
+        send = to_dev(xs)
+        recv = empty_dev(n, count, dtype)
+        V.vAllReduce(send, recv, count, dtype, op, comm)
+        cases.append((xs, op, send, recv))
+    V.vcommGroupEnd(comm)
+    torch.cuda.synchronize()
+    assert V.vcommGetAsyncError(comm) == V.vSuccess
+    for xs, op, _, recv in cases:
+        assert_bits_equal(recv, oracle.allreduce(xs, op), f"group allreduce {xs[0].dtype} {op}")
+
+
+def test_group_runs_nothing_before_end(comm):
+    n, count = 8, 4096
+    xs = inputs.uniform_ranks(n, count, torch.float32, 3)
+    send = to_dev(xs)
+    recv = empty_dev(n, count, torch.float32, fill=-1.0)
+    V.vcommGroupStart(comm)
+    V.vAllReduce(send, recv, count, torch.float32, "sum", comm)
+    torch.cuda.synchronize()
+    assert bool((recv[0] == -1.0).all())
+    V.vcommGroupEnd(comm)
+    torch.cuda.synchronize()
+    assert_bits_equal(recv, oracle.allreduce(xs, "sum"), "after end")
+
+
+def test_group_beyond_one_launch_and_with_other_collectives(comm):
+    n = 8
+    many = []
+    V.vcommGroupStart(comm)
+    V.vcommGroupStart(comm)                      # nested: only the outer end enqueues
+    for i in range(1100):                        # more than one fused launch holds
+        count = 1 + (i * 37) % 300
+        xs = inputs.uniform_ranks(n, count, torch.float32, seed=1000 + i)
+        send = to_dev(xs)
+        recv = empty_dev(n, count, torch.float32)
+        V.vAllReduce(send, recv, count, torch.float32, "sum", comm)
+        many.append((xs, send, recv))      # the buffers must live until the group has run
+    ag_in = inputs.uniform_ranks(n, 5000, torch.bfloat16, 9)
+    ag_send = to_dev(ag_in)
+    ag_recv = empty_dev(n, n * 5000, torch.bfloat16)
+    V.vAllGather(ag_send, ag_recv, 5000, torch.bfloat16, "sum", comm)
+    rs_in = inputs.uniform_ranks(n, n * 3000, torch.float32, 10)
+    rs_send = to_dev(rs_in)
+    rs_recv = empty_dev(n, 3000, torch.float32)
+    V.vReduceScatter(rs_send, rs_recv, 3000, torch.float32, "min", comm)
+    V.vcommGroupEnd(comm)                        # inner end: still recorded
+    V.vcommGroupEnd(comm)
+    torch.cuda.synchronize()
+    assert V.vcommGetAsyncError(comm) == V.vSuccess
+    for xs, _, recv in many:
+        assert_bits_equal(recv, oracle.allreduce(xs, "sum"), "many")
+    assert_bits_equal(ag_recv, oracle.allgather(ag_in), "group allgather")
+    assert_bits_equal(rs_recv, oracle.reduce_scatter(rs_in, "min"), "group reduce-scatter")
+
+
+def test_group_end_without_start_and_errors(comm):
+    with pytest.raises(V.VcommError) as e:
+        V.vcommGroupEnd(comm)
+    assert e.value.code == V.vInvalidUsage
+    x = [torch.zeros(16, device=DEV) for _ in range(8)]
+    V.vcommGroupStart(comm)
+    with pytest.raises(V.VcommError) as e:          # argument errors are reported at the call
+        V.vAllReduce(x[:7] + [None], x, 16, torch.float32, "sum", comm)
+    assert e.value.code == V.vInvalidArgument
+    V.vcommGroupEnd(comm)
+
+
+def test_ring_all_reduce_in_a_group_runs_unfused(comm):
+    n, count = 8, 50_000
+    V.vcommSetAlgo(comm, "ring")
+    xs = inputs.uniform_ranks(n, count, torch.float16, 5)
+    send = to_dev(xs)
+    recv = empty_dev(n, count, torch.float16)
+    V.vcommGroupStart(comm)
+    V.vAllReduce(send, recv, count, torch.float16, "sum", comm)
+    V.vcommGroupEnd(comm)
+    torch.cuda.synchronize()
+    V.vcommSetAlgo(comm, "auto")
+    assert_bits_equal(recv, oracle.allreduce(xs, "sum"), "ring in group")

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libvcomm.so")
 
 SOURCES = ["vcomm.cpp", "planner.cpp", "ring_launch.cu", "k_onepass.cu", "k_copy.cu",
-           "k_ring_simple.cu", "k_ring_ll.cu", "k_ring_ll128.cu", "noalloc.cu"]
+           "k_ring_simple.cu", "k_ring_ll.cu", "k_ring_ll128.cu", "noalloc.cu", "k_tma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

@@ -78,10 +78,26 @@ __device__ __forceinline__ uint16_t op_16(uint16_t a, uint16_t b) {
 }
 
 // One 32-bit word: one fp32/int32 element or two 16-bit elements.
+//
+// fp16/bf16 sum uses the packed add, which rounds the exact sum once.  That equals the
+// widen / fp32 add / round definition: two 16-bit floats whose exponents differ by at
+// most 13 (fp16) or 15 (bf16) have an exact sum that fits fp32's 24-bit significand, so
+// the fp32 add does not round; with a larger gap the smaller operand is below half an
+// ulp of the larger in the 16-bit type, and both routes return the larger operand.
+// (Products are not done this way: a bf16 product in the subnormal range can round twice.)
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t op_word(uint32_t a, uint32_t b) {
     if (DT == kF32) return __float_as_uint(op_f32<OP>(__uint_as_float(a), __uint_as_float(b)));
     if (DT == kI32) return op_i32<OP>(a, b);
+    if (OP == kSum && DT == kBF16) {
+        const __nv_bfloat162 r = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    if (OP == kSum && DT == kF16) {
+        const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
     const uint32_t lo = op_16<DT, OP>((uint16_t)(a & 0xFFFFu), (uint16_t)(b & 0xFFFFu));
     const uint32_t hi = op_16<DT, OP>((uint16_t)(a >> 16), (uint16_t)(b >> 16));
     return lo | (hi << 16);

@@ -79,7 +79,7 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
 // All-gather: block s = send[s] lands at recv[r] + s*sc for every r.  a.count = sc.
 // Gather (a.outRoot = root) writes recv[root] only.
 template <int ESZ, int VB>
-__global__ void __launch_bounds__(kOnePassThreads)
+__global__ void __launch_bounds__(kOnePassThreads, 2)
 k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
@@ -87,21 +87,19 @@ k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
     const size_t sc = a.count;
     const TileSpan sp = tile_span<ESZ>(a, ch, sc);
     const size_t nTiles = sp.tilesPerBlock * (size_t)N;
+    char* const* dsts = a.outRoot >= 0 ? (char* const*)&a.recv[a.outRoot] : (char* const*)a.recv;
+    const int nd = a.outRoot >= 0 ? 1 : N;
     for (size_t t = cta; t < nTiles; t += a.ctasPerChannel) {
         const int s = (int)(t / sp.tilesPerBlock);
         const size_t k = t - (size_t)s * sp.tilesPerBlock;
         const size_t tlo = sp.lo + k * sp.tileElems, thi = min(tlo + sp.tileElems, sp.hi);
-        if (a.outRoot >= 0)
-            tile_copy<ESZ, VB>((const char*)a.send[s], (char* const*)&a.recv[a.outRoot], (size_t)s * sc, 1,
-                               tlo, thi);
-        else
-            tile_copy<ESZ, VB>((const char*)a.send[s], (char* const*)a.recv, (size_t)s * sc, N, tlo, thi);
+        tile_copy<ESZ, VB>((const char*)a.send[s], dsts, (size_t)s * sc, nd, tlo, thi);
     }
 }
 
 // Broadcast: recv[r][t] = send[root][t] for all r.
 template <int ESZ, int VB>
-__global__ void __launch_bounds__(kOnePassThreads)
+__global__ void __launch_bounds__(kOnePassThreads, 2)
 k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
@@ -114,7 +112,7 @@ k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
 
 // Uniform all-to-all: recv[j][i*c + t] = send[i][j*c + t].  a.count = c.
 template <int ESZ, int VB>
-__global__ void __launch_bounds__(kOnePassThreads)
+__global__ void __launch_bounds__(kOnePassThreads, 2)
 k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
@@ -134,7 +132,7 @@ k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
 
 // Scatter: block j of send[root] lands in recv[j].  a.count = recvcount.
 template <int ESZ, int VB>
-__global__ void __launch_bounds__(kOnePassThreads)
+__global__ void __launch_bounds__(kOnePassThreads, 2)
 k_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;

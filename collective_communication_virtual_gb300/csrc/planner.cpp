@@ -136,6 +136,19 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         }
         maxPer = std::max<size_t>(1, maxPer);
         per = (int)std::min<size_t>((size_t)per, maxPer);
+        // Fan-out copies (all-gather, gather, broadcast) through TMA bulk copies: 16 KiB
+        // tiles through shared memory, single-warp CTAs, up to 3 per SM.
+        const bool fanout = q->coll == vCollAllGather || q->coll == vCollGather || q->coll == vCollBroadcast;
+        if (fanout && vec && q->noBulkCopy == 0 && (B * esz) % 16 == 0 && q->nChannels >= 1) {
+            const size_t blocks = q->coll == vCollBroadcast ? 1 : (size_t)N;
+            const size_t tiles = div_up(B * esz, (size_t)16 * 1024) * blocks;
+            p->bulkCopy = 1;
+            p->nChannels = 1;
+            p->ctasPerChannel = (int)std::min<size_t>((size_t)vc::kTmaCtasPerSm * smCount, tiles);
+            p->gridCtas = p->ctasPerChannel;
+            p->threadsPerCta = 32;
+            return vSuccess;
+        }
         if (q->coll == vCollAllToAllv) { p->nChannels = 1; per = smCount; }   // 1 CTA per SM
         p->ctasPerChannel = per;
         p->gridCtas = per * p->nChannels;

@@ -28,6 +28,7 @@ struct Config {
     size_t chunkBytes = 0;           // 0: planner default
     int timeoutMs = 2000;
     bool debug = false;
+    bool bulkCopy = true;            // TMA bulk copies for the fan-out copies
 };
 
 // One call recorded between vcommGroupStart and vcommGroupEnd.
@@ -138,6 +139,7 @@ void read_env(Config* cfg) {
         if (v >= 1 && v <= 3600 * 1000) cfg->timeoutMs = (int)v;
     }
     if (const char* s = std::getenv("VCOMM_DEBUG")) cfg->debug = !std::strcmp(s, "INFO");
+    if (const char* s = std::getenv("VCOMM_COPY_TMA")) cfg->bulkCopy = std::strcmp(s, "0") != 0;
 }
 
 void free_comm(vcomm* c) {
@@ -209,6 +211,7 @@ vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned,
     q.chunkBytes = c->cfg.chunkBytes;
     q.aligned16 = aligned >= 16 ? 1 : 0;
     q.aligned32 = aligned >= 32 ? 1 : 0;
+    q.noBulkCopy = c->cfg.bulkCopy ? 0 : 1;
     q.smCount = c->smCount;
     q.l2Bytes = c->l2Bytes;
     return vPlanCompute(&q, p);
@@ -756,6 +759,9 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
         return launch_ring_plan(c, vCollAllGather, send, recv, sendcount, dt, vSum, dt, 0, false, 1.0f, p, stream);
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, sendcount);
+    if (p.bulkCopy)
+        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, c->statusDev,
+                                                      c->statusHostDev, stream), stream, "allgather");
     return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "allgather");
 }
@@ -786,6 +792,9 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, count);
     a.root = root;
+    if (p.bulkCopy)
+        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), true, p.gridCtas, c->statusDev,
+                                                      c->statusHostDev, stream), stream, "broadcast");
     return finish_launch(c, vc::launch_broadcast_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "broadcast");
 }
@@ -857,6 +866,9 @@ vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, 
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, sendcount);
     a.outRoot = root;
+    if (p.bulkCopy)
+        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, c->statusDev,
+                                                      c->statusHostDev, stream), stream, "gather");
     return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "gather");
 }

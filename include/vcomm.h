@@ -112,7 +112,9 @@ typedef enum {
  * vUnhandledCudaError.  The communicator owns a small status block in pinned host
  * memory and, once a ring transfer is planned, its staging FIFOs in device memory.
  * Environment (read once here): VCOMM_ALGO=auto|onepass|ring, VCOMM_CHUNK_BYTES,
- * VCOMM_TIMEOUT_MS, VCOMM_DEBUG=INFO (prints every plan to stderr). */
+ * VCOMM_TIMEOUT_MS, VCOMM_COPY_TMA=0|1 (1, the default: all-gather, gather and broadcast
+ * stage tiles in shared memory with TMA bulk copies when blocks are 16-byte aligned; 0:
+ * every thread loads and stores), VCOMM_DEBUG=INFO (prints every plan to stderr). */
 vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol);
 
 /* Wait for the communicator's last enqueued work, then free everything it owns.
@@ -272,6 +274,7 @@ typedef struct {
     int smCount;               /* streaming multiprocessors of the device */
     size_t l2Bytes;            /* L2 cache size of the device */
     int aligned32;             /* 1 if every buffer pointer is 32-byte aligned */
+    int noBulkCopy;            /* 1: never use TMA bulk copies (VCOMM_COPY_TMA=0) */
 } vPlanRequest_t;
 
 typedef struct {
@@ -292,6 +295,7 @@ typedef struct {
     double minBytes;           /* algorithmic minimum HBM bytes read + written */
     double busFactor;          /* busBW = algBW * busFactor (nSteps / nRanks) */
     int vecBytes;              /* bytes per vector access of the one-pass kernels: 0, 16, 32 */
+    int bulkCopy;              /* 1: all-gather / gather / broadcast through TMA bulk copies */
 } vPlanInfo_t;
 
 /* Compute the plan a collective with these parameters would run.  Pure host

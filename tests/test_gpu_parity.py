@@ -492,3 +492,41 @@ def test_bad_alltoallv_table_sets_async_error():
         assert V.vcommGetAsyncError(c) == V.vInvalidArgument
     finally:
         V.vcommDestroy(c)
+
+
+# ---------------------------------------------------------------------------------------
+# Fan-out copies through both engines: TMA bulk copies (default) and per-thread loads/stores
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("tma", [True, False], ids=["tma", "lsu"])
+def test_fanout_copies_both_engines(tma, monkeypatch):
+    monkeypatch.setenv("VCOMM_COPY_TMA", "1" if tma else "0")
+    n = 8
+    c = V.vcommInit(n, 1, V.vProtoSimple)
+    try:
+        for dtype, sc in [(torch.float32, 1 << 20), (torch.bfloat16, 1_638_400), (torch.float16, 8),
+                          (torch.int32, 12_348)]:
+            plan = V.vcommQueryPlan(c, V.vCollAllGather, sc, dtype, 32)
+            assert plan["bulkCopy"] == (1 if tma else 0)
+            xs = inputs.uniform_ranks(n, sc, dtype, seed=sc)
+            send = to_dev(xs)
+            recv = empty_dev(n, n * sc, dtype)
+            V.vAllGather(send, recv, sc, dtype, "sum", c)
+            _sync_ok(c)
+            assert_bits_equal(recv, oracle.allgather(xs), f"allgather {dtype} {sc} tma={tma}")
+            root = 5
+            g = [None] * n
+            g[root] = torch.empty(n * sc, dtype=dtype, device=DEV)
+            V.vGather(send, g, sc, dtype, root, c)
+            _sync_ok(c)
+            assert_bits_equal([g[root]], [oracle.gather(xs, root)], "gather")
+            bcast = empty_dev(n, n * sc, dtype)
+            big = inputs.uniform_ranks(1, n * sc, dtype, seed=sc + 1)[0]
+            src = [None] * n
+            src[root] = big.to(DEV)
+            V.vBroadcast(src, bcast, n * sc, dtype, "sum", root, c)
+            _sync_ok(c)
+            assert all(torch.equal(b.cpu().view(torch.int16 if b.element_size() == 2 else torch.int32),
+                                   big.view(torch.int16 if big.element_size() == 2 else torch.int32)) for b in bcast)
+    finally:
+        V.vcommDestroy(c)

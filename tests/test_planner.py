@@ -59,7 +59,7 @@ def test_reduce_scatter_and_copies_partition():
     for coll, nblocks in [(V.vCollReduceScatter, None), (V.vCollAllGather, None),
                           (V.vCollBroadcast, 1)]:
         for n, count, nch in [(8, 4096, 8), (5, 3001, 3), (2, 1, 4)]:
-            p = plan(coll=coll, nRanks=n, nChannels=nch, count=count)
+            p = plan(coll=coll, nRanks=n, nChannels=nch, count=count, noBulkCopy=1)
             nb = nblocks or n
             assert covered(p, count * nb, nb, nch)
 
@@ -134,7 +134,19 @@ def test_32_byte_vectors_when_blocks_and_pointers_allow():
     assert plan(count=4099, aligned16=0, aligned32=0).vecBytes == 0
     assert plan(coll=V.vCollReduceScatter, count=4096, aligned32=1).vecBytes == 32
     assert plan(coll=V.vCollAllGather, count=4096, aligned32=1).vecBytes == 32
-    assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1).gridCtas == 2 * 152
+    assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1).gridCtas == 2 * 152
+
+
+def test_fanout_copies_use_tma_bulk_copies_when_blocks_allow():
+    p = plan(coll=V.vCollAllGather, count=1 << 21)                   # 8 MiB blocks
+    assert p.bulkCopy == 1 and p.threadsPerCta == 32 and p.gridCtas == 3 * 152
+    p = plan(coll=V.vCollBroadcast, count=4096)                      # 16 KiB: one tile
+    assert p.bulkCopy == 1 and p.gridCtas == 1
+    assert plan(coll=V.vCollGather, count=1 << 20).bulkCopy == 1
+    assert plan(coll=V.vCollBroadcast, count=4097).bulkCopy == 0     # not a multiple of 16 bytes
+    assert plan(coll=V.vCollAllGather, count=1 << 20, aligned16=0).bulkCopy == 0
+    assert plan(coll=V.vCollAllGather, count=1 << 20, noBulkCopy=1).bulkCopy == 0
+    assert plan(coll=V.vCollAllToAll, count=1 << 20).bulkCopy == 0
     assert plan(coll=V.vCollAllGather, count=4100, aligned32=1).vecBytes == 16
     for n, count, nch in [(8, 16 << 20, 32), (3, 100_003, 5)]:
         p = plan(nRanks=n, nChannels=nch, count=count)

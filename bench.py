@@ -519,8 +519,10 @@ def channel_sweep(torch, V, send, recv, stream):
                 V.vcommSetChunkBytes(comm, chunk)
             try:
                 t = time_allreduce(V, torch, comm, send, recv, COUNT, 3, 1, stream)
+                pred = V.vcommQueryPlan(comm, V.vCollAllReduce, COUNT, torch.float32, 32)["predictedUs"]
                 out.append({"algo": algo, "proto": pname, "channels": ch, "chunk_bytes": chunk,
-                            "busbw_gbs": BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9})
+                            "busbw_gbs": BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9,
+                            "measured_us": t * 1e6, "model_us": pred})
             except V.VcommError as e:
                 out.append({"algo": algo, "proto": pname, "channels": ch, "chunk_bytes": chunk,
                             "error": str(e)})

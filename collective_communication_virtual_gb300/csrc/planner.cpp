@@ -15,6 +15,7 @@
 //  * bus bandwidth factor nSteps / nRanks with nSteps = 2(N-1) for all-reduce and N-1
 //    otherwise (NCCL book chapter 5, ring.cc, algBw = busBw * nRanks / nSteps).
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "internal.h"
@@ -37,6 +38,47 @@ size_t pow2_floor(size_t x) {
     while (p * 2 <= x) p *= 2;
     return p;
 }
+
+// ---- cost model ---------------------------------------------------------------------------
+//
+// The ring model of the NCCL book chapter 5 (ring.cc): time = latency + bus bytes / bus
+// bandwidth, where a collective of S bytes per rank moves S * nSteps / N bus bytes
+// (nSteps = 2(N-1) for all-reduce, N-1 otherwise), and LL / LL128 trade bandwidth for
+// latency.  The constants are refit on a GB300 from CUDA-graph replay times of an fp32
+// all-reduce over 8 virtual ranks, 1 KiB .. 256 MiB per rank: latency = time at 1 KiB;
+// bus rate from the 256 MiB point, at 1, 8 and 32 channels (interpolated in log2 of the
+// channel count, held flat beyond).  Ring latency grows with the number of steps, so it
+// is scaled by nSteps / 14 (14 steps for an 8-rank all-reduce).  The one-pass kernels are
+// modelled as latency + minimum HBM bytes / effective HBM rate.
+struct RingFit {
+    double latUs[3];           // at 1, 8, 32 channels
+    double busBytesPerUs[3];
+};
+const RingFit kRingFit[3] = {
+    {{43.3, 48.0, 49.4}, {14852.0, 96543.0, 186388.0}},      // Simple
+    {{33.1, 37.5, 38.3}, {6821.0, 46568.0, 107373.0}},       // LL
+    {{50.8, 51.4, 56.0}, {6184.0, 42541.0, 103539.0}},       // LL128
+};
+const double kOnePassLatUs = 2.1;
+const double kOnePassBytesPerUs = 6.37e6;                    // minimum bytes / (time - latency)
+
+double interp_ch(const double v[3], int ch) {
+    const double x = ch <= 1 ? 0.0 : (ch >= 32 ? 5.0 : std::log2((double)ch));
+    if (x <= 3.0) return v[0] + (v[1] - v[0]) * (x / 3.0);
+    return v[1] + (v[2] - v[1]) * ((x - 3.0) / 2.0);
+}
+
+int n_steps(int coll, int N) { return coll == vCollAllReduce ? 2 * (N - 1) : N - 1; }
+
+double predict_ring_us(int proto, int coll, int N, int nCh, double bytesPerRank) {
+    const RingFit& f = kRingFit[proto];
+    const double steps = (double)n_steps(coll, N);
+    const double lat = interp_ch(f.latUs, nCh) * steps / 14.0;
+    const double busBytes = bytesPerRank * steps / N;
+    return lat + busBytes / interp_ch(f.busBytesPerUs, nCh);
+}
+
+double predict_onepass_us(double minBytes) { return kOnePassLatUs + minBytes / kOnePassBytesPerUs; }
 
 }  // namespace
 
@@ -88,13 +130,6 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     const bool v32 = vec && q->aligned32 != 0 && (B * esz) % 32 == 0;
     p->vecBytes = v32 ? 32 : vec ? 16 : 0;
 
-    // ---- algorithm --------------------------------------------------------------------
-    bool ring = q->algo == vAlgoRing && N > 1 &&
-                (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ||
-                 q->coll == vCollAllGather || q->coll == vCollBroadcast);
-    p->algo = ring ? vAlgoRing : vAlgoOnePass;
-    p->launches = 1;
-
     // ---- traffic model ----------------------------------------------------------------
     const double S = (double)count * (double)esz;
     switch (q->coll) {
@@ -107,6 +142,25 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     case vCollGather: case vCollScatter: p->minBytes = 2.0 * N * S; p->busFactor = (double)(N - 1) / N; break;
     default: p->minBytes = 0; p->busFactor = (double)(N - 1) / N; break;
     }
+
+    // ---- algorithm and protocol: fixed by the caller, or the cheaper predicted time ----
+    const bool ringable = N > 1 && (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ||
+                                    q->coll == vCollAllGather || q->coll == vCollBroadcast);
+    const double bytesPerRank = q->coll == vCollAllGather ? S * N : q->coll == vCollReduceScatter ? S * N : S;
+    int ringProto = q->proto;
+    if (ringProto == vProtoAuto) {
+        double best = 0;
+        for (int pr = vProtoSimple; pr <= vProtoLL128; pr++) {
+            const double t = predict_ring_us(pr, q->coll, N, q->nChannels, bytesPerRank);
+            if (pr == vProtoSimple || t < best) { best = t; ringProto = pr; }
+        }
+    }
+    const double tOne = predict_onepass_us(p->minBytes);
+    const double tRing = ringable ? predict_ring_us(ringProto, q->coll, N, q->nChannels, bytesPerRank) : 0.0;
+    bool ring = ringable && (q->algo == vAlgoRing || (q->algo == vAlgoAuto && tRing < tOne));
+    p->algo = ring ? vAlgoRing : vAlgoOnePass;
+    p->predictedUs = ring ? tRing : (q->coll == vCollAllToAllv ? 0.0 : tOne);
+    p->launches = 1;
 
     if (!ring) {
         // One pass: about two resident CTAs of 512 threads per SM, dealt evenly to the
@@ -157,10 +211,7 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     }
 
     // ---- ring geometry ------------------------------------------------------------------
-    int proto = q->proto;
-    const double perChannelBytes = (double)p->channelElems * esz;
-    if (proto == vProtoAuto)
-        proto = perChannelBytes < 64.0 * 1024 ? vProtoLL : perChannelBytes < 1024.0 * 1024 ? vProtoLL128 : vProtoSimple;
+    const int proto = ringProto;
     p->proto = proto;
     size_t chunk = q->chunkBytes;
     if (chunk == 0) {

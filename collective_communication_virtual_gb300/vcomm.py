@@ -56,7 +56,8 @@ class vPlanInfo_t(ctypes.Structure):
                 ("channelElems", ctypes.c_size_t), ("chunkElems", ctypes.c_size_t),
                 ("slotPayloadElems", ctypes.c_size_t), ("slotBytes", ctypes.c_size_t),
                 ("fifoBytes", ctypes.c_size_t), ("minBytes", ctypes.c_double),
-                ("busFactor", ctypes.c_double), ("vecBytes", ctypes.c_int), ("bulkCopy", ctypes.c_int)]
+                ("busFactor", ctypes.c_double), ("vecBytes", ctypes.c_int), ("bulkCopy", ctypes.c_int),
+                ("predictedUs", ctypes.c_double)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -81,7 +81,9 @@ typedef enum { vSum = 0, vProd = 1, vMin = 2, vMax = 3 } vRedOp_t;
  * Simple moves raw data through FIFO slots guarded by head/tail counters; LL packs
  * 4 bytes of data with a 4-byte flag in every 8-byte word (half the bandwidth); LL128
  * carries 120 bytes of data and an 8-byte flag in every 128-byte line.
- * vProtoAuto lets the planner choose. */
+ * vProtoAuto lets the planner choose the protocol its cost model predicts fastest for the
+ * size and channel count (a ring cost model in the form of the NCCL book's ring.cc, with
+ * latencies and bus bandwidths measured on GB300). */
 typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 } vProto_t;
 
 /* Algorithms.  vAlgoOnePass: one kernel reads every rank's buffer once and writes
@@ -89,7 +91,8 @@ typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 }
  * NCCL book chapter 5 section 5).  vAlgoRing: the literal ring of the NCCL book
  * section 2.3, N-1 reduce-scatter steps then N-1 all-gather steps, each hop staged
  * through a device FIFO with the communicator's protocol.  Both give identical bits.
- * vAlgoAuto lets the planner choose. */
+ * vAlgoAuto picks the smaller predicted time (on GB300 the one-pass kernels are faster
+ * at every size: about 2 us of latency against 33-56 us for the ring's steps). */
 typedef enum { vAlgoAuto = 0, vAlgoOnePass = 1, vAlgoRing = 2 } vAlgo_t;
 
 typedef enum {
@@ -296,6 +299,7 @@ typedef struct {
     double busFactor;          /* busBW = algBW * busFactor (nSteps / nRanks) */
     int vecBytes;              /* bytes per vector access of the one-pass kernels: 0, 16, 32 */
     int bulkCopy;              /* 1: all-gather / gather / broadcast through TMA bulk copies */
+    double predictedUs;        /* the planner's cost model for this plan (GB300 fit) */
 } vPlanInfo_t;
 
 /* Compute the plan a collective with these parameters would run.  Pure host

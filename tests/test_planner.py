@@ -91,11 +91,45 @@ def test_default_chunk_keeps_fifos_within_half_of_l2():
         assert p.fifoBytes * n * nch <= l2 // 2 or p.slotBytes * 4 == 16384
 
 
-def test_auto_protocol_by_size():
-    small = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=1024)
-    mid = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=8 * 64 * 1024)
-    big = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=8 << 20)
-    assert (small.proto, mid.proto, big.proto) == (V.vProtoLL, V.vProtoLL128, V.vProtoSimple)
+def test_auto_protocol_follows_the_fitted_ring_model():
+    # 32 channels: LL has the lowest latency, Simple the highest bus bandwidth
+    small = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=256, nChannels=32)       # 1 KiB
+    big = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=16 << 20, nChannels=32)    # 64 MiB
+    assert (small.proto, big.proto) == (V.vProtoLL, V.vProtoSimple)
+    # the prediction is the smallest of the three protocols
+    for count in (256, 1 << 18, 1 << 20, 16 << 20):
+        auto = plan(algo=V.vAlgoRing, proto=V.vProtoAuto, count=count, nChannels=8)
+        each = [plan(algo=V.vAlgoRing, proto=p, count=count, nChannels=8).predictedUs for p in range(3)]
+        assert auto.predictedUs == pytest.approx(min(each))
+
+
+def test_model_reproduces_its_measured_anchor_points():
+    # fp32 all-reduce, 8 ranks: one-pass 2.1 us at 1 KiB, 676.6 us at 256 MiB per rank;
+    # ring Simple at 32 channels 49.4 us and 2569.7 us
+    assert plan(count=256).predictedUs == pytest.approx(2.1, rel=0.01)
+    assert plan(count=64 << 20).predictedUs == pytest.approx(676.6, rel=0.01)
+    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(49.4, rel=0.01)
+    assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=32).predictedUs == pytest.approx(2569.7, rel=0.01)
+
+
+def test_auto_algorithm_picks_the_one_pass_kernels():
+    for count in (256, 1 << 16, 1 << 22, 1 << 26):
+        for nch in (1, 8, 32):
+            p = plan(algo=V.vAlgoAuto, count=count, nChannels=nch, proto=V.vProtoAuto)
+            assert p.algo == V.vAlgoOnePass
+            assert p.predictedUs < plan(algo=V.vAlgoRing, count=count, nChannels=nch,
+                                        proto=V.vProtoAuto).predictedUs
+
+
+def test_prediction_grows_with_size_and_channels_help_the_ring():
+    prev = 0
+    for k in range(11):
+        t = plan(algo=V.vAlgoRing, count=256 * 4 ** k, nChannels=8).predictedUs
+        assert t > prev
+        prev = t
+    big = 16 << 20
+    assert plan(algo=V.vAlgoRing, count=big, nChannels=32).predictedUs < \
+        plan(algo=V.vAlgoRing, count=big, nChannels=1).predictedUs
 
 
 def test_one_rank_and_alltoall_always_one_pass():

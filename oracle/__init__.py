@@ -54,12 +54,16 @@ def lib() -> ctypes.CDLL:
             "orc_alltoall": [sz, i32, sz, pp, pp],
             "orc_alltoallv": [sz, i32, ip, ip, ip, pp, pp],
             "orc_reduce": [i32, i32, i32, sz, i32, pp, pp, i32],
+            "orc_allreduce_tree": [i32, i32, i32, sz, pp, pp, i32],
             "orc_gather": [sz, i32, sz, i32, pp, pp],
             "orc_scatter": [sz, i32, sz, i32, pp, pp],
         }.items():
             f = getattr(L, name)
             f.argtypes, f.restype = args, ctypes.c_int
         L.orc_block_elems.argtypes, L.orc_block_elems.restype = [sz, i32, sz], sz
+        ipn = ctypes.POINTER(ctypes.c_int)
+        L.orc_btree.argtypes, L.orc_btree.restype = [i32, i32, ipn, ipn, ipn], None
+        L.orc_dtree.argtypes, L.orc_dtree.restype = [i32, i32, i32, ipn, ipn, ipn], None
         L.orc_f32_to_type.argtypes, L.orc_f32_to_type.restype = [i32, sz, vp, vp], None
         L.orc_type_to_f32.argtypes, L.orc_type_to_f32.restype = [i32, sz, vp, vp], None
         _lib = L
@@ -96,6 +100,23 @@ def allreduce(xs, op: str = "sum", nthreads: int = 1):
     _ok(lib().orc_allreduce(DTYPE_CODE[xs[0].dtype], OP_CODE[op], n, count, _ptrs(xs), _ptrs(out),
                             nthreads), "allreduce")
     return out
+
+
+def allreduce_tree(xs, op: str = "sum", nthreads: int = 1):
+    """Double-binary-tree all-reduce (first half up tree 0, second half up tree 1)."""
+    _check(xs)
+    n, count = len(xs), xs[0].numel()
+    out = [torch.empty_like(xs[0]) for _ in range(n)]
+    _ok(lib().orc_allreduce_tree(DTYPE_CODE[xs[0].dtype], OP_CODE[op], n, count, _ptrs(xs), _ptrs(out),
+                                 nthreads), "allreduce_tree")
+    return out
+
+
+def tree_links(n: int, rank: int, tree: int = 0):
+    """(parent, child0, child1) of `rank` in tree 0 or 1 of the double binary tree."""
+    u, a, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    lib().orc_dtree(n, rank, tree, ctypes.byref(u), ctypes.byref(a), ctypes.byref(b))
+    return u.value, a.value, b.value
 
 
 def reduce_scatter(xs, op: str = "sum", nthreads: int = 1):

@@ -35,6 +35,12 @@
  *    (collective table, reduce row; NCCL runs Reduce as such a chain).  Gather:
  *    recv_root = concat over s of send_s.  Scatter: recv_r = block r of send_root
  *    (collective table, gather and scatter rows).
+ *  - Double binary tree all-reduce (NCCL book chapter 4, trees.cc ncclGetBtree /
+ *    ncclGetDtree): the first half of the buffer is reduced up tree 0 (the binary tree
+ *    rooted at rank 0 that ncclGetBtree builds from the ranks' lowest set bits), the
+ *    second half up tree 1 (tree 0 mirrored, rank r -> N-1-r, for even N; shifted,
+ *    r -> r+1, for odd N); every rank receives the root's result.  A node's partial is its
+ *    own element, then OP with the partial of child d0, then with that of child d1.
  *  - Special cases: count 0 does nothing; N = 1 is a plain copy (taskAppend:
  *    count==0 returns at once, nRanks==1 runs a local one-rank reduction).
  *
@@ -192,6 +198,54 @@ static uint32_t reduce_op(int dt, int op, uint32_t a, uint32_t b) {
     }
 }
 
+/* ---------------------------------------------------------------------------- */
+/* Trees.                                                                          */
+/* ---------------------------------------------------------------------------- */
+
+/* Parent and children of `rank` in the binary tree over ranks 0..n-1: the tree hangs
+ * from rank 0; a rank's lowest set bit `bit` fixes its level; its parent is the rank
+ * with that bit cleared and the next one set (or just cleared when that is out of
+ * range); its children are rank -/+ bit/2 (the right one shrunk until it is in range).
+ * -1 marks a missing link. */
+void orc_btree(int n, int rank, int* up, int* d0, int* d1) {
+    int bit = 1;
+    while (bit < n && !(bit & rank)) bit <<= 1;
+    if (rank == 0) {
+        *up = -1;
+        *d0 = -1;
+        *d1 = n > 1 ? bit >> 1 : -1;
+        return;
+    }
+    int u = (rank ^ bit) | (bit << 1);
+    if (u >= n) u = rank ^ bit;
+    *up = u;
+    int low = bit >> 1;
+    *d0 = low ? rank - low : -1;
+    int right = -1;
+    while (low) {
+        if (rank + low < n) { right = rank + low; break; }
+        low >>= 1;
+    }
+    *d1 = right;
+}
+
+/* Tree `t` (0 or 1) of the double binary tree. */
+void orc_dtree(int n, int rank, int t, int* up, int* d0, int* d1) {
+    if (t == 0) { orc_btree(n, rank, up, d0, d1); return; }
+    int u, a, b;
+    if (n % 2 == 0) {                       /* mirror */
+        orc_btree(n, n - 1 - rank, &u, &a, &b);
+        *up = u < 0 ? -1 : n - 1 - u;
+        *d0 = a < 0 ? -1 : n - 1 - a;
+        *d1 = b < 0 ? -1 : n - 1 - b;
+    } else {                                /* shift */
+        orc_btree(n, (rank - 1 + n) % n, &u, &a, &b);
+        *up = u < 0 ? -1 : (u + 1) % n;
+        *d0 = a < 0 ? -1 : (a + 1) % n;
+        *d1 = b < 0 ? -1 : (b + 1) % n;
+    }
+}
+
 static int valid_dt_op(int dt, int op) {
     return elem_size(dt) != 0 && op >= ORC_SUM && op <= ORC_MAX;
 }
@@ -219,7 +273,7 @@ static uint32_t ring_reduce(int dt, int op, int n, const void* const* x, size_t 
 
 typedef struct {
     int kind;                 /* 0 all-reduce, 1 reduce-scatter, 2 reduce-scatter + epilogue,
-                                 3 reduce to root */
+                                 3 reduce to root, 4 double-tree all-reduce */
     int dt, op, n, outdt;
     size_t count, recvcount, block;
     int root;
@@ -229,11 +283,40 @@ typedef struct {
     size_t lo, hi;            /* element range [lo, hi) of the flat send index handled */
 } job_t;
 
+/* Partial of the subtree under `v` in tree t, element e. */
+static uint32_t tree_reduce(int dt, int op, int n, const void* const* x, size_t esz, size_t e, int t, int v) {
+    int up, d0, d1;
+    orc_dtree(n, v, t, &up, &d0, &d1);
+    uint32_t acc = load_bits(x[v], esz, e);
+    if (d0 >= 0) acc = reduce_op(dt, op, acc, tree_reduce(dt, op, n, x, esz, e, t, d0));
+    if (d1 >= 0) acc = reduce_op(dt, op, acc, tree_reduce(dt, op, n, x, esz, e, t, d1));
+    return acc;
+}
+
+/* Root of tree t: the rank without a parent. */
+static int tree_root(int n, int t) {
+    for (int r = 0; r < n; r++) {
+        int up, d0, d1;
+        orc_dtree(n, r, t, &up, &d0, &d1);
+        if (up < 0) return r;
+    }
+    return 0;
+}
+
 static void run_job(const job_t* j) {
     size_t esz = elem_size(j->dt);
     if (j->kind == 0) {
         for (size_t e = j->lo; e < j->hi; e++) {
             uint32_t acc = ring_reduce(j->dt, j->op, j->n, j->send, esz, e, e / j->block);
+            for (int r = 0; r < j->n; r++) store_bits(j->recv[r], esz, e, acc);
+        }
+        return;
+    }
+    if (j->kind == 4) {
+        /* first half (block = the split point) up tree 0, the rest up tree 1 */
+        for (size_t e = j->lo; e < j->hi; e++) {
+            const int t = e < j->block ? 0 : 1;
+            const uint32_t acc = tree_reduce(j->dt, j->op, j->n, j->send, esz, e, t, tree_root(j->n, t));
             for (int r = 0; r < j->n; r++) store_bits(j->recv[r], esz, e, acc);
         }
         return;
@@ -310,6 +393,20 @@ int orc_reduce_scatter(int dt, int op, int n, size_t recvcount, const void* cons
     j.kind = 1; j.dt = dt; j.op = op; j.n = n; j.recvcount = recvcount;
     j.send = send; j.recv = recv;
     return run_split(j, recvcount * (size_t)n, nthreads);
+}
+
+/* Double-binary-tree all-reduce.  The split point between the two trees is
+ * alignUp(ceil(count / 2), 16 / elemSize) elements. */
+int orc_allreduce_tree(int dt, int op, int n, size_t count, const void* const* send, void* const* recv,
+                       int nthreads) {
+    if (!valid_dt_op(dt, op) || n < 1) return -1;
+    if (count == 0) return 0;
+    if (!send || !recv) return -2;
+    job_t j; memset(&j, 0, sizeof j);
+    j.kind = 4; j.dt = dt; j.op = op; j.n = n; j.count = count;
+    j.block = orc_block_elems(count, 2, elem_size(dt));
+    j.send = send; j.recv = recv;
+    return run_split(j, count, nthreads);
 }
 
 /* Reduce to root: only recv[root] is written. */

@@ -129,3 +129,38 @@ def ring_reduce_chain(xs, op: str, root: int):
     for k in range(2, n + 1):
         partial = combine(op, partial, xs[(root + k) % n])
     return partial
+
+
+def tree_allreduce(xs, op: str, links, split: int):
+    """Double-binary-tree all-reduce by messages up each tree: every rank starts with its
+    own element; a rank that has heard from all its children sends its partial to its
+    parent, which combines it in child order (child 0, then child 1).  `links(rank, t)`
+    gives (parent, child0, child1); elements [0, split) use tree 0, the rest tree 1."""
+    n = len(xs)
+    out = torch.empty_like(xs[0])
+    for t, sl in ((0, slice(0, split)), (1, slice(split, xs[0].numel()))):
+        partial = {r: xs[r][sl].clone() for r in range(n)}
+        pending = {r: [c for c in links(r, t)[1:] if c >= 0] for r in range(n)}
+        received = {r: {} for r in range(n)}
+        sent = set()
+        root = None
+        while len(sent) < n - 1 or root is None:
+            progress = False
+            for r in range(n):
+                parent = links(r, t)[0]
+                if r in sent or any(c not in received[r] for c in pending[r]):
+                    continue
+                value = partial[r]
+                for c in pending[r]:                     # child 0 first, then child 1
+                    value = combine(op, value, received[r][c])
+                if parent < 0:
+                    root = value
+                    sent.add(r)
+                else:
+                    received[parent][r] = value
+                    sent.add(r)
+                progress = True
+            if not progress:
+                raise RuntimeError("tree has a cycle or an unreachable rank")
+        out[sl] = root
+    return [out.clone() for _ in range(n)]

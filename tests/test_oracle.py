@@ -386,3 +386,74 @@ def test_gather_and_scatter_are_cat_and_chunk():
     # scatter of a gather gives every rank its own buffer back
     back = oracle.scatter(oracle.gather(xs, 2), n, 2)
     assert all(_same_bits(a, b) for a, b in zip(back, xs))
+
+
+# ---------------------------------------------------------------------------------------
+# Double binary tree
+# ---------------------------------------------------------------------------------------
+
+def test_btree_worked_example_golden(golden_dir):
+    (row,) = _read_rows(os.path.join(golden_dir, "btree_rank1_n8.txt"))
+    n, rank, parent, c0, c1 = row
+    assert oracle.tree_links(n, rank, 0) == (parent, c0, c1)
+
+
+@pytest.mark.parametrize("tree", [0, 1])
+def test_trees_are_spanning_trees(tree):
+    for n in range(1, 65):
+        links = [oracle.tree_links(n, r, tree) for r in range(n)]
+        roots = [r for r in range(n) if links[r][0] < 0]
+        assert len(roots) == 1, (n, roots)
+        for r, (up, c0, c1) in enumerate(links):
+            for c in (c0, c1):
+                if c >= 0:
+                    assert 0 <= c < n and links[c][0] == r, (n, r, c)
+            if up >= 0:
+                assert r in links[up][1:], (n, r, up)
+        seen, stack = set(), [roots[0]]
+        while stack:
+            v = stack.pop()
+            assert v not in seen
+            seen.add(v)
+            stack += [c for c in links[v][1:] if c >= 0]
+        assert seen == set(range(n)), n
+    # tree 0 hangs from rank 0; tree 1 is its mirror (even n) or shift (odd n)
+    assert oracle.tree_links(8, 0, 0)[0] < 0 and oracle.tree_links(8, 7, 1)[0] < 0
+    assert oracle.tree_links(5, 1, 1)[0] < 0
+
+
+def test_tree_order_golden_fp32(golden_dir):
+    for row in _read_rows(os.path.join(golden_dir, "tree_allreduce_order_n4.txt")):
+        count, expected = row[0], row[1:]
+        vals = [1.0, 2.0**24, 1.0, -(2.0**24)]
+        xs = [torch.full((count,), v, dtype=torch.float32) for v in vals]
+        for out in oracle.allreduce_tree(xs, "sum"):
+            assert out.tolist() == [float(v) for v in expected]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=lambda d: str(d).split(".")[1])
+@pytest.mark.parametrize("op", OPS)
+def test_tree_allreduce_matches_message_passing(dtype, op):
+    esz = torch.tensor([], dtype=dtype).element_size()
+    for n in (1, 2, 3, 4, 5, 7, 8, 13):
+        for count in (0, 1, 7, 16, 33, 255, 1000):
+            xs = _inputs(n, count, dtype, seed=3 * n + count)
+            got = oracle.allreduce_tree(xs, op)
+            split = -(-count // 2)
+            split = -(-split // (16 // esz)) * (16 // esz)
+            sim = ring_sim.tree_allreduce(xs, op, lambda r, t: oracle.tree_links(n, r, t), min(split, count))
+            for r in range(n):
+                assert _same_bits(got[r], sim[r]), (n, count, r)
+
+
+def test_tree_allreduce_library_special_cases():
+    xs = inputs.uniform_ranks(8, 3001, torch.int32, 12)
+    s64 = torch.stack([x.to(torch.int64) for x in xs])
+    assert torch.equal(oracle.allreduce_tree(xs, "sum")[3], ring_sim._wrap32(s64.sum(0)))
+    assert torch.equal(oracle.allreduce_tree(xs, "min")[0], s64.amin(0).to(torch.int32))
+    ys = inputs.small_int_ranks(8, 4000, torch.bfloat16, 2)
+    want = torch.stack([y.float() for y in ys]).sum(0).to(torch.bfloat16)
+    assert _same_bits(oracle.allreduce_tree(ys, "sum")[0], want)
+    # a different order than the ring: random fp32 sums differ somewhere
+    zs = inputs.uniform_ranks(8, 4096, torch.float32, 1)
+    assert not _same_bits(oracle.allreduce_tree(zs, "sum")[0], oracle.allreduce(zs, "sum")[0])

@@ -445,6 +445,11 @@ def other_workloads(torch, V, dev, stream, hbm):
     rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
     t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
     rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    tree = V.vcommInit(n, 1, V.vProtoSimple)
+    V.vcommSetAlgo(tree, "tree")
+    t = tm(lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", tree, stream))
+    rec("allreduce_double_binary_tree_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, 2 * f1)
+    V.vcommDestroy(tree)
     # group batching: 64 gradient buckets of 64 KiB fp32, separate calls vs one group
     nb, bc = 64, 16384
     bx = [[torch.rand(bc, device=dev) for _ in range(n)] for _ in range(nb)]

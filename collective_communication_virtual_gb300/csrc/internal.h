@@ -86,6 +86,23 @@ struct RingArgs {
     int testStallRank;               // test hook: this rank never posts data (-1 = off)
 };
 
+// Double-binary-tree all-reduce.  prog[t] lists tree t's ranks in post-order (children
+// before parents, child 0's subtree before child 1's); nchild[t][i] is the number of
+// children of prog[t][i].
+struct TreeArgs {
+    const void* send[VCOMM_MAX_RANKS];
+    void* recv[VCOMM_MAX_RANKS];
+    signed char prog[2][VCOMM_MAX_RANKS];
+    signed char nchild[2][VCOMM_MAX_RANKS];
+    int nRanks;
+    size_t count;
+    size_t split;                    // elements [0, split) use tree 0
+};
+constexpr int kTreeMaxStack = 16;
+
+cudaError_t launch_allreduce_tree(const TreeArgs& a, vDataType_t dt, vRedOp_t op, int vb, int grid,
+                                  int threads, cudaStream_t s);
+
 // A batch of all-reduces of one type and op run by one launch (group batching).  The
 // work table lives in device memory: items[i] describes all-reduce i, whose 2*N rank
 // pointers are ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).

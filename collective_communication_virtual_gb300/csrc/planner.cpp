@@ -90,7 +90,7 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     if (q->nChannels < 1 || q->nChannels > VCOMM_MAX_CHANNELS) return vInvalidArgument;
     if (q->coll < vCollAllReduce || q->coll > vCollScatter) return vInvalidArgument;
     if (q->proto < vProtoSimple || q->proto > vProtoAuto) return vInvalidArgument;
-    if (q->algo < vAlgoAuto || q->algo > vAlgoRing) return vInvalidArgument;
+    if (q->algo < vAlgoAuto || q->algo > vAlgoTree) return vInvalidArgument;
     const size_t esz = elem_size(q->datatype);
     if (esz == 0) return vInvalidArgument;
     if (q->chunkBytes != 0 && (q->chunkBytes < 4096 || q->chunkBytes > (64u << 20) ||
@@ -159,6 +159,22 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     const double tRing = ringable ? predict_ring_us(ringProto, q->coll, N, q->nChannels, bytesPerRank) : 0.0;
     bool ring = ringable && (q->algo == vAlgoRing || (q->algo == vAlgoAuto && tRing < tOne));
     p->algo = ring ? vAlgoRing : vAlgoOnePass;
+    if (q->algo == vAlgoTree && q->coll == vCollAllReduce && N > 1) {
+        // Double binary tree, one pass: two "blocks", the halves of the buffer.
+        p->algo = vAlgoTree;
+        p->blockElems = align_up(div_up(count, (size_t)2), VE);
+        if (p->vecBytes == 32 && (p->blockElems * esz) % 32 != 0) p->vecBytes = 16;
+        p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
+        p->nChannels = 1;
+        p->threadsPerCta = vc::kOnePassThreads;
+        const size_t unit = p->vecBytes ? p->vecBytes / esz : 1;
+        const size_t work = div_up(count, unit);
+        p->ctasPerChannel = (int)std::max<size_t>(1, std::min<size_t>((size_t)2 * smCount, div_up(work, vc::kOnePassThreads)));
+        p->gridCtas = p->ctasPerChannel;
+        p->predictedUs = tOne;
+        p->launches = 1;
+        return vSuccess;
+    }
     p->predictedUs = ring ? tRing : (q->coll == vCollAllToAllv ? 0.0 : tOne);
     p->launches = 1;
 
@@ -247,5 +263,44 @@ extern "C" vResult_t vPlanChannelRange(const vPlanInfo_t* p, size_t count, int c
     h = std::min(h, count);
     *lo = l;
     *hi = std::max(l, h);
+    return vSuccess;
+}
+
+extern "C" vResult_t vPlanTreeLinks(int nRanks, int rank, int tree, int* parent, int* child0, int* child1) {
+    if (nRanks < 1 || nRanks > VCOMM_MAX_RANKS || rank < 0 || rank >= nRanks || (tree != 0 && tree != 1) ||
+        !parent || !child0 || !child1)
+        return vInvalidArgument;
+    // Binary tree over ranks 0..n-1 (NCCL book chapter 4, ncclGetBtree): the lowest set bit
+    // of a rank is its level's step; rank 0 (no bit in range) is the root.
+    auto btree = [nRanks](int r, int* u, int* a, int* b) {
+        int step = 1;
+        while (step < nRanks && (r & step) == 0) step <<= 1;
+        if (r == 0) {
+            *u = -1;
+            *a = -1;
+            *b = nRanks > 1 ? step / 2 : -1;
+            return;
+        }
+        int up = (r ^ step) | (step << 1);
+        *u = up < nRanks ? up : (r ^ step);
+        int half = step / 2;
+        *a = half > 0 ? r - half : -1;
+        *b = -1;
+        for (; half > 0; half /= 2)
+            if (r + half < nRanks) { *b = r + half; break; }
+    };
+    if (tree == 0) {
+        btree(rank, parent, child0, child1);
+        return vSuccess;
+    }
+    // Second tree (ncclGetDtree): the first one mirrored for an even count, shifted by one
+    // rank for an odd count.
+    int u, a, b;
+    const bool mirror = nRanks % 2 == 0;
+    btree(mirror ? nRanks - 1 - rank : (rank + nRanks - 1) % nRanks, &u, &a, &b);
+    auto map = [&](int x) { return x < 0 ? -1 : (mirror ? nRanks - 1 - x : (x + 1) % nRanks); };
+    *parent = map(u);
+    *child0 = map(a);
+    *child1 = map(b);
     return vSuccess;
 }

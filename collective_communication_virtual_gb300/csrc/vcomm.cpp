@@ -128,6 +128,7 @@ void read_env(Config* cfg) {
     if (const char* s = std::getenv("VCOMM_ALGO")) {
         if (!std::strcmp(s, "onepass")) cfg->algo = vAlgoOnePass;
         else if (!std::strcmp(s, "ring")) cfg->algo = vAlgoRing;
+        else if (!std::strcmp(s, "tree")) cfg->algo = vAlgoTree;
         else cfg->algo = vAlgoAuto;
     }
     if (const char* s = std::getenv("VCOMM_CHUNK_BYTES")) {
@@ -619,7 +620,7 @@ vResult_t vcommGroupEnd(vcomm_t c) {
 }
 
 vResult_t vcommSetAlgo(vcomm_t c, vAlgo_t algo) {
-    if (!comm_ok(c) || algo < vAlgoAuto || algo > vAlgoRing) return vInvalidArgument;
+    if (!comm_ok(c) || algo < vAlgoAuto || algo > vAlgoTree) return vInvalidArgument;
     c->cfg.algo = algo;
     return vSuccess;
 }
@@ -689,6 +690,40 @@ vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, v
     debug_plan(c, vCollAllReduce, count, dt, p);
     if (p.algo == vAlgoRing)
         return launch_ring_plan(c, vCollAllReduce, send, recv, count, dt, op, dt, 0, false, 1.0f, p, stream);
+    if (p.algo == vAlgoTree) {
+        vc::TreeArgs ta;
+        std::memset(&ta, 0, sizeof(ta));
+        for (int r = 0; r < c->nRanks; r++) {
+            ta.send[r] = send[r];
+            ta.recv[r] = recv[r];
+        }
+        ta.nRanks = c->nRanks;
+        ta.count = count;
+        ta.split = std::min(p.blockElems, count);
+        for (int t = 0; t < 2; t++) {
+            // post-order of tree t: children before parents, child 0's subtree first
+            int root = 0;
+            for (int v = 0; v < c->nRanks; v++) {
+                int u, a0, a1;
+                vPlanTreeLinks(c->nRanks, v, t, &u, &a0, &a1);
+                if (u < 0) root = v;
+            }
+            int n = 0;
+            std::function<void(int)> visit = [&](int v) {
+                int u, a0, a1;
+                vPlanTreeLinks(c->nRanks, v, t, &u, &a0, &a1);
+                int kids = 0;
+                if (a0 >= 0) { visit(a0); kids++; }
+                if (a1 >= 0) { visit(a1); kids++; }
+                ta.prog[t][n] = (signed char)v;
+                ta.nchild[t][n] = (signed char)kids;
+                n++;
+            };
+            visit(root);
+        }
+        return finish_launch(c, vc::launch_allreduce_tree(ta, dt, op, p.vecBytes, p.gridCtas, p.threadsPerCta,
+                                                          stream), stream, "allreduce tree");
+    }
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, count);
     return finish_launch(c, vc::launch_allreduce_onepass(a, dt, op, p.vecBytes, p.gridCtas,

@@ -20,7 +20,7 @@ vInvalidArgument, vInvalidUsage, vTimeout, vInProgress, vAborted = 4, 5, 6, 7, 8
 vFloat32, vFloat16, vBFloat16, vInt32 = 0, 1, 2, 3
 vSum, vProd, vMin, vMax = 0, 1, 2, 3
 vProtoSimple, vProtoLL, vProtoLL128, vProtoAuto = 0, 1, 2, 3
-vAlgoAuto, vAlgoOnePass, vAlgoRing = 0, 1, 2
+vAlgoAuto, vAlgoOnePass, vAlgoRing, vAlgoTree = 0, 1, 2, 3
 vCollAllReduce, vCollReduceScatter, vCollAllGather = 0, 1, 2
 vCollBroadcast, vCollAllToAll, vCollAllToAllv = 3, 4, 5
 vCollReduce, vCollGather, vCollScatter = 6, 7, 8
@@ -31,7 +31,7 @@ RESULT_NAMES = {0: "vSuccess", 1: "vUnhandledCudaError", 2: "vSystemError", 3: "
                 8: "vAborted"}
 OPS = {"sum": vSum, "prod": vProd, "min": vMin, "max": vMax}
 PROTOCOLS = {"simple": vProtoSimple, "ll": vProtoLL, "ll128": vProtoLL128, "auto": vProtoAuto}
-ALGOS = {"auto": vAlgoAuto, "onepass": vAlgoOnePass, "ring": vAlgoRing}
+ALGOS = {"auto": vAlgoAuto, "onepass": vAlgoOnePass, "ring": vAlgoRing, "tree": vAlgoTree}
 
 
 class VcommError(RuntimeError):
@@ -81,6 +81,8 @@ _SIGNATURES = {
     "vcommQueryPlan": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                         ctypes.POINTER(vPlanInfo_t)], ctypes.c_int),
     "vPlanCompute": ([ctypes.POINTER(vPlanRequest_t), ctypes.POINTER(vPlanInfo_t)], ctypes.c_int),
+    "vPlanTreeLinks": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                        ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "vPlanChannelRange": ([ctypes.POINTER(vPlanInfo_t), ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                            ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "vAllReduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
@@ -242,6 +244,13 @@ def vPlanCompute(**req) -> vPlanInfo_t:
     info = vPlanInfo_t()
     _check(lib().vPlanCompute(ctypes.byref(q), ctypes.byref(info)), "vPlanCompute")
     return info
+
+
+def vPlanTreeLinks(n_ranks: int, rank: int, tree: int = 0) -> tuple[int, int, int]:
+    u, a, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().vPlanTreeLinks(n_ranks, rank, tree, ctypes.byref(u), ctypes.byref(a), ctypes.byref(b)),
+           "vPlanTreeLinks")
+    return u.value, a.value, b.value
 
 
 def vPlanChannelRange(plan: vPlanInfo_t, count: int, channel: int, block: int) -> tuple[int, int]:

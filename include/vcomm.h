@@ -92,8 +92,14 @@ typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 }
  * section 2.3, N-1 reduce-scatter steps then N-1 all-gather steps, each hop staged
  * through a device FIFO with the communicator's protocol.  Both give identical bits.
  * vAlgoAuto picks the smaller predicted time (on GB300 the one-pass kernels are faster
- * at every size: about 2 us of latency against 33-56 us for the ring's steps). */
-typedef enum { vAlgoAuto = 0, vAlgoOnePass = 1, vAlgoRing = 2 } vAlgo_t;
+ * at every size: about 2 us of latency against 33-56 us for the ring's steps).
+ * vAlgoTree (all-reduce only; other collectives run one-pass): the double binary tree of
+ * the NCCL book chapter 4 (ncclGetBtree / ncclGetDtree).  The first half of the buffer,
+ * up to alignUp(ceil(count / 2), 16 / elemSize) elements, is reduced up tree 0, the rest
+ * up tree 1; a tree node combines its own element, then child 0's partial, then child
+ * 1's; every rank receives the root's result.  Its bits generally differ from the ring
+ * order's (a different reduction order). */
+typedef enum { vAlgoAuto = 0, vAlgoOnePass = 1, vAlgoRing = 2, vAlgoTree = 3 } vAlgo_t;
 
 typedef enum {
     vCollAllReduce = 0, vCollReduceScatter = 1, vCollAllGather = 2,
@@ -316,6 +322,12 @@ vResult_t vPlanChannelRange(const vPlanInfo_t* plan, size_t count, int channel, 
  * starts (its CTAs return at once), so its neighbours' bounded waits run out and the
  * transfer ends with the sticky error vTimeout.  -1 turns the hook off. */
 vResult_t vcommTestSetStallRank(vcomm_t comm, int rank);
+
+/* Links of `rank` in tree `tree` (0 or 1) of the double binary tree over nRanks ranks
+ * (NCCL book chapter 4, ncclGetBtree / ncclGetDtree): tree 0 hangs from rank 0, a
+ * rank's lowest set bit fixes its level; tree 1 mirrors it (rank r -> nRanks-1-r) for an
+ * even rank count and shifts it (r -> r+1) for an odd one.  -1 marks a missing link. */
+vResult_t vPlanTreeLinks(int nRanks, int rank, int tree, int* parent, int* child0, int* child1);
 
 /* vPlanCompute for this communicator's device and settings.  `aligned` is the largest
  * power-of-two alignment (in bytes, up to 32) shared by every buffer pointer. */

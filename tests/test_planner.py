@@ -1,6 +1,8 @@
 """Host planner (vPlanCompute / vPlanChannelRange), no GPU needed."""
 from __future__ import annotations
 
+import os
+
 import pytest
 
 import oracle
@@ -199,8 +201,27 @@ def test_grid_is_about_two_ctas_per_sm_and_never_idle():
 
 def test_bad_requests():
     for kw in [dict(nRanks=0), dict(nRanks=65), dict(nChannels=0), dict(nChannels=65), dict(coll=9),
-               dict(datatype=7), dict(proto=5), dict(algo=4), dict(chunkBytes=1000), dict(coll=10),
+               dict(datatype=7), dict(proto=5), dict(algo=5), dict(chunkBytes=1000), dict(coll=10),
                dict(chunkBytes=3 << 20)]:
         with pytest.raises(V.VcommError) as e:
             plan(**kw)
         assert e.value.code == V.vInvalidArgument
+
+
+def test_tree_links_match_the_pages_example_and_the_oracle(golden_dir):
+    # NCCL book ncclGetBtree worked example: rank 1 of 8 is a leaf under rank 2
+    with open(os.path.join(golden_dir, "btree_rank1_n8.txt")) as f:
+        row = [l for l in f if l.strip() and not l.startswith("#")][0].split()
+    n, rank, parent, c0, c1 = map(int, row)
+    assert V.vPlanTreeLinks(n, rank, 0) == (parent, c0, c1)
+    for n in range(1, 65):
+        for t in (0, 1):
+            for r in range(n):
+                assert V.vPlanTreeLinks(n, r, t) == oracle.tree_links(n, r, t), (n, t, r)
+
+
+def test_tree_plan():
+    p = plan(algo=V.vAlgoTree, count=16 << 20)
+    assert p.algo == V.vAlgoTree and p.blockElems == 8 << 20
+    assert plan(algo=V.vAlgoTree, count=16 << 20, coll=V.vCollReduceScatter).algo == V.vAlgoOnePass
+    assert plan(algo=V.vAlgoTree, count=100, nRanks=1).algo == V.vAlgoOnePass

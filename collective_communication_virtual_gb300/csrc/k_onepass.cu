@@ -20,10 +20,24 @@ namespace vc {
 
 // Load the VB-byte vector at byte offset `boff` of every rank, starting at rank `first`
 // and wrapping, and reduce in that order.  Up to 8 loads are in flight before the first use.
-template <int DT, int OP, int VB>
-__device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const void* const* send, int N,
+template <int DT, int OP, int VB, int NF = 0>
+__device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const void* const* send, int Nrt,
                                                                 int first, size_t boff) {
     using VT = typename VecOf<VB>::T;
+    const int N = NF ? NF : Nrt;
+    if (NF) {
+        // rank count known at compile time: all loads issued, then the fold, unrolled
+        VT v[NF ? NF : 1];
+#pragma unroll
+        for (int k = 0; k < NF; k++) {
+            const int rk = first + k >= NF ? first + k - NF : first + k;
+            v[k] = VecOf<VB>::ld((const char*)send[rk] + boff);
+        }
+        VT acc = v[0];
+#pragma unroll
+        for (int k = 1; k < NF; k++) acc = op_vec<DT, OP>(acc, v[k]);
+        return acc;
+    }
     VT acc = VecOf<VB>::ld((const char*)send[first] + boff);
     int rk = first + 1 == N ? 0 : first + 1;
     for (int k = 1; k < N; k += 8) {
@@ -76,12 +90,12 @@ __device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch
 // path), 16 or 32 bytes per vector; the 32-byte kernel keeps twice the registers, so it
 // runs one 512-thread CTA per SM instead of two.  Reduce to root (a.orderRoot = a.outRoot
 // = root) reduces every block in the root's order and writes only recv[root].
-template <int DT, int OP, int VB>
+template <int DT, int OP, int VB, int NF = 0>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
-    const int N = a.nRanks;
+    const int N = NF ? NF : a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
     const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
@@ -101,8 +115,13 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
         const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
         if (VB && e + U <= hi) {
             const size_t boff = e * ESZ;
-            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a.send, N, first, boff);
-            for (int r = r0; r < r1; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16, NF>(a.send, N, first, boff);
+            if (NF && a.outRoot < 0) {
+#pragma unroll
+                for (int r = 0; r < (NF ? NF : 1); r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
+            } else {
+                for (int r = r0; r < r1; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
+            }
         } else {
             for (size_t x = e; x < min(e + U, hi); x++) {
                 const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, x);
@@ -445,7 +464,9 @@ k_allreduce_tree_fixed(const __grid_constant__ TreeArgs a) {
 template <int DT, int OP>
 static cudaError_t ar_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
                                    cudaStream_t s) {
-    if (vb == 32) k_allreduce_onepass<DT, OP, 32><<<grid, threads, 0, s>>>(a);
+    if (a.nRanks == 8 && vb == 32) k_allreduce_onepass<DT, OP, 32, 8><<<grid, threads, 0, s>>>(a);
+    else if (a.nRanks == 8 && vb == 16) k_allreduce_onepass<DT, OP, 16, 8><<<grid, threads, 0, s>>>(a);
+    else if (vb == 32) k_allreduce_onepass<DT, OP, 32><<<grid, threads, 0, s>>>(a);
     else if (vb == 16) k_allreduce_onepass<DT, OP, 16><<<grid, threads, 0, s>>>(a);
     else k_allreduce_onepass<DT, OP, 0><<<grid, threads, 0, s>>>(a);
     return cudaGetLastError();

@@ -103,10 +103,13 @@ constexpr int kTreeMaxStack = 16;
 cudaError_t launch_allreduce_tree(const TreeArgs& a, vDataType_t dt, vRedOp_t op, int vb, int grid,
                                   int threads, cudaStream_t s);
 
-// A batch of all-reduces of one type and op run by one launch (group batching).  The
-// work table lives in device memory: items[i] describes all-reduce i, whose 2*N rank
-// pointers are ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).
-constexpr int kMaxGroupItems = 1024;
+// A batch of all-reduces of one type and op run by one launch (group batching).  The work
+// table travels inside the kernel's parameter block (which may hold up to 32,764 bytes), so
+// a batch needs no upload, no device memory and no host staging, and a launch captured
+// into a CUDA graph carries its own copy.  table: items[0..nItems) (item i describes
+// all-reduce i), then at byte ptrByteOff the rank pointers: item i's 2*N pointers are
+// ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).
+constexpr int kGroupTableBytes = 32 * 1024 - 256;
 struct GroupItem {
     unsigned long long unitStart;    // first flat work unit of this item
     unsigned long long count;        // elements per rank
@@ -116,12 +119,19 @@ struct GroupItem {
     int pad;
 };
 struct GroupArgs {
-    const GroupItem* items;
-    const void* const* ptrs;
     int nItems;
     int nRanks;
     unsigned long long totalUnits;
+    int ptrByteOff;                  // multiple of 16
+    int pad;
+    alignas(16) unsigned char table[kGroupTableBytes];
 };
+// Items one launch can hold for nRanks ranks, and the most for any rank count.
+constexpr int group_capacity(int nRanks) {
+    return (int)((kGroupTableBytes - 16) / (sizeof(GroupItem) + 2 * (size_t)nRanks * sizeof(void*)));
+}
+constexpr int kMaxGroupItems = group_capacity(1);
+static_assert(sizeof(GroupArgs) <= 32764, "kernel parameters are limited to 32,764 bytes");
 
 // Launchers (defined in the kernel translation units).  Each returns the launch status.
 // vb: bytes per vector of the one-pass reductions, 0 (element path), 16 or 32.

@@ -230,8 +230,10 @@ __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_group(const __grid_constant__ GroupArgs a) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
+    const GroupItem* items = reinterpret_cast<const GroupItem*>(a.table);
+    const void* const* ptrs = reinterpret_cast<const void* const*>(a.table + a.ptrByteOff);
     __shared__ unsigned long long sStart[kMaxGroupItems];
-    for (int i = threadIdx.x; i < a.nItems; i += blockDim.x) sStart[i] = a.items[i].unitStart;
+    for (int i = threadIdx.x; i < a.nItems; i += blockDim.x) sStart[i] = items[i].unitStart;
     __syncthreads();
     const int N = a.nRanks;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -242,9 +244,9 @@ k_allreduce_group(const __grid_constant__ GroupArgs a) {
             if (sStart[mid] <= j) lo = mid;
             else hi = mid - 1;
         }
-        const GroupItem it = a.items[lo];
-        const void* const* send = a.ptrs + it.ptrOff;
-        void* const* recv = (void* const*)(a.ptrs + it.ptrOff + N);
+        const GroupItem it = items[lo];
+        const void* const* send = ptrs + it.ptrOff;
+        void* const* recv = (void* const*)(ptrs + it.ptrOff + N);
         const size_t u = j - it.unitStart;
         const int b = (int)(u / it.unitsPerBlock);
         const size_t e = (size_t)b * it.blockElems + (u - (size_t)b * it.unitsPerBlock) * U;

@@ -169,7 +169,10 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         p->threadsPerCta = vc::kOnePassThreads;
         const size_t unit = p->vecBytes ? p->vecBytes / esz : 1;
         const size_t work = div_up(count, unit);
-        p->ctasPerChannel = (int)std::max<size_t>(1, std::min<size_t>((size_t)2 * smCount, div_up(work, vc::kOnePassThreads)));
+        // The 8-rank 32-byte kernel keeps its vectors in registers (one CTA per SM); the
+        // others fit two per SM.
+        const size_t resident = (size_t)((N == 8 && p->vecBytes == 32) ? 1 : 2) * smCount;
+        p->ctasPerChannel = (int)std::max<size_t>(1, std::min<size_t>(resident, div_up(work, vc::kOnePassThreads)));
         p->gridCtas = p->ctasPerChannel;
         p->predictedUs = tOne;
         p->launches = 1;

@@ -76,11 +76,7 @@ struct vcomm {
     // group batching
     int groupDepth;
     std::vector<GroupRec>* group;
-    char* groupTable[2];             // device work tables (items, then rank pointers)
-    char* groupStage[2];             // pinned staging of the tables
-    cudaEvent_t groupEv[2];
-    bool groupEvRecorded[2];
-    unsigned groupSlot;
+    vc::GroupArgs* groupArgs;        // host copy of a batch's parameter block
     unsigned long long endMagic;
 };
 
@@ -145,11 +141,7 @@ void read_env(Config* cfg) {
 
 void free_comm(vcomm* c) {
     delete c->group;
-    for (int k = 0; k < 2; k++) {
-        if (c->groupEv[k]) cudaEventDestroy(c->groupEv[k]);
-        if (c->groupTable[k]) cudaFree(c->groupTable[k]);
-        if (c->groupStage[k]) cudaFreeHost(c->groupStage[k]);
-    }
+    delete c->groupArgs;
     if (c->lastEvent) cudaEventDestroy(c->lastEvent);
     if (c->fifo) cudaFree(c->fifo);
     if (c->ctrl) cudaFree(c->ctrl);
@@ -359,35 +351,22 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
     return finish_launch(c, e, stream, "ring launch");
 }
 
-size_t group_table_bytes(int nRanks) {
-    return (size_t)vc::kMaxGroupItems * sizeof(vc::GroupItem) +
-           (size_t)vc::kMaxGroupItems * 2 * (size_t)nRanks * sizeof(void*);
-}
-
-// One launch for up to kMaxGroupItems recorded all-reduces of one type, op, stream and
-// vector width.  The work table goes through one of two pinned staging buffers, each
-// reused only after the launch that last read it has finished.
+// One launch for up to vc::group_capacity(N) recorded all-reduces of one type, op, stream
+// and vector width.  The work table is built in the kernel's parameter block, which the
+// launch copies, so the host copy is free for the next batch as soon as this returns.
 vResult_t launch_group_batch(vcomm* c, const std::vector<const GroupRec*>& items) {
     const int N = c->nRanks;
     const GroupRec& r0 = *items[0];
-    const size_t tableBytes = group_table_bytes(N);
-    if (!c->groupTable[0]) {
-        for (int k = 0; k < 2; k++) {
-            cudaError_t e = cudaMalloc(&c->groupTable[k], tableBytes);
-            if (e == cudaSuccess) e = cudaHostAlloc(&c->groupStage[k], tableBytes, cudaHostAllocDefault);
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->groupEv[k], cudaEventDisableTiming);
-            if (e != cudaSuccess) return cuda_fail(c, e, "group buffers");
-        }
-    }
-    const int k = (int)(c->groupSlot++ & 1u);
-    if (c->groupEvRecorded[k]) cudaEventSynchronize(c->groupEv[k]);
-    // Table: the batch's items, then their rank pointers right after them, so one copy
-    // uploads both.
     const size_t n = items.size();
+    if (n > (size_t)vc::group_capacity(N)) return vInternalError;
+    if (!c->groupArgs) {
+        c->groupArgs = new (std::nothrow) vc::GroupArgs;
+        if (!c->groupArgs) return vSystemError;
+    }
+    vc::GroupArgs& a = *c->groupArgs;
     const size_t itemBytes = (n * sizeof(vc::GroupItem) + 15) / 16 * 16;
-    const size_t tableUsed = itemBytes + n * 2 * (size_t)N * sizeof(void*);
-    vc::GroupItem* it = reinterpret_cast<vc::GroupItem*>(c->groupStage[k]);
-    const void** ptrs = reinterpret_cast<const void**>(c->groupStage[k] + itemBytes);
+    vc::GroupItem* it = reinterpret_cast<vc::GroupItem*>(a.table);
+    const void** ptrs = reinterpret_cast<const void**>(a.table + itemBytes);
     const size_t esz = elem_size(r0.dt);
     const size_t U = r0.vecBytes ? (size_t)r0.vecBytes / esz : 1;
     unsigned long long units = 0;
@@ -405,26 +384,17 @@ vResult_t launch_group_batch(vcomm* c, const std::vector<const GroupRec*>& items
         }
         units += it[i].unitsPerBlock * (unsigned long long)N;
     }
-    (void)tableBytes;
-    cudaError_t e = cudaMemcpyAsync(c->groupTable[k], c->groupStage[k], tableUsed, cudaMemcpyHostToDevice,
-                                    r0.stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "group table upload");
-    vc::GroupArgs a;
-    a.items = reinterpret_cast<const vc::GroupItem*>(c->groupTable[k]);
-    a.ptrs = reinterpret_cast<const void* const*>(c->groupTable[k] + itemBytes);
     a.nItems = (int)n;
     a.nRanks = N;
     a.totalUnits = units;
+    a.ptrByteOff = (int)itemBytes;
+    a.pad = 0;
     const int perSm = r0.vecBytes == 32 ? 1 : 2;
     const unsigned long long need = (units + vc::kOnePassThreads - 1) / vc::kOnePassThreads;
     const int grid = (int)std::min<unsigned long long>((unsigned long long)perSm * c->smCount, std::max(1ull, need));
-    e = vc::launch_allreduce_group(a, r0.dt, r0.op, r0.vecBytes, grid, vc::kOnePassThreads, r0.stream);
-    if (e != cudaSuccess) {
-        c->hostError = vUnhandledCudaError;
-        return cuda_fail(c, e, "group launch");
-    }
-    if (cudaEventRecord(c->groupEv[k], r0.stream) == cudaSuccess) c->groupEvRecorded[k] = true;
-    return finish_launch(c, cudaSuccess, r0.stream, "group");
+    const cudaError_t e = vc::launch_allreduce_group(a, r0.dt, r0.op, r0.vecBytes, grid, vc::kOnePassThreads,
+                                                     r0.stream);
+    return finish_launch(c, e, r0.stream, "group launch");
 }
 
 // Shared front half of every collective.
@@ -583,7 +553,7 @@ vResult_t vcommGroupEnd(vcomm_t c) {
     if (!g.ok) return vUnhandledCudaError;
     vResult_t first = vSuccess;
     // Fused all-reduces: batches of one (type, op, stream, vector width), in order of
-    // their first call; a batch of one, or one on a capturing stream, runs on its own.
+    // their first call; a batch of one runs on its own.
     std::vector<bool> done(recs.size(), false);
     for (size_t i = 0; i < recs.size(); i++) {
         if (!recs[i].fusable || done[i]) continue;
@@ -597,15 +567,15 @@ vResult_t vcommGroupEnd(vcomm_t c) {
             batch.push_back(&b);
             done[j] = true;
         }
-        const bool single = batch.size() == 1 || stream_capturing(recs[i].stream);
-        for (size_t k = 0; k < batch.size(); k += (single ? 1 : vc::kMaxGroupItems)) {
+        const bool single = batch.size() == 1;
+        const size_t cap = (size_t)vc::group_capacity(c->nRanks);
+        for (size_t k = 0; k < batch.size(); k += (single ? 1 : cap)) {
             vResult_t r;
             if (single) {
                 const GroupRec& b = *batch[k];
                 r = vAllReduce(b.send.data(), b.recv.data(), b.count, b.dt, b.op, c, b.stream);
             } else {
-                std::vector<const GroupRec*> part(batch.begin() + k,
-                                                  batch.begin() + std::min(batch.size(), k + vc::kMaxGroupItems));
+                std::vector<const GroupRec*> part(batch.begin() + k, batch.begin() + std::min(batch.size(), k + cap));
                 r = launch_group_batch(c, part);
             }
             if (r != vSuccess && first == vSuccess) first = r;

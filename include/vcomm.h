@@ -144,14 +144,15 @@ const char* vcommGetErrorString(vResult_t result);
  * ncclGroupEnd).  Between vcommGroupStart and vcommGroupEnd every collective call on
  * this communicator is checked and recorded (its pointer arrays copied) and returns
  * vSuccess; nothing is enqueued.  vcommGroupEnd enqueues them: one-pass all-reduces of
- * the same type, op, stream and vector width are fused into one kernel launch (up to
- * 1024 per launch, each keeping its own block order, so the bits equal separate calls);
- * every other call is enqueued as its own launch, in call order.  Calls in one group
- * must not depend on each other's results.  Groups nest; only the outermost end
- * enqueues.  vcommGroupEnd returns the first error of the recorded calls, or
- * vInvalidUsage without a matching start.  On a stream being captured into a CUDA
- * graph the all-reduces are enqueued one by one.  The communicator keeps two small
- * device work tables and their pinned staging copies for the fused launches. */
+ * the same type, op, stream and vector width are fused into one kernel launch (each
+ * keeping its own block order, so the bits equal separate calls); a launch holds as many
+ * as its 32 KiB parameter block fits: 32,496 / (40 + 16 N) of them, 193 at N = 8, and a
+ * larger batch takes several launches.  Every other call is enqueued as its own launch,
+ * in call order.  Calls in one group must not depend on each other's results.  Groups
+ * nest; only the outermost end enqueues.  vcommGroupEnd returns the first error of the
+ * recorded calls, or vInvalidUsage without a matching start.  The work table travels in
+ * the launch's parameters: no device memory, no upload, and on a stream being captured
+ * into a CUDA graph the fused launch is captured like any other. */
 vResult_t vcommGroupStart(vcomm_t comm);
 vResult_t vcommGroupEnd(vcomm_t comm);
 

@@ -109,3 +109,27 @@ def test_ring_all_reduce_in_a_group_runs_unfused(comm):
     torch.cuda.synchronize()
     V.vcommSetAlgo(comm, "auto")
     assert_bits_equal(recv, oracle.allreduce(xs, "sum"), "ring in group")
+
+
+def test_group_captured_in_a_graph_replays_the_fused_launch(comm):
+    # The work table rides in the launch's parameters, so a captured group replays with
+    # its own table; new data written into the same buffers gives new, exact results.
+    n, counts = 8, [4096, 1000, 77, 65_536, 3]
+    bufs = [(empty_dev(n, c, torch.float32), empty_dev(n, c, torch.float32)) for c in counts]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        V.vcommGroupStart(comm)
+        for (send, recv), c in zip(bufs, counts):
+            V.vAllReduce(send, recv, c, torch.float32, "sum", comm)
+        V.vcommGroupEnd(comm)
+    for rep in range(2):
+        xss = [inputs.uniform_ranks(n, c, torch.float32, seed=50 + 10 * rep + i) for i, c in enumerate(counts)]
+        for (send, _), xs in zip(bufs, xss):
+            for r in range(n):
+                send[r].copy_(xs[r])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert V.vcommGetAsyncError(comm) == V.vSuccess
+        for (_, recv), xs in zip(bufs, xss):
+            assert_bits_equal(recv, oracle.allreduce(xs, "sum"), f"captured group, replay {rep}")

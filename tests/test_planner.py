@@ -223,5 +223,11 @@ def test_tree_links_match_the_pages_example_and_the_oracle(golden_dir):
 def test_tree_plan():
     p = plan(algo=V.vAlgoTree, count=16 << 20)
     assert p.algo == V.vAlgoTree and p.blockElems == 8 << 20
+    # grid = one wave of resident CTAs: one per SM for the register-held 8-rank 32-byte
+    # kernel, two per SM otherwise
+    wide = plan(algo=V.vAlgoTree, count=16 << 20, aligned32=1)
+    assert wide.vecBytes == 32 and wide.gridCtas == 152
+    assert plan(algo=V.vAlgoTree, count=16 << 20, nRanks=4, aligned32=1).gridCtas == 304
+    assert p.vecBytes == 16 and p.gridCtas == 304
     assert plan(algo=V.vAlgoTree, count=16 << 20, coll=V.vCollReduceScatter).algo == V.vAlgoOnePass
     assert plan(algo=V.vAlgoTree, count=100, nRanks=1).algo == V.vAlgoOnePass

@@ -168,7 +168,7 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
         const int i = p / N, j = p - (p / N) * N;
         const int32_t cnt = a.counts[p], so = a.sdispls[p], ro = a.rdispls[j * N + i];
         unsigned long long tiles = 0;
-        if (cnt < 0 || so < 0 || ro < 0) sBad = 1;
+        if (cnt < 0 || so < 0 || ro < 0 || (cnt > 0 && (!a.send[i] || !a.recv[j]))) sBad = 1;
         else tiles = ((unsigned long long)cnt + tileElems - 1) / tileElems;
         tileStart[p + 1] = tiles;
     }

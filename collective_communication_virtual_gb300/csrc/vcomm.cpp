@@ -914,10 +914,17 @@ vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* 
     vResult_t s = sticky(c);
     if (s != vSuccess) return s;
     const size_t esz = elem_size(dt);
-    if (esz == 0 || !counts || !sdispls || !rdispls) return vInvalidArgument;
-    int aligned = 0;
-    vResult_t r = check_ptrs(c, send, recv, esz, 0, true, &aligned);
-    if (r != vSuccess) return r;
+    if (esz == 0 || !counts || !sdispls || !rdispls || !send || !recv) return vInvalidArgument;
+    // NULL entries are allowed (a rank with nothing to send or receive); the kernel
+    // rejects a positive count that would touch one.
+    uintptr_t bits = 32;
+    for (int i = 0; i < c->nRanks; i++) {
+        if ((send[i] && !ptr_aligned(send[i], esz)) || (recv[i] && !ptr_aligned(recv[i], esz)))
+            return vInvalidArgument;
+        bits |= (uintptr_t)send[i] | (uintptr_t)recv[i];
+    }
+    const int aligned = (int)(bits & (~bits + 1));
+    vResult_t r;
     DeviceGuard g(c->device);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;

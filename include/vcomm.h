@@ -220,9 +220,11 @@ vResult_t vAllToAll(const void* const* sendbuffs, void* const* recvbuffs, size_t
 /* Variable all-to-all.  counts, sdispls and rdispls are DEVICE arrays of nRanks *
  * nRanks int32 values, in elements: counts[i * nRanks + j] elements go from
  * sendbuffs[i] + sdispls[i * nRanks + j] to recvbuffs[j] + rdispls[j * nRanks + i].
- * The caller guarantees that every block lies inside its buffers.  A negative entry
- * makes the kernel skip that block and sets the sticky error vInvalidArgument.
- * Send and receive buffers must not overlap. */
+ * The caller guarantees that every block lies inside its buffers.  A rank that sends
+ * (receives) nothing may pass a NULL send (receive) buffer, as an empty tensor has.  A
+ * negative entry, or a positive count whose source or destination buffer is NULL, makes
+ * the kernel skip that block and sets the sticky error vInvalidArgument.  Send and
+ * receive buffers must not overlap. */
 vResult_t vAllToAllv(const void* const* sendbuffs, void* const* recvbuffs, const int32_t* counts,
                      const int32_t* sdispls, const int32_t* rdispls, vDataType_t datatype,
                      vcomm_t comm, cudaStream_t stream);

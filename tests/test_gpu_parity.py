@@ -479,6 +479,43 @@ def test_abort_stops_a_waiting_transfer():
         V.vcommDestroy(c)
 
 
+def test_alltoallv_rank_with_nothing_to_send_or_receive():
+    # An empty tensor has a NULL data pointer; a rank that sends (or receives) nothing may
+    # pass one.  Rank 2 sends nothing, rank 3 receives nothing.
+    n = 4
+    counts = torch.tensor([[5, 0, 7, 0], [1, 2, 3, 0], [0, 0, 0, 0], [9, 4, 0, 0]], dtype=torch.int32)
+    sd = (torch.cumsum(counts, 1) - counts).to(torch.int32)
+    rd = (torch.cumsum(counts, 0) - counts).t().contiguous().to(torch.int32)
+    recv_elems = [int(v) for v in counts.sum(0)]
+    xs = [torch.arange(int(counts[i].sum()), dtype=torch.float32) + 1000 * i for i in range(n)]
+    send = [x.to(DEV) for x in xs]
+    recv = [torch.full((e,), -1.0, device=DEV) for e in recv_elems]
+    assert send[2].data_ptr() == 0 and recv[3].data_ptr() == 0
+    c = V.vcommInit(n, 1, V.vProtoSimple)
+    try:
+        V.vAllToAllv(send, recv, *[t.to(DEV) for t in (counts, sd, rd)], torch.float32, c)
+        torch.cuda.synchronize()
+        assert V.vcommGetAsyncError(c) == V.vSuccess
+        assert_bits_equal(recv, oracle.alltoallv(xs, counts, sd, rd, recv_elems), "alltoallv empty ranks")
+    finally:
+        V.vcommDestroy(c)
+
+
+def test_alltoallv_positive_count_into_null_buffer_sets_async_error():
+    n = 2
+    c = V.vcommInit(n, 1, V.vProtoSimple)
+    try:
+        counts = torch.tensor([[2, 2], [2, 2]], dtype=torch.int32, device=DEV)
+        sd = torch.tensor([[0, 2], [0, 2]], dtype=torch.int32, device=DEV)
+        x = [torch.zeros(4, device=DEV) for _ in range(n)]
+        y = [torch.zeros(4, device=DEV), None]
+        V.vAllToAllv(x, y, counts, sd, sd, torch.float32, c)
+        torch.cuda.synchronize()
+        assert V.vcommGetAsyncError(c) == V.vInvalidArgument
+    finally:
+        V.vcommDestroy(c)
+
+
 def test_bad_alltoallv_table_sets_async_error():
     n = 2
     c = V.vcommInit(n, 1, V.vProtoSimple)

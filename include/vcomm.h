@@ -120,7 +120,7 @@ typedef enum {
  * with ncclInvalidArgument, "NCCL Expert Course 17").  No usable device gives
  * vUnhandledCudaError.  The communicator owns a small status block in pinned host
  * memory and, once a ring transfer is planned, its staging FIFOs in device memory.
- * Environment (read once here): VCOMM_ALGO=auto|onepass|ring, VCOMM_CHUNK_BYTES,
+ * Environment (read once here): VCOMM_ALGO=auto|onepass|ring|tree, VCOMM_CHUNK_BYTES,
  * VCOMM_TIMEOUT_MS, VCOMM_COPY_TMA=0|1 (1, the default: all-gather, gather and broadcast
  * stage tiles in shared memory with TMA bulk copies when blocks are 16-byte aligned; 0:
  * every thread loads and stores), VCOMM_DEBUG=INFO (prints every plan to stderr). */

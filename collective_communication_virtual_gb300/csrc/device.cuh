@@ -151,21 +151,22 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
 }
 
 // 32-byte accesses (Blackwell's 256-bit global loads and stores): half the instructions
-// of the 16-byte path for the same bytes in flight.  Data streamed once is marked
-// evict-first in L2 so it does not displace lines that are still to be read.
+// of the 16-byte path for the same bytes in flight.  No L2 eviction hint: with the CTAs
+// of a flat grid dispatched in order, plain accesses measured about 1 % faster than
+// evict-first ones on GB300.
 struct V32 {
     uint4 lo, hi;
 };
 __device__ __forceinline__ V32 ld_stream32(const void* p) {
     V32 v;
-    asm("ld.global.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm("ld.global.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y),
           "=r"(v.hi.z), "=r"(v.hi.w)
         : "l"(p));
     return v;
 }
 __device__ __forceinline__ void st_stream32(void* p, const V32& v) {
-    asm volatile("st.global.L2::evict_first.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
                  :: "l"(p), "r"(v.lo.x), "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x),
                     "r"(v.hi.y), "r"(v.hi.z), "r"(v.hi.w)
                  : "memory");

@@ -41,6 +41,7 @@ struct OnePassArgs {
     size_t count;                    // AR: count; RS: N*recvcount; AG: sendcount; BC: count; A2A: block
     size_t blockElems;               // B
     size_t chanElems;                // elements of each block owned by one channel
+    size_t tileBytes;                // copy kernels: bytes of one CTA's tile
 };
 
 struct A2AvArgs {
@@ -52,9 +53,14 @@ struct A2AvArgs {
     int nRanks;
     int elemSize;
     size_t tileBytes;
+    unsigned int* tileCounter;       // {next tile, CTAs done}: zero at launch, reset by the
+                                     // last CTA to finish
     Status* status;                  // device copy
     volatile Status* statusHost;     // pinned mirror
 };
+// Tile-counter pairs a communicator rotates through, so that variable all-to-alls in
+// flight at the same time (on different streams) use different counters.
+constexpr int kTileCounterSlots = 64;
 
 // Staged ring kernels: one CTA per (channel, rank).
 struct RingArgs {
@@ -109,6 +115,8 @@ cudaError_t launch_allreduce_tree(const TreeArgs& a, vDataType_t dt, vRedOp_t op
 // into a CUDA graph carries its own copy.  table: items[0..nItems) (item i describes
 // all-reduce i), then at byte ptrByteOff the rank pointers: item i's 2*N pointers are
 // ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).
+// Largest grid the flat one-pass launches use; kernels stride over anything beyond.
+constexpr int kMaxGridCtas = 1 << 30;
 constexpr int kGroupTableBytes = 32 * 1024 - 256;
 struct GroupItem {
     unsigned long long unitStart;    // first flat work unit of this item

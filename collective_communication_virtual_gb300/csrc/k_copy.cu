@@ -9,11 +9,10 @@
 
 namespace vc {
 
-constexpr int kCopyUnroll = 8;             // vectors in flight per thread in a tile copy
-constexpr size_t kTileBytes = 64 * 1024;   // unit of work dealt to a CTA
-
-// The copy kernels deal 64 KiB tiles of a channel's block ranges to the channel's CTAs
-// round-robin: tile t covers elements [lo + k*T, lo + (k+1)*T) of block p = t / tilesPerBlock.
+// The copy kernels deal tiles (16, 32 or 64 KiB, 128 bytes per thread, chosen by the
+// planner) of a channel's block ranges to the channel's CTAs round-robin -- with the
+// default flat grid, one tile per CTA: tile t covers elements [lo + k*T, lo + (k+1)*T) of
+// block p = t / tilesPerBlock.
 // Consecutive CTAs take consecutive tiles of one block, so the grid streams through a
 // few blocks at a time, and the index arithmetic costs one division per tile.  Inside a
 // tile each thread issues all its loads (up to kCopyUnroll 16-byte vectors) before its
@@ -71,7 +70,7 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
     TileSpan t;
     t.lo = min((size_t)ch * a.chanElems, blockLen);
     t.hi = min((size_t)(ch + 1) * a.chanElems, blockLen);
-    t.tileElems = kTileBytes / ESZ;
+    t.tileElems = a.tileBytes / ESZ;
     t.tilesPerBlock = (t.hi - t.lo + t.tileElems - 1) / t.tileElems;
     return t;
 }
@@ -150,15 +149,19 @@ k_scatter_onepass(const __grid_constant__ OnePassArgs a) {
 }
 
 // Variable all-to-all.  The N*N blocks are cut into tiles of a.tileBytes; tiles are
-// numbered across all blocks and dealt to CTAs round-robin, so a hot destination's many
-// tiles spread over the whole grid.  Every CTA builds the tile prefix sums in shared
-// memory from the device tables.
+// numbered across all blocks (sender-major), so a hot destination's many tiles spread
+// over the whole grid.  The host cannot size the grid (the tables live on the device), so
+// one resident wave of CTAs takes tiles in order from an atomic counter: the tiles in
+// flight stay within a narrow window of the buffers, as with the flat grids of the other
+// copies.  The last CTA to finish resets the counter for the next launch.  Every CTA
+// builds the tile prefix sums in shared memory from the device tables.
 // Three copy widths are inlined here, so the kernel keeps 128 registers: one CTA per SM.
 template <int ESZ>
 __global__ void __launch_bounds__(kOnePassThreads, 1)
 k_alltoallv(const __grid_constant__ A2AvArgs a) {
     __shared__ unsigned long long tileStart[VCOMM_MAX_RANKS * VCOMM_MAX_RANKS + 1];
     __shared__ int sBad;
+    __shared__ unsigned int sTile;
     const int N = a.nRanks;
     const int NB = N * N;
     const size_t tileElems = a.tileBytes / ESZ;
@@ -181,8 +184,13 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
     __syncthreads();
     const unsigned long long nTiles = tileStart[NB];
     int p = 0;
-    for (unsigned long long tile = blockIdx.x; tile < nTiles; tile += gridDim.x) {
-        while (tileStart[p + 1] <= tile) p++;          // tiles ascend, so p only grows
+    for (;;) {
+        if (threadIdx.x == 0) sTile = atomicAdd(&a.tileCounter[0], 1u);
+        __syncthreads();
+        const unsigned long long tile = sTile;
+        __syncthreads();                               // all have read sTile
+        if (tile >= nTiles) break;
+        while (tileStart[p + 1] <= tile) p++;          // a CTA's tiles ascend, so p only grows
         const int i = p / N, j = p - (p / N) * N;
         const size_t cnt = (size_t)a.counts[p];
         const size_t k = tile - tileStart[p];
@@ -193,6 +201,11 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
         if (al == 0) tile_copy<ESZ, 32>(src, &dst, 0, 1, lo, hi);
         else if ((al & 15) == 0) tile_copy<ESZ, 16>(src, &dst, 0, 1, lo, hi);
         else tile_copy<ESZ, 0>(src, &dst, 0, 1, lo, hi);
+    }
+    // Every CTA has taken its last tile number; the last one out clears the counter.
+    if (threadIdx.x == 0 && atomicAdd(&a.tileCounter[1], 1u) == gridDim.x - 1) {
+        atomicExch(&a.tileCounter[0], 0u);
+        atomicExch(&a.tileCounter[1], 0u);
     }
 }
 

@@ -118,6 +118,10 @@ template <int DT, int OUT>
 __device__ __forceinline__ void store_epilogue_vec(void* outBase, size_t outElem, const V32& acc,
                                                    bool hasScale, float scale) {
     constexpr int VE = 16 / DTypeOf<DT>::size;
+    if (DT == OUT && !hasScale) {
+        st_stream32((char*)outBase + outElem * DTypeOf<DT>::size, acc);
+        return;
+    }
     store_epilogue_vec<DT, OUT>(outBase, outElem, acc.lo, hasScale, scale);
     store_epilogue_vec<DT, OUT>(outBase, outElem + VE, acc.hi, hasScale, scale);
 }
@@ -136,13 +140,14 @@ __device__ __forceinline__ void store_epilogue_elem(void* outBase, size_t outEle
 }
 
 // Reduce-scatter: block r = [r*rc, (r+1)*rc) of every send buffer lands in recv[r].
-// a.count = N * rc, a.blockElems = rc.  VB > 0 requires rc * esz % VB == 0.
-template <int DT, int OP, int OUT, int VB>
+// a.count = N * rc, a.blockElems = rc.  VB > 0 requires rc * esz % VB == 0.  NF > 0 fixes
+// the rank count at compile time (the loads and the fold unroll completely).
+template <int DT, int OP, int OUT, int VB, int NF = 0>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
-    const int N = a.nRanks;
+    const int N = NF ? NF : a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
     const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
@@ -159,7 +164,7 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
         const size_t base = (size_t)r * rc;
         const int first = r + 1 == N ? 0 : r + 1;
         if (VB && t + U <= chEnd) {
-            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(a.send, N, first, (base + t) * ESZ);
+            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16, NF>(a.send, N, first, (base + t) * ESZ);
             store_epilogue_vec<DT, OUT>(a.recv[r], t, acc, hasScale, a.scale);
         } else {
             for (size_t x = t; x < min(t + U, chEnd); x++) {
@@ -209,7 +214,9 @@ cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedO
 template <int DT, int OP, int OUT>
 static cudaError_t rs_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
                                    cudaStream_t s) {
-    if (vb == 32) k_reduce_scatter_onepass<DT, OP, OUT, 32><<<grid, threads, 0, s>>>(a);
+    if (a.nRanks == 8 && vb == 32) k_reduce_scatter_onepass<DT, OP, OUT, 32, 8><<<grid, threads, 0, s>>>(a);
+    else if (a.nRanks == 8 && vb == 16) k_reduce_scatter_onepass<DT, OP, OUT, 16, 8><<<grid, threads, 0, s>>>(a);
+    else if (vb == 32) k_reduce_scatter_onepass<DT, OP, OUT, 32><<<grid, threads, 0, s>>>(a);
     else if (vb == 16) k_reduce_scatter_onepass<DT, OP, OUT, 16><<<grid, threads, 0, s>>>(a);
     else k_reduce_scatter_onepass<DT, OP, OUT, 0><<<grid, threads, 0, s>>>(a);
     return cudaGetLastError();

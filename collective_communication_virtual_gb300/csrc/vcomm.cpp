@@ -28,7 +28,8 @@ struct Config {
     size_t chunkBytes = 0;           // 0: planner default
     int timeoutMs = 2000;
     bool debug = false;
-    bool bulkCopy = true;            // TMA bulk copies for the fan-out copies
+    bool bulkCopy = false;           // TMA bulk copies for the fan-out copies (opt-in)
+    bool persistentGrid = false;     // one-pass grids of one resident wave (A/B switch)
 };
 
 // One call recorded between vcommGroupStart and vcommGroupEnd.
@@ -77,6 +78,8 @@ struct vcomm {
     int groupDepth;
     std::vector<GroupRec>* group;
     vc::GroupArgs* groupArgs;        // host copy of a batch's parameter block
+    unsigned int* tileCounters;      // variable all-to-all tile counters (device)
+    unsigned int tileCounterSeq;
     unsigned long long endMagic;
 };
 
@@ -136,7 +139,8 @@ void read_env(Config* cfg) {
         if (v >= 1 && v <= 3600 * 1000) cfg->timeoutMs = (int)v;
     }
     if (const char* s = std::getenv("VCOMM_DEBUG")) cfg->debug = !std::strcmp(s, "INFO");
-    if (const char* s = std::getenv("VCOMM_COPY_TMA")) cfg->bulkCopy = std::strcmp(s, "0") != 0;
+    if (const char* s = std::getenv("VCOMM_COPY_TMA")) cfg->bulkCopy = !std::strcmp(s, "1");
+    if (const char* s = std::getenv("VCOMM_GRID")) cfg->persistentGrid = !std::strcmp(s, "persistent");
 }
 
 void free_comm(vcomm* c) {
@@ -147,6 +151,7 @@ void free_comm(vcomm* c) {
     if (c->ctrl) cudaFree(c->ctrl);
     if (c->statusDev) cudaFree(c->statusDev);
     if (c->abortDev) cudaFree(c->abortDev);
+    if (c->tileCounters) cudaFree(c->tileCounters);
     if (c->statusHost) cudaFreeHost(c->statusHost);
     if (c->abortHost) cudaFreeHost(c->abortHost);
     c->startMagic = c->endMagic = 0;
@@ -205,6 +210,7 @@ vResult_t make_plan(const vcomm* c, int coll, size_t count, int dt, int aligned,
     q.aligned16 = aligned >= 16 ? 1 : 0;
     q.aligned32 = aligned >= 32 ? 1 : 0;
     q.noBulkCopy = c->cfg.bulkCopy ? 0 : 1;
+    q.persistentGrid = c->cfg.persistentGrid ? 1 : 0;
     q.smCount = c->smCount;
     q.l2Bytes = c->l2Bytes;
     return vPlanCompute(&q, p);
@@ -245,6 +251,7 @@ void fill_onepass(vc::OnePassArgs* a, const vcomm* c, const void* const* send, v
     a->count = count;
     a->blockElems = p.blockElems;
     a->chanElems = p.channelElems;
+    a->tileBytes = p.tileBytes ? p.tileBytes : (size_t)64 * 1024;
 }
 
 // Grow the ring FIFOs and control words if this plan needs more than the communicator has.
@@ -389,9 +396,12 @@ vResult_t launch_group_batch(vcomm* c, const std::vector<const GroupRec*>& items
     a.totalUnits = units;
     a.ptrByteOff = (int)itemBytes;
     a.pad = 0;
-    const int perSm = r0.vecBytes == 32 ? 1 : 2;
+    // One thread per work unit, CTAs dispatched in order (or one resident wave striding
+    // over the units when the persistent grid is asked for).
     const unsigned long long need = (units + vc::kOnePassThreads - 1) / vc::kOnePassThreads;
-    const int grid = (int)std::min<unsigned long long>((unsigned long long)perSm * c->smCount, std::max(1ull, need));
+    const unsigned long long cap =
+        c->cfg.persistentGrid ? (unsigned long long)(r0.vecBytes == 32 ? 1 : 2) * c->smCount : vc::kMaxGridCtas;
+    const int grid = (int)std::min<unsigned long long>(cap, std::max(1ull, need));
     const cudaError_t e = vc::launch_allreduce_group(a, r0.dt, r0.op, r0.vecBytes, grid, vc::kOnePassThreads,
                                                      r0.stream);
     return finish_launch(c, e, r0.stream, "group launch");
@@ -496,6 +506,10 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
     if ((e = cudaMemset(c->statusDev, 0, sizeof(vc::Status))) != cudaSuccess) goto fail;
     if ((e = cudaMalloc(&c->abortDev, sizeof(unsigned int))) != cudaSuccess) goto fail;
     if ((e = cudaMemset(c->abortDev, 0, sizeof(unsigned int))) != cudaSuccess) goto fail;
+    if ((e = cudaMalloc(&c->tileCounters, vc::kTileCounterSlots * 2 * sizeof(unsigned int))) != cudaSuccess)
+        goto fail;
+    if ((e = cudaMemset(c->tileCounters, 0, vc::kTileCounterSlots * 2 * sizeof(unsigned int))) != cudaSuccess)
+        goto fail;
     if ((e = cudaHostAlloc(&c->statusHost, sizeof(vc::Status), cudaHostAllocMapped)) != cudaSuccess) goto fail;
     std::memset(c->statusHost, 0, sizeof(vc::Status));
     if ((e = cudaHostGetDevicePointer(&c->statusHostDev, c->statusHost, 0)) != cudaSuccess) goto fail;
@@ -943,6 +957,7 @@ vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* 
     a.nRanks = c->nRanks;
     a.elemSize = (int)esz;
     a.tileBytes = 64 * 1024;
+    a.tileCounter = c->tileCounters + 2 * (size_t)(c->tileCounterSeq++ % vc::kTileCounterSlots);
     a.status = c->statusDev;
     a.statusHost = c->statusHostDev;
     return finish_launch(c, vc::launch_alltoallv(a, p.gridCtas, p.threadsPerCta, stream), stream, "alltoallv");

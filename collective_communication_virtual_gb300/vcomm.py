@@ -45,7 +45,7 @@ class vPlanRequest_t(ctypes.Structure):
                 ("algo", ctypes.c_int), ("coll", ctypes.c_int), ("datatype", ctypes.c_int),
                 ("count", ctypes.c_size_t), ("chunkBytes", ctypes.c_size_t),
                 ("aligned16", ctypes.c_int), ("smCount", ctypes.c_int), ("l2Bytes", ctypes.c_size_t),
-                ("aligned32", ctypes.c_int), ("noBulkCopy", ctypes.c_int)]
+                ("aligned32", ctypes.c_int), ("noBulkCopy", ctypes.c_int), ("persistentGrid", ctypes.c_int)]
 
 
 class vPlanInfo_t(ctypes.Structure):
@@ -57,7 +57,7 @@ class vPlanInfo_t(ctypes.Structure):
                 ("slotPayloadElems", ctypes.c_size_t), ("slotBytes", ctypes.c_size_t),
                 ("fifoBytes", ctypes.c_size_t), ("minBytes", ctypes.c_double),
                 ("busFactor", ctypes.c_double), ("vecBytes", ctypes.c_int), ("bulkCopy", ctypes.c_int),
-                ("predictedUs", ctypes.c_double)]
+                ("predictedUs", ctypes.c_double), ("tileBytes", ctypes.c_size_t)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

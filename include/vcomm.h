@@ -28,7 +28,9 @@
  * call on that communicator returns that error without launching, and the
  * communicator must be destroyed.
  *
- * Threading: a communicator is used by one host thread at a time.
+ * Threading: a communicator is used by one host thread at a time.  Staged ring transfers
+ * on one communicator share its FIFOs, so they must not overlap on the GPU: issue them on
+ * one stream or order the streams (NCCL orders a communicator's operations the same way).
  *
  * CUDA graphs: collectives may be captured into a graph.  A ring transfer can be
  * captured only after an eager ring call of at least the same size on the same
@@ -121,9 +123,11 @@ typedef enum {
  * vUnhandledCudaError.  The communicator owns a small status block in pinned host
  * memory and, once a ring transfer is planned, its staging FIFOs in device memory.
  * Environment (read once here): VCOMM_ALGO=auto|onepass|ring|tree, VCOMM_CHUNK_BYTES,
- * VCOMM_TIMEOUT_MS, VCOMM_COPY_TMA=0|1 (1, the default: all-gather, gather and broadcast
- * stage tiles in shared memory with TMA bulk copies when blocks are 16-byte aligned; 0:
- * every thread loads and stores), VCOMM_DEBUG=INFO (prints every plan to stderr). */
+ * VCOMM_TIMEOUT_MS, VCOMM_COPY_TMA=0|1 (0, the default: every thread loads and stores; 1:
+ * all-gather, gather and broadcast stage tiles in shared memory with TMA bulk copies when
+ * blocks are 16-byte aligned), VCOMM_GRID=flat|persistent (flat, the default: the
+ * one-pass kernels launch one CTA per slice of work; persistent: about one resident wave
+ * of CTAs striding over it), VCOMM_DEBUG=INFO (prints every plan to stderr). */
 vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol);
 
 /* Wait for the communicator's last enqueued work, then free everything it owns.
@@ -286,7 +290,11 @@ typedef struct {
     int smCount;               /* streaming multiprocessors of the device */
     size_t l2Bytes;            /* L2 cache size of the device */
     int aligned32;             /* 1 if every buffer pointer is 32-byte aligned */
-    int noBulkCopy;            /* 1: never use TMA bulk copies (VCOMM_COPY_TMA=0) */
+    int noBulkCopy;            /* 1: never use TMA bulk copies (a communicator sets it unless
+                                  VCOMM_COPY_TMA=1) */
+    int persistentGrid;        /* 1: one-pass grids of about one resident wave whose CTAs
+                                  stride over their work (VCOMM_GRID=persistent); 0 (the
+                                  default): one CTA per slice of work, dispatched in order */
 } vPlanRequest_t;
 
 typedef struct {
@@ -309,6 +317,7 @@ typedef struct {
     int vecBytes;              /* bytes per vector access of the one-pass kernels: 0, 16, 32 */
     int bulkCopy;              /* 1: all-gather / gather / broadcast through TMA bulk copies */
     double predictedUs;        /* the planner's cost model for this plan (GB300 fit) */
+    size_t tileBytes;          /* copies (load/store path): bytes each CTA moves per tile */
 } vPlanInfo_t;
 
 /* Compute the plan a collective with these parameters would run.  Pure host

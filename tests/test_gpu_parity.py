@@ -501,6 +501,49 @@ def test_alltoallv_rank_with_nothing_to_send_or_receive():
         V.vcommDestroy(c)
 
 
+def test_alltoallv_tile_counter_resets_across_launches_and_graph_replays():
+    # The variable all-to-all hands tiles out from a per-launch counter that its last CTA
+    # clears; many launches in a row (more than the rotating counter slots) and replays of
+    # a captured launch must each copy every tile exactly once.
+    n = 8
+    g = torch.Generator().manual_seed(31)
+    counts = torch.randint(0, 70_000, (n, n), generator=g, dtype=torch.int32)
+    sd = (torch.cumsum(counts, 1) - counts).to(torch.int32)
+    rd = (torch.cumsum(counts, 0) - counts).t().contiguous().to(torch.int32)
+    recv_elems = [int(v) for v in counts.sum(0)]
+    tabs = [t.to(DEV) for t in (counts, sd, rd)]
+    send = [torch.empty(int(counts[i].sum()), device=DEV) for i in range(n)]
+    recv = [torch.empty(e, device=DEV) for e in recv_elems]
+    c = V.vcommInit(n, 1, V.vProtoSimple)
+    try:
+        def fill(k):
+            xs = [inputs.uniform_ranks(1, int(counts[i].sum()), torch.float32, 1000 * k + i)[0] for i in range(n)]
+            for d, x in zip(send, xs):
+                d.copy_(x)
+            return xs
+        for k in range(140):
+            xs = fill(k) if k % 35 == 0 else None
+            for t in recv:
+                t.fill_(-7.0)
+            V.vAllToAllv(send, recv, *tabs, torch.float32, c)
+            if xs is not None:
+                torch.cuda.synchronize()
+                assert_bits_equal(recv, oracle.alltoallv(xs, counts, sd, rd, recv_elems), f"launch {k}")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            V.vAllToAllv(send, recv, *tabs, torch.float32, c)
+        for k in range(3):
+            xs = fill(500 + k)
+            for t in recv:
+                t.fill_(-7.0)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert_bits_equal(recv, oracle.alltoallv(xs, counts, sd, rd, recv_elems), f"replay {k}")
+        assert V.vcommGetAsyncError(c) == V.vSuccess
+    finally:
+        V.vcommDestroy(c)
+
+
 def test_alltoallv_positive_count_into_null_buffer_sets_async_error():
     n = 2
     c = V.vcommInit(n, 1, V.vProtoSimple)

@@ -163,14 +163,18 @@ def test_traffic_and_bus_factor():
 def test_32_byte_vectors_when_blocks_and_pointers_allow():
     # B = 2M fp32 elements (8 MiB): a multiple of 32 bytes
     p = plan(count=16 << 20, aligned32=1)
-    assert p.vecBytes == 32 and p.gridCtas == 152          # one 512-thread CTA per SM
+    # flat grid: one 512-thread CTA per 512 vectors of every rank (2M / 8 / 512 = 512 per
+    # block, 8 blocks); the persistent grid is one 512-thread CTA per SM
+    assert p.vecBytes == 32 and p.gridCtas == 4096
+    assert plan(count=16 << 20, aligned32=1, persistentGrid=1).gridCtas == 152
     assert plan(count=16 << 20, aligned32=0).vecBytes == 16
     # B = alignUp(513, 4) = 516 elements = 2064 bytes: 16-byte blocks only
     assert plan(count=4099, aligned32=1).vecBytes == 16
     assert plan(count=4099, aligned16=0, aligned32=0).vecBytes == 0
     assert plan(coll=V.vCollReduceScatter, count=4096, aligned32=1).vecBytes == 32
     assert plan(coll=V.vCollAllGather, count=4096, aligned32=1).vecBytes == 32
-    assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1).gridCtas == 2 * 152
+    assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1).gridCtas == 8 * 1024  # 64 KiB tiles
+    assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1, persistentGrid=1).gridCtas == 2 * 152
 
 
 def test_fanout_copies_use_tma_bulk_copies_when_blocks_allow():
@@ -189,14 +193,22 @@ def test_fanout_copies_use_tma_bulk_copies_when_blocks_allow():
         assert (p.channelElems * 4) % 32 == 0
 
 
-def test_grid_is_about_two_ctas_per_sm_and_never_idle():
+def test_flat_grid_covers_the_work_once_and_persistent_grid_is_one_wave():
+    # flat (default): one 512-thread CTA per 512 units (a 16-byte vector of every rank)
     p = plan(count=16 << 20, nChannels=1)
-    assert p.gridCtas == 2 * 152
+    assert p.vecBytes == 16 and p.gridCtas == (16 << 20) // 4 // 512
     p = plan(count=16 << 20, nChannels=32)
     assert p.nChannels * p.ctasPerChannel == p.gridCtas
-    assert 2 * 152 - 32 < p.gridCtas <= 2 * 152                    # one wave, nearly full
-    p = plan(count=256)                                  # 1 KiB per rank: one CTA is enough
-    assert p.gridCtas == 1
+    assert p.ctasPerChannel * 512 * 4 >= (16 << 20) // 32              # every unit has a thread
+    assert (p.ctasPerChannel - 1) * 512 * 4 < (16 << 20) // 32         # and no CTA is idle
+    # persistent: about two resident 512-thread CTAs per SM, one wave, nearly full
+    p = plan(count=16 << 20, nChannels=1, persistentGrid=1)
+    assert p.gridCtas == 2 * 152
+    p = plan(count=16 << 20, nChannels=32, persistentGrid=1)
+    assert p.nChannels * p.ctasPerChannel == p.gridCtas
+    assert 2 * 152 - 32 < p.gridCtas <= 2 * 152
+    for persistent in (0, 1):
+        assert plan(count=256, persistentGrid=persistent).gridCtas == 1   # 1 KiB per rank
 
 
 def test_bad_requests():
@@ -225,9 +237,14 @@ def test_tree_plan():
     assert p.algo == V.vAlgoTree and p.blockElems == 8 << 20
     # grid = one wave of resident CTAs: one per SM for the register-held 8-rank 32-byte
     # kernel, two per SM otherwise
+    # flat (default): one 512-thread CTA per 512 vectors of every rank
     wide = plan(algo=V.vAlgoTree, count=16 << 20, aligned32=1)
+    assert wide.vecBytes == 32 and wide.gridCtas == (16 << 20) // 8 // 512
+    assert p.vecBytes == 16 and p.gridCtas == (16 << 20) // 4 // 512
+    # persistent: one wave of resident CTAs
+    wide = plan(algo=V.vAlgoTree, count=16 << 20, aligned32=1, persistentGrid=1)
     assert wide.vecBytes == 32 and wide.gridCtas == 152
-    assert plan(algo=V.vAlgoTree, count=16 << 20, nRanks=4, aligned32=1).gridCtas == 304
-    assert p.vecBytes == 16 and p.gridCtas == 304
+    assert plan(algo=V.vAlgoTree, count=16 << 20, nRanks=4, aligned32=1, persistentGrid=1).gridCtas == 304
+    assert plan(algo=V.vAlgoTree, count=16 << 20, persistentGrid=1).gridCtas == 304
     assert plan(algo=V.vAlgoTree, count=16 << 20, coll=V.vCollReduceScatter).algo == V.vAlgoOnePass
     assert plan(algo=V.vAlgoTree, count=100, nRanks=1).algo == V.vAlgoOnePass

@@ -60,7 +60,7 @@ const RingFit kRingFit[3] = {
     {{50.8, 51.4, 56.0}, {6184.0, 42541.0, 103539.0}},       // LL128
 };
 const double kOnePassLatUs = 2.1;
-const double kOnePassBytesPerUs = 6.37e6;                    // minimum bytes / (time - latency)
+const double kOnePassBytesPerUs = 7.05e6;                    // minimum bytes / (time - latency)
 
 double interp_ch(const double v[3], int ch) {
     const double x = ch <= 1 ? 0.0 : (ch >= 32 ? 5.0 : std::log2((double)ch));
@@ -172,8 +172,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         // The 8-rank 32-byte kernel keeps its vectors in registers (one CTA per SM); the
         // others fit two per SM.
         const size_t resident = (size_t)((N == 8 && p->vecBytes == 32) ? 1 : 2) * smCount;
-        const size_t cap = q->persistentGrid ? resident : (size_t)vc::kMaxGridCtas;
-        p->ctasPerChannel = (int)std::max<size_t>(1, std::min<size_t>(cap, div_up(work, vc::kOnePassThreads)));
+        const size_t need = div_up(work, vc::kOnePassThreads);
+        const size_t cap = (q->persistentGrid || need < 2 * resident) ? resident : (size_t)vc::kMaxGridCtas;
+        p->ctasPerChannel = (int)std::max<size_t>(1, std::min<size_t>(cap, need));
         p->gridCtas = p->ctasPerChannel;
         p->predictedUs = tOne;
         p->launches = 1;
@@ -224,7 +225,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
             }
         }
         maxPer = std::max<size_t>(1, maxPer);
-        if (q->persistentGrid || q->coll == vCollAllToAllv)
+        // Work of under two waves runs as one wave (a partly filled second wave costs
+        // more than the drift of CTAs that stride at most twice).
+        if (q->persistentGrid || q->coll == vCollAllToAllv || maxPer < 2 * (size_t)per)
             per = (int)std::min<size_t>((size_t)per, maxPer);
         else
             per = (int)std::min<size_t>((size_t)vc::kMaxGridCtas / (size_t)q->nChannels, maxPer);

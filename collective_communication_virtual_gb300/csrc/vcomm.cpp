@@ -396,11 +396,11 @@ vResult_t launch_group_batch(vcomm* c, const std::vector<const GroupRec*>& items
     a.totalUnits = units;
     a.ptrByteOff = (int)itemBytes;
     a.pad = 0;
-    // One thread per work unit, CTAs dispatched in order (or one resident wave striding
-    // over the units when the persistent grid is asked for).
+    // One thread per work unit, CTAs dispatched in order; one resident wave striding over
+    // the units when the persistent grid is asked for or the work is under two waves.
     const unsigned long long need = (units + vc::kOnePassThreads - 1) / vc::kOnePassThreads;
-    const unsigned long long cap =
-        c->cfg.persistentGrid ? (unsigned long long)(r0.vecBytes == 32 ? 1 : 2) * c->smCount : vc::kMaxGridCtas;
+    const unsigned long long resident = (unsigned long long)(r0.vecBytes == 32 ? 1 : 2) * c->smCount;
+    const unsigned long long cap = (c->cfg.persistentGrid || need < 2 * resident) ? resident : vc::kMaxGridCtas;
     const int grid = (int)std::min<unsigned long long>(cap, std::max(1ull, need));
     const cudaError_t e = vc::launch_allreduce_group(a, r0.dt, r0.op, r0.vecBytes, grid, vc::kOnePassThreads,
                                                      r0.stream);

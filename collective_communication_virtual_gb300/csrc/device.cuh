@@ -19,6 +19,33 @@
 
 namespace vc {
 
+// Programmatic dependent launch (Hopper and Blackwell).  A one-pass kernel first allows
+// the next kernel on the stream to be scheduled, so that kernel's CTAs become resident
+// while this one's last CTAs finish, then waits until the previous kernel has completed
+// and its memory is visible before it touches global memory.  Both instructions do
+// nothing for a launch without the attribute, so the ordering of a stream is kept.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch a one-pass kernel, with programmatic stream serialization when enabled.
+template <typename... KArgs, typename... Args>
+inline cudaError_t pdl_launch(void (*kernel)(KArgs...), unsigned grid, unsigned threads, size_t smem,
+                              cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 enum { kSum = 0, kProd = 1, kMin = 2, kMax = 3 };
 enum { kF32 = 0, kF16 = 1, kBF16 = 2, kI32 = 3 };
 

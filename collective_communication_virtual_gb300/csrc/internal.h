@@ -115,6 +115,10 @@ cudaError_t launch_allreduce_tree(const TreeArgs& a, vDataType_t dt, vRedOp_t op
 // into a CUDA graph carries its own copy.  table: items[0..nItems) (item i describes
 // all-reduce i), then at byte ptrByteOff the rank pointers: item i's 2*N pointers are
 // ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).
+// Programmatic dependent launch of the one-pass kernels (on unless VCOMM_PDL=0; read when
+// a communicator is created).
+bool& pdl_enabled();
+
 // Largest grid the flat one-pass launches use; kernels stride over anything beyond.
 constexpr int kMaxGridCtas = 1 << 30;
 constexpr int kGroupTableBytes = 32 * 1024 - 256;

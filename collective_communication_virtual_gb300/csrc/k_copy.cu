@@ -80,6 +80,7 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
 template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, 2)
 k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
@@ -100,6 +101,7 @@ k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
 template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, 2)
 k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
     const TileSpan sp = tile_span<ESZ>(a, ch, a.count);
@@ -113,6 +115,7 @@ k_broadcast_onepass(const __grid_constant__ OnePassArgs a) {
 template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, 2)
 k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
@@ -133,6 +136,7 @@ k_alltoall_onepass(const __grid_constant__ OnePassArgs a) {
 template <int ESZ, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, 2)
 k_scatter_onepass(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
     const int N = a.nRanks;
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
@@ -159,6 +163,7 @@ k_scatter_onepass(const __grid_constant__ OnePassArgs a) {
 template <int ESZ>
 __global__ void __launch_bounds__(kOnePassThreads, 1)
 k_alltoallv(const __grid_constant__ A2AvArgs a) {
+    pdl_begin();
     __shared__ unsigned long long tileStart[VCOMM_MAX_RANKS * VCOMM_MAX_RANKS + 1];
     __shared__ int sBad;
     __shared__ unsigned int sTile;
@@ -213,9 +218,9 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
 
 #define VC_COPY_LAUNCH_ESZ(KERNEL, E)                                                      \
     do {                                                                                   \
-        if (vb == 32) KERNEL<E, 32><<<grid, threads, 0, s>>>(a);                           \
-        else if (vb == 16) KERNEL<E, 16><<<grid, threads, 0, s>>>(a);                      \
-        else KERNEL<E, 0><<<grid, threads, 0, s>>>(a);                                     \
+        if (vb == 32) (void)pdl_launch(KERNEL<E, 32>, grid, threads, 0, s, a);                           \
+        else if (vb == 16) (void)pdl_launch(KERNEL<E, 16>, grid, threads, 0, s, a);                      \
+        else (void)pdl_launch(KERNEL<E, 0>, grid, threads, 0, s, a);                                     \
     } while (0)
 
 #define VC_COPY_LAUNCH(KERNEL)                                                             \
@@ -247,8 +252,8 @@ cudaError_t launch_scatter_onepass(const OnePassArgs& a, int elemSize, int vb, i
 }
 
 cudaError_t launch_alltoallv(const A2AvArgs& a, int grid, int threads, cudaStream_t s) {
-    if (a.elemSize == 4) k_alltoallv<4><<<grid, threads, 0, s>>>(a);
-    else if (a.elemSize == 2) k_alltoallv<2><<<grid, threads, 0, s>>>(a);
+    if (a.elemSize == 4) (void)pdl_launch(k_alltoallv<4>, grid, threads, 0, s, a);
+    else if (a.elemSize == 2) (void)pdl_launch(k_alltoallv<2>, grid, threads, 0, s, a);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

@@ -13,6 +13,7 @@ namespace vc {
 template <int DT, int OP, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_group(const __grid_constant__ GroupArgs a) {
+    pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
     const GroupItem* items = reinterpret_cast<const GroupItem*>(a.table);
@@ -53,9 +54,9 @@ k_allreduce_group(const __grid_constant__ GroupArgs a) {
 
 template <int DT, int OP>
 static cudaError_t group_dispatch_vec(const GroupArgs& a, int vb, int grid, int threads, cudaStream_t s) {
-    if (vb == 32) k_allreduce_group<DT, OP, 32><<<grid, threads, 0, s>>>(a);
-    else if (vb == 16) k_allreduce_group<DT, OP, 16><<<grid, threads, 0, s>>>(a);
-    else k_allreduce_group<DT, OP, 0><<<grid, threads, 0, s>>>(a);
+    if (vb == 32) (void)pdl_launch(k_allreduce_group<DT, OP, 32>, grid, threads, 0, s, a);
+    else if (vb == 16) (void)pdl_launch(k_allreduce_group<DT, OP, 16>, grid, threads, 0, s, a);
+    else (void)pdl_launch(k_allreduce_group<DT, OP, 0>, grid, threads, 0, s, a);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@ __device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch
 template <int DT, int OP, int VB, int NF = 0>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
     const int N = NF ? NF : a.nRanks;
@@ -145,6 +146,7 @@ __device__ __forceinline__ void store_epilogue_elem(void* outBase, size_t outEle
 template <int DT, int OP, int OUT, int VB, int NF = 0>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
     const int N = NF ? NF : a.nRanks;
@@ -180,11 +182,13 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
 template <int DT, int OP>
 static cudaError_t ar_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
                                    cudaStream_t s) {
-    if (a.nRanks == 8 && vb == 32) k_allreduce_onepass<DT, OP, 32, 8><<<grid, threads, 0, s>>>(a);
-    else if (a.nRanks == 8 && vb == 16) k_allreduce_onepass<DT, OP, 16, 8><<<grid, threads, 0, s>>>(a);
-    else if (vb == 32) k_allreduce_onepass<DT, OP, 32><<<grid, threads, 0, s>>>(a);
-    else if (vb == 16) k_allreduce_onepass<DT, OP, 16><<<grid, threads, 0, s>>>(a);
-    else k_allreduce_onepass<DT, OP, 0><<<grid, threads, 0, s>>>(a);
+    if (a.nRanks == 8 && vb == 32) (void)pdl_launch(k_allreduce_onepass<DT, OP, 32, 8>,
+            grid, threads, 0, s, a);
+    else if (a.nRanks == 8 && vb == 16) (void)pdl_launch(k_allreduce_onepass<DT, OP, 16, 8>,
+            grid, threads, 0, s, a);
+    else if (vb == 32) (void)pdl_launch(k_allreduce_onepass<DT, OP, 32>, grid, threads, 0, s, a);
+    else if (vb == 16) (void)pdl_launch(k_allreduce_onepass<DT, OP, 16>, grid, threads, 0, s, a);
+    else (void)pdl_launch(k_allreduce_onepass<DT, OP, 0>, grid, threads, 0, s, a);
     return cudaGetLastError();
 }
 
@@ -214,11 +218,13 @@ cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedO
 template <int DT, int OP, int OUT>
 static cudaError_t rs_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
                                    cudaStream_t s) {
-    if (a.nRanks == 8 && vb == 32) k_reduce_scatter_onepass<DT, OP, OUT, 32, 8><<<grid, threads, 0, s>>>(a);
-    else if (a.nRanks == 8 && vb == 16) k_reduce_scatter_onepass<DT, OP, OUT, 16, 8><<<grid, threads, 0, s>>>(a);
-    else if (vb == 32) k_reduce_scatter_onepass<DT, OP, OUT, 32><<<grid, threads, 0, s>>>(a);
-    else if (vb == 16) k_reduce_scatter_onepass<DT, OP, OUT, 16><<<grid, threads, 0, s>>>(a);
-    else k_reduce_scatter_onepass<DT, OP, OUT, 0><<<grid, threads, 0, s>>>(a);
+    if (a.nRanks == 8 && vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32, 8>,
+            grid, threads, 0, s, a);
+    else if (a.nRanks == 8 && vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16, 8>,
+            grid, threads, 0, s, a);
+    else if (vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32>, grid, threads, 0, s, a);
+    else if (vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16>, grid, threads, 0, s, a);
+    else (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0>, grid, threads, 0, s, a);
     return cudaGetLastError();
 }
 

@@ -155,6 +155,7 @@ __device__ void tma_fanout(const TmaJob& j, Status* st, volatile Status* stHost)
 // land at recv[r] + s * sc.  Broadcast: one block send[root] to every recv[r].
 __global__ void __launch_bounds__(32) k_fanout_tma(const __grid_constant__ OnePassArgs a, int esz, int isBroadcast,
                                                   Status* st, Status* stHost) {
+    pdl_begin();
     TmaJob j;
     const char* const* sends = (const char* const*)a.send;
     j.dst = a.outRoot >= 0 ? (char* const*)&a.recv[a.outRoot] : (char* const*)a.recv;
@@ -182,8 +183,8 @@ cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast
         if (e != cudaSuccess) return e;
         attrSet = true;
     }
-    k_fanout_tma<<<grid, 32, kTmaSmemBytes, s>>>(a, elemSize, broadcast ? 1 : 0, st, (Status*)stHost);
-    return cudaGetLastError();
+    return pdl_launch(k_fanout_tma, grid, 32, kTmaSmemBytes, s, a, elemSize, broadcast ? 1 : 0, st,
+                      (Status*)stHost);
 }
 
 }  // namespace vc

@@ -14,6 +14,7 @@ namespace vc {
 template <int DT, int OP, int VB>
 __global__ void __launch_bounds__(kOnePassThreads, 2)
 k_allreduce_tree(const __grid_constant__ TreeArgs a) {
+    pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
     using VT = typename VecOf<VB ? VB : 16>::T;
@@ -167,6 +168,7 @@ __device__ __forceinline__ typename VecOf<VT_BYTES>::T eval_tree_fixed(const typ
 template <int DT, int OP, int VB, int N>
 __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_tree_fixed(const __grid_constant__ TreeArgs a) {
+    pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB / ESZ;
     using VT = typename VecOf<VB>::T;
@@ -203,11 +205,13 @@ k_allreduce_tree_fixed(const __grid_constant__ TreeArgs a) {
 
 template <int DT, int OP>
 static cudaError_t tree_dispatch_vec(const TreeArgs& a, int vb, int grid, int threads, cudaStream_t s) {
-    if (a.nRanks == 8 && vb == 32) k_allreduce_tree_fixed<DT, OP, 32, 8><<<grid, threads, 0, s>>>(a);
-    else if (a.nRanks == 8 && vb == 16) k_allreduce_tree_fixed<DT, OP, 16, 8><<<grid, threads, 0, s>>>(a);
-    else if (vb == 32) k_allreduce_tree<DT, OP, 32><<<grid, threads, 0, s>>>(a);
-    else if (vb == 16) k_allreduce_tree<DT, OP, 16><<<grid, threads, 0, s>>>(a);
-    else k_allreduce_tree<DT, OP, 0><<<grid, threads, 0, s>>>(a);
+    if (a.nRanks == 8 && vb == 32) (void)pdl_launch(k_allreduce_tree_fixed<DT, OP, 32, 8>,
+            grid, threads, 0, s, a);
+    else if (a.nRanks == 8 && vb == 16) (void)pdl_launch(k_allreduce_tree_fixed<DT, OP, 16, 8>,
+            grid, threads, 0, s, a);
+    else if (vb == 32) (void)pdl_launch(k_allreduce_tree<DT, OP, 32>, grid, threads, 0, s, a);
+    else if (vb == 16) (void)pdl_launch(k_allreduce_tree<DT, OP, 16>, grid, threads, 0, s, a);
+    else (void)pdl_launch(k_allreduce_tree<DT, OP, 0>, grid, threads, 0, s, a);
     return cudaGetLastError();
 }
 

@@ -19,6 +19,13 @@
 
 #include <algorithm>
 
+namespace vc {
+bool& pdl_enabled() {
+    static bool on = true;
+    return on;
+}
+}  // namespace vc
+
 namespace {
 
 constexpr unsigned long long kMagic = 0x76636F6D6D763031ull;   // "vcommv01"
@@ -141,6 +148,8 @@ void read_env(Config* cfg) {
     if (const char* s = std::getenv("VCOMM_DEBUG")) cfg->debug = !std::strcmp(s, "INFO");
     if (const char* s = std::getenv("VCOMM_COPY_TMA")) cfg->bulkCopy = !std::strcmp(s, "1");
     if (const char* s = std::getenv("VCOMM_GRID")) cfg->persistentGrid = !std::strcmp(s, "persistent");
+    const char* pdl = std::getenv("VCOMM_PDL");
+    vc::pdl_enabled() = !pdl || std::strcmp(pdl, "0") != 0;
 }
 
 void free_comm(vcomm* c) {
@@ -225,14 +234,18 @@ bool stream_capturing(cudaStream_t stream) {
     return cs != cudaStreamCaptureStatusNone;
 }
 
-vResult_t finish_launch(vcomm* c, cudaError_t e, cudaStream_t stream, const char* what) {
+// usesComm: the kernel touches communicator memory (FIFOs, counters, the status word), so
+// vcommDestroy must wait for it.  Launches that touch only the caller's buffers are not
+// tracked: an event recorded between two kernels would also stop the second from being
+// scheduled during the first one's tail (programmatic dependent launch).
+vResult_t finish_launch(vcomm* c, cudaError_t e, cudaStream_t stream, const char* what, bool usesComm = false) {
     if (e != cudaSuccess) {
         c->hostError = vUnhandledCudaError;
         return cuda_fail(c, e, what);
     }
     // Track the last eager launch for vcommDestroy; launches being captured into a graph
     // run when the graph does, which the caller orders.
-    if (!stream_capturing(stream) && cudaEventRecord(c->lastEvent, stream) == cudaSuccess)
+    if (usesComm && !stream_capturing(stream) && cudaEventRecord(c->lastEvent, stream) == cudaSuccess)
         c->eventRecorded = true;
     return vSuccess;
 }
@@ -355,7 +368,7 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
         cudaGetLastError();
         return vInvalidUsage;
     }
-    return finish_launch(c, e, stream, "ring launch");
+    return finish_launch(c, e, stream, "ring launch", true);
 }
 
 // One launch for up to vc::group_capacity(N) recorded all-reduces of one type, op, stream
@@ -780,7 +793,7 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
     fill_onepass(&a, c, send, recv, p, sendcount);
     if (p.bulkCopy)
         return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, c->statusDev,
-                                                      c->statusHostDev, stream), stream, "allgather");
+                                                      c->statusHostDev, stream), stream, "allgather", true);
     return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "allgather");
 }
@@ -813,7 +826,7 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
     a.root = root;
     if (p.bulkCopy)
         return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), true, p.gridCtas, c->statusDev,
-                                                      c->statusHostDev, stream), stream, "broadcast");
+                                                      c->statusHostDev, stream), stream, "broadcast", true);
     return finish_launch(c, vc::launch_broadcast_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "broadcast");
 }
@@ -887,7 +900,7 @@ vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, 
     a.outRoot = root;
     if (p.bulkCopy)
         return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, c->statusDev,
-                                                      c->statusHostDev, stream), stream, "gather");
+                                                      c->statusHostDev, stream), stream, "gather", true);
     return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "gather");
 }
@@ -960,7 +973,8 @@ vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* 
     a.tileCounter = c->tileCounters + 2 * (size_t)(c->tileCounterSeq++ % vc::kTileCounterSlots);
     a.status = c->statusDev;
     a.statusHost = c->statusHostDev;
-    return finish_launch(c, vc::launch_alltoallv(a, p.gridCtas, p.threadsPerCta, stream), stream, "alltoallv");
+    return finish_launch(c, vc::launch_alltoallv(a, p.gridCtas, p.threadsPerCta, stream), stream, "alltoallv",
+                         true);
 }
 
 }  // extern "C"

@@ -37,6 +37,12 @@
  * communicator (its FIFOs are allocated then; capturing it earlier returns
  * vInvalidUsage); the captured transfer clears its FIFOs before every replay.  Graph
  * replays are ordered by the caller: vcommDestroy waits only for eager launches.
+ *
+ * Launch: the one-pass kernels are launched with programmatic stream serialization
+ * (programmatic dependent launch): a kernel may become resident while the previous
+ * kernel on the stream finishes, and waits for that kernel's completion (and its memory)
+ * before touching any buffer, so stream order is kept.  VCOMM_PDL=0 launches them
+ * plainly.
  */
 #ifndef VCOMM_H
 #define VCOMM_H
@@ -127,10 +133,13 @@ typedef enum {
  * all-gather, gather and broadcast stage tiles in shared memory with TMA bulk copies when
  * blocks are 16-byte aligned), VCOMM_GRID=flat|persistent (flat, the default: the
  * one-pass kernels launch one CTA per slice of work; persistent: about one resident wave
- * of CTAs striding over it), VCOMM_DEBUG=INFO (prints every plan to stderr). */
+ * of CTAs striding over it), VCOMM_PDL=0|1 (1, the default: programmatic dependent
+ * launch of the one-pass kernels), VCOMM_DEBUG=INFO (prints every plan to stderr). */
 vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol);
 
-/* Wait for the communicator's last enqueued work, then free everything it owns.
+/* Wait for the last enqueued work that uses the communicator's device memory (staged
+ * ring transfers, variable all-to-all, bulk-copy fan-out), then free everything it owns.
+ * The other collectives touch only the caller's buffers and need not have finished.
  * A NULL or already destroyed communicator gives vInvalidArgument. */
 vResult_t vcommDestroy(vcomm_t comm);
 

@@ -115,8 +115,9 @@ cudaError_t launch_allreduce_tree(const TreeArgs& a, vDataType_t dt, vRedOp_t op
 // into a CUDA graph carries its own copy.  table: items[0..nItems) (item i describes
 // all-reduce i), then at byte ptrByteOff the rank pointers: item i's 2*N pointers are
 // ptrs[items[i].ptrOff .. + 2N) (send pointers, then receive pointers).
-// Programmatic dependent launch of the one-pass kernels (on unless VCOMM_PDL=0; read when
-// a communicator is created).
+// Programmatic dependent launch of the one-pass kernels for the calling thread's next
+// launches (set from the communicator of the call: on unless it was created with
+// VCOMM_PDL=0).
 bool& pdl_enabled();
 
 // Largest grid the flat one-pass launches use; kernels stride over anything beyond.

@@ -21,7 +21,7 @@
 
 namespace vc {
 bool& pdl_enabled() {
-    static bool on = true;
+    thread_local bool on = true;      // set from the communicator of the call being launched
     return on;
 }
 }  // namespace vc
@@ -37,6 +37,7 @@ struct Config {
     bool debug = false;
     bool bulkCopy = false;           // TMA bulk copies for the fan-out copies (opt-in)
     bool persistentGrid = false;     // one-pass grids of one resident wave (A/B switch)
+    bool pdl = true;                 // programmatic dependent launch of the one-pass kernels
 };
 
 // One call recorded between vcommGroupStart and vcommGroupEnd.
@@ -112,6 +113,8 @@ struct DeviceGuard {
         if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
         if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
     }
+    // Also selects the communicator's launch mode for this thread's launches.
+    explicit DeviceGuard(const vcomm* c) : DeviceGuard(c->device) { vc::pdl_enabled() = c->cfg.pdl; }
     ~DeviceGuard() {
         int cur = -1;
         if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
@@ -148,8 +151,7 @@ void read_env(Config* cfg) {
     if (const char* s = std::getenv("VCOMM_DEBUG")) cfg->debug = !std::strcmp(s, "INFO");
     if (const char* s = std::getenv("VCOMM_COPY_TMA")) cfg->bulkCopy = !std::strcmp(s, "1");
     if (const char* s = std::getenv("VCOMM_GRID")) cfg->persistentGrid = !std::strcmp(s, "persistent");
-    const char* pdl = std::getenv("VCOMM_PDL");
-    vc::pdl_enabled() = !pdl || std::strcmp(pdl, "0") != 0;
+    if (const char* s = std::getenv("VCOMM_PDL")) cfg->pdl = std::strcmp(s, "0") != 0;
 }
 
 void free_comm(vcomm* c) {
@@ -543,7 +545,7 @@ fail:
 
 vResult_t vcommDestroy(vcomm_t c) {
     if (!comm_ok(c)) return vInvalidArgument;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (c->eventRecorded) cudaEventSynchronize(c->lastEvent);
     free_comm(c);
     return vSuccess;
@@ -576,7 +578,7 @@ vResult_t vcommGroupEnd(vcomm_t c) {
     recs.swap(*c->group);
     vResult_t s = sticky(c);
     if (s != vSuccess) return s;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vResult_t first = vSuccess;
     // Fused all-reduces: batches of one (type, op, stream, vector width), in order of
@@ -682,7 +684,7 @@ vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, v
         c->group->push_back(std::move(rec));
         return vSuccess;
     }
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     debug_plan(c, vCollAllReduce, count, dt, p);
     if (p.algo == vAlgoRing)
@@ -741,7 +743,7 @@ static vResult_t reduce_scatter_impl(const void* const* send, void* const* recv,
     if (outType != dt && !(outType == vFloat32 && (dt == vFloat16 || dt == vBFloat16))) return vInvalidArgument;
     for (int r = 0; r < c->nRanks; r++)
         if (!ptr_aligned(recv[r], elem_size(outType))) return vInvalidArgument;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollReduceScatter, rc, dt, f.aligned, &p);
@@ -781,7 +783,7 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
     (void)op;
     Front f = front(c, send, recv, sendcount, dt, 0, true);
     if (f.res != vSuccess || sendcount == 0) return f.res;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollAllGather, sendcount, dt, f.aligned, &p);
@@ -810,7 +812,7 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
     if (root < 0 || root >= c->nRanks) return vInvalidArgument;
     Front f = front(c, send, recv, count, dt, root, false);
     if (f.res != vSuccess || count == 0) return f.res;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollBroadcast, count, dt, f.aligned, &p);
@@ -841,7 +843,7 @@ vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vD
     (void)op;
     Front f = front(c, send, recv, count, dt, 0, true);
     if (f.res != vSuccess || count == 0) return f.res;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollAllToAll, count, dt, f.aligned, &p);
@@ -864,7 +866,7 @@ vResult_t vReduce(const void* const* send, void* const* recv, size_t count, vDat
     if (root < 0 || root >= c->nRanks || !valid_op(op)) return vInvalidArgument;
     Front f = front(c, send, recv, count, dt, root, true, false);
     if (f.res != vSuccess || count == 0) return f.res;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollReduce, count, dt, f.aligned, &p);
@@ -889,7 +891,7 @@ vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, 
     if (root < 0 || root >= c->nRanks) return vInvalidArgument;
     Front f = front(c, send, recv, sendcount, dt, root, true, false);
     if (f.res != vSuccess || sendcount == 0) return f.res;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollGather, sendcount, dt, f.aligned, &p);
@@ -916,7 +918,7 @@ vResult_t vScatter(const void* const* send, void* const* recv, size_t recvcount,
     if (root < 0 || root >= c->nRanks) return vInvalidArgument;
     Front f = front(c, send, recv, recvcount, dt, root, false, true);
     if (f.res != vSuccess || recvcount == 0) return f.res;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     vResult_t r = make_plan(c, vCollScatter, recvcount, dt, f.aligned, &p);
@@ -952,7 +954,7 @@ vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* 
     }
     const int aligned = (int)(bits & (~bits + 1));
     vResult_t r;
-    DeviceGuard g(c->device);
+    DeviceGuard g(c);
     if (!g.ok) return vUnhandledCudaError;
     vPlanInfo_t p;
     r = make_plan(c, vCollAllToAllv, 0, dt, aligned, &p);

@@ -61,6 +61,25 @@ def draw(case: int) -> dict:
 
 @pytest.mark.parametrize("case", range(N_CASES))
 def test_random_case_matches_oracle(comms, case):
+    run_case(comms, case)
+
+
+# The engines that are not the default stay selectable; the first cases run again under
+# each (the switches are read when a communicator is created).
+@pytest.mark.parametrize("env", [{"VCOMM_GRID": "persistent"}, {"VCOMM_COPY_TMA": "1"}, {"VCOMM_PDL": "0"}],
+                         ids=["persistent_grid", "tma_fanout", "no_pdl"])
+@pytest.mark.parametrize("case", range(0, N_CASES, 4))
+def test_random_case_with_other_engines(monkeypatch, env, case):
+    for name, value in env.items():
+        monkeypatch.setenv(name, value)
+    local = Comms()
+    try:
+        run_case(local, case)
+    finally:
+        local.close()
+
+
+def run_case(comms, case):
     k = draw(case)
     n, count, dt, op, root, pad = k["n"], k["count"], k["dtype"], k["op"], k["root"], k["pad"]
     c = comms.get(n, k["channels"], k["proto"], k["algo"], chunk=k["chunk"])

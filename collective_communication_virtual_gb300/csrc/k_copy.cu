@@ -159,7 +159,8 @@ k_scatter_onepass(const __grid_constant__ OnePassArgs a) {
 // flight stay within a narrow window of the buffers, as with the flat grids of the other
 // copies.  The last CTA to finish resets the counter for the next launch.  Every CTA
 // builds the tile prefix sums in shared memory from the device tables.
-// Three copy widths are inlined here, so the kernel keeps 128 registers: one CTA per SM.
+// Three copy widths are inlined here, so the kernel keeps 128 registers: one CTA per SM,
+// so the grid is one wave of CTAs that take tiles from the counter.
 template <int ESZ>
 __global__ void __launch_bounds__(kOnePassThreads, 1)
 k_alltoallv(const __grid_constant__ A2AvArgs a) {

@@ -185,22 +185,23 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
 
     if (!ring) {
         // One pass.  Default ("flat"): one CTA per slice of work -- a 512-thread CTA per
-        // 512 vectors of every rank for the reductions, per 64 KiB tile for the copies --
-        // so the hardware hands CTAs out in order and the DRAM pages in use at any moment
+        // 512 vectors of every rank for the reductions, per 16-64 KiB tile for the copies
+        // -- so the hardware hands CTAs out in order and the DRAM pages in use at any moment
         // stay within a narrow window of every buffer.  A persistent grid of one resident
         // wave whose CTAs stride over the work lets the CTAs drift apart and spreads the
         // accesses; measured on GB300 (8 ranks x 64 MiB fp32) it is 8-10 % slower.  It
         // stays selectable (persistentGrid) for comparison.
         p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
         p->threadsPerCta = vc::kOnePassThreads;
-        // Round down so the grid never spills into a second, mostly idle wave.  The
-        // 32-byte reduction kernels hold 128 registers: one CTA per SM; the copies two.
+        // One resident wave (the persistent shape, and the cap for small work): rounded down
+        // so it never spills into a second, mostly idle wave.  The 32-byte reduction kernels
+        // hold up to 128 registers, one 512-thread CTA per SM; the copies fit two.
         const bool wide = p->vecBytes == 32 && (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ||
                                                 q->coll == vCollReduce);
         const int target = (wide ? 1 : 2) * smCount;
         int per = std::max(1, target / q->nChannels);
         // Never more CTAs than a channel has work items: for the reductions a work item is
-        // one thread's unit (a 16-byte vector of every rank), for the copies a 64 KiB tile.
+        // one thread's unit (a vector of every rank), for the copies a tile.
         size_t maxPer = 1;
         if (q->coll == vCollAllToAllv) {
             maxPer = (size_t)target;

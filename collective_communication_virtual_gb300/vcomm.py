@@ -132,12 +132,18 @@ def lib() -> ctypes.CDLL:
 
 # ---- marshalling helpers -------------------------------------------------------------------
 
+_DTYPE_CODES: dict = {}
+_ARRAY_TYPES: dict = {}
+
+
 def _dtype_code(dt) -> int:
     if isinstance(dt, int):
         return dt
-    import torch
-    return {torch.float32: vFloat32, torch.float16: vFloat16, torch.bfloat16: vBFloat16,
-            torch.int32: vInt32}[dt]
+    if not _DTYPE_CODES:
+        import torch
+        _DTYPE_CODES.update({torch.float32: vFloat32, torch.float16: vFloat16, torch.bfloat16: vBFloat16,
+                             torch.int32: vInt32})
+    return _DTYPE_CODES[dt]
 
 
 def _op_code(op) -> int:
@@ -153,10 +159,12 @@ def _addr(x) -> int | None:
 
 
 def _ptr_array(bufs):
-    arr = (ctypes.c_void_p * len(bufs))()
-    for i, b in enumerate(bufs):
-        arr[i] = _addr(b)
-    return arr
+    """A C array of the buffers' device addresses (None for NULL)."""
+    n = len(bufs)
+    arr_t = _ARRAY_TYPES.get(n)
+    if arr_t is None:
+        arr_t = _ARRAY_TYPES[n] = ctypes.c_void_p * n
+    return arr_t(*[None if b is None else (b if isinstance(b, int) else b.data_ptr()) for b in bufs])
 
 
 def _stream(stream) -> int | None:

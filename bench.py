@@ -227,7 +227,7 @@ def cpu_baseline_sample(torch):
     xs = inputs.uniform_ranks(N_RANKS, COUNT, torch.float32, 1)
     oracle.allreduce(xs, "sum", nthreads=cores)
     reps, t0 = 0, time.perf_counter()
-    while reps < 3 or (time.perf_counter() - t0 < 10.0 and reps < 50):
+    while reps < 3 or (time.perf_counter() - t0 < 10.0 and reps < 1000):     # about 10 s of CPU work
         oracle.allreduce(xs, "sum", nthreads=cores)
         reps += 1
     dt = (time.perf_counter() - t0) / reps
@@ -496,8 +496,28 @@ def other_workloads(torch, V, dev, stream, hbm):
     return out
 
 
+def time_graph_allreduce(V, torch, comm, send, recv, count, launches, reps):
+    """Device time per all-reduce with no host gaps: `launches` calls captured into one CUDA
+    graph, replayed `reps` times."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(launches):
+            V.vAllReduce(send, recv, count, torch.float32, "sum", comm)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / (reps * launches)
+
+
 def sweep(torch, V, dev, stream, hbm):
-    """busBW and HBM fraction against bytes per rank (1 KiB .. 1 GiB, powers of 4)."""
+    """busBW and HBM fraction against bytes per rank (1 KiB .. 1 GiB, powers of 4): eager
+    calls (host launch cost included) and the same calls replayed from a CUDA graph (device
+    time only)."""
     out = []
     comm = V.vcommInit(N_RANKS, 1, V.vProtoSimple)
     V.vcommSetAlgo(comm, "onepass")
@@ -508,8 +528,11 @@ def sweep(torch, V, dev, stream, hbm):
         recv = [torch.empty_like(s) for s in send]
         steps = 200 if nbytes <= (1 << 20) else (50 if nbytes <= (64 << 20) else 10)
         t = time_allreduce(V, torch, comm, send, recv, count, steps, 5, stream)
+        tg = time_graph_allreduce(V, torch, comm, send, recv, count, 20 if nbytes <= (64 << 20) else 4, 5)
         out.append({"bytes_per_rank": nbytes, "busbw_gbs": nbytes / t * bus_factor(N_RANKS) / 1e9,
-                    "hbm_frac": 2 * N_RANKS * nbytes / t / 1e9 / hbm, "us": t * 1e6})
+                    "hbm_frac": 2 * N_RANKS * nbytes / t / 1e9 / hbm, "us": t * 1e6,
+                    "graph_us": tg * 1e6, "graph_busbw_gbs": nbytes / tg * bus_factor(N_RANKS) / 1e9,
+                    "graph_hbm_frac": 2 * N_RANKS * nbytes / tg / 1e9 / hbm})
         del send, recv
         torch.cuda.empty_cache()
     V.vcommDestroy(comm)

@@ -302,6 +302,7 @@ def run_ours(args):
     if rank == 0 and not args.no_extras:
         line["e2e"] = e2e_allreduce(torch, V, comm, xs, dev, stream, steps=max(3, min(args.steps, 10)))
         line["sweep"] = sweep(torch, V, dev, stream, hbm)
+        line["sweep_collectives"] = sweep_collectives(torch, V, dev, hbm)
         line["channel_sweep"] = channel_sweep(torch, V, send, recv, stream)
         line["other_workloads"] = other_workloads(torch, V, dev, stream, hbm)
         line["cpu_baseline"] = cpu_baseline_sample(torch)
@@ -535,6 +536,74 @@ def sweep(torch, V, dev, stream, hbm):
                     "graph_hbm_frac": 2 * N_RANKS * nbytes / tg / 1e9 / hbm})
         del send, recv
         torch.cuda.empty_cache()
+    V.vcommDestroy(comm)
+    return out
+
+
+def sweep_collectives(torch, V, dev, hbm):
+    """Reduce-scatter, all-gather, broadcast and all-to-all (fp32) against bytes per rank,
+    1 KiB .. 1 GiB in powers of 4: eager and replayed from a CUDA graph.  Bytes per rank
+    is the send size (RS, BC, A2A) or the receive size (AG); minimum bytes and bus factor
+    as the planner reports them."""
+    n = N_RANKS
+    comm = V.vcommInit(n, 1, V.vProtoSimple)
+    V.vcommSetAlgo(comm, "onepass")
+    out = {}
+
+    def calls(coll, send, recv, elems):
+        if coll == "reduce_scatter":
+            return lambda: V.vReduceScatter(send, recv, elems // n, torch.float32, "sum", comm)
+        if coll == "allgather":
+            return lambda: V.vAllGather(send, recv, elems // n, torch.float32, "sum", comm)
+        if coll == "broadcast":
+            return lambda: V.vBroadcast(send, recv, elems, torch.float32, "sum", 0, comm)
+        return lambda: V.vAllToAll(send, recv, elems // n, torch.float32, "sum", comm)
+
+    codes = {"reduce_scatter": V.vCollReduceScatter, "allgather": V.vCollAllGather,
+             "broadcast": V.vCollBroadcast, "alltoall": V.vCollAllToAll}
+    for coll in ("reduce_scatter", "allgather", "broadcast", "alltoall"):
+        rows = []
+        for k in range(11):
+            nbytes = 1024 * 4 ** k
+            elems = nbytes // 4                          # elements per rank of the big side
+            small = elems // n
+            send_elems = small if coll == "allgather" else elems
+            recv_elems = small if coll == "reduce_scatter" else elems
+            send = [torch.rand(send_elems, device=dev) for _ in range(n)]
+            recv = [torch.empty(recv_elems, device=dev) for _ in range(n)]
+            fn = calls(coll, send, recv, elems)
+            count = small if coll in ("reduce_scatter", "allgather", "alltoall") else elems
+            plan = V.vcommQueryPlan(comm, codes[coll], count, torch.float32, 32)
+            steps = 200 if nbytes <= (1 << 20) else (50 if nbytes <= (64 << 20) else 10)
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            t = a.elapsed_time(b) / 1e3 / steps
+            g = torch.cuda.CUDAGraph()
+            launches = 20 if nbytes <= (64 << 20) else 4
+            with torch.cuda.graph(g):
+                for _ in range(launches):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(5):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            tg = a.elapsed_time(b) / 1e3 / (5 * launches)
+            rows.append({"bytes_per_rank": nbytes, "us": t * 1e6, "graph_us": tg * 1e6,
+                         "busbw_gbs": nbytes / tg * plan["busFactor"] / 1e9,
+                         "graph_hbm_frac": plan["minBytes"] / tg / 1e9 / hbm})
+            del send, recv, g
+            torch.cuda.empty_cache()
+        out[coll] = rows
     V.vcommDestroy(comm)
     return out
 

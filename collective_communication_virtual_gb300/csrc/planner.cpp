@@ -172,7 +172,10 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         // The 8-rank 32-byte kernel keeps its vectors in registers (one CTA per SM); the
         // others fit two per SM.
         const size_t resident = (size_t)((N == 8 && p->vecBytes == 32) ? 1 : 2) * smCount;
-        const size_t need = div_up(work, vc::kOnePassThreads);
+        if (!q->persistentGrid)                       // small work: smaller CTAs, more SMs
+            while (p->threadsPerCta > 64 && div_up(work, (size_t)p->threadsPerCta) < (size_t)smCount)
+                p->threadsPerCta /= 2;
+        const size_t need = div_up(work, (size_t)p->threadsPerCta);
         const size_t cap = (q->persistentGrid || need < 2 * resident) ? resident : (size_t)vc::kMaxGridCtas;
         p->ctasPerChannel = (int)std::max<size_t>(1, std::min<size_t>(cap, need));
         p->gridCtas = p->ctasPerChannel;
@@ -209,19 +212,30 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
             const size_t chElems = std::min(p->channelElems, B);
             if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter || q->coll == vCollReduce) {
                 const size_t unit = p->vecBytes ? p->vecBytes / esz : 1;
-                maxPer = div_up(div_up(chElems, unit) * (size_t)N, (size_t)p->threadsPerCta);
+                const size_t units = div_up(chElems, unit) * (size_t)N;
+                // Small work: smaller CTAs (down to 64 threads) spread it over more SMs
+                // instead of loading a few SMs with 512 threads each.
+                if (!q->persistentGrid)
+                    while (p->threadsPerCta > 64 &&
+                           div_up(units * (size_t)q->nChannels, (size_t)p->threadsPerCta) < (size_t)smCount)
+                        p->threadsPerCta /= 2;
+                maxPer = div_up(units, (size_t)p->threadsPerCta);
             } else {
                 size_t blocks = q->coll == vCollBroadcast ? 1 : q->coll == vCollAllToAll ? (size_t)N * N : (size_t)N;
                 // Copies: 64 KiB tiles (128 bytes in flight per thread of a 512-thread CTA)
                 // unless that leaves fewer than four waves of resident CTAs (two per SM);
                 // then 32 or 16 KiB tiles, so the last, partly filled wave is a smaller
                 // share of the launch.
+                // Small messages: tiles down to 2 KiB (CTAs of tile / 32 threads, at least
+                // 64) until there is a tile for every SM.
                 size_t tile = (size_t)64 * 1024;
-                if (!q->persistentGrid)
-                    while (tile > 16 * 1024 &&
-                           div_up(chElems * esz, tile) * blocks * (size_t)q->nChannels < (size_t)8 * smCount)
-                        tile /= 2;
+                auto tiles = [&](size_t t) { return div_up(chElems * esz, t) * blocks * (size_t)q->nChannels; };
+                if (!q->persistentGrid) {
+                    while (tile > 16 * 1024 && tiles(tile) < (size_t)8 * smCount) tile /= 2;
+                    while (tile > 2 * 1024 && tiles(tile) < (size_t)smCount) tile /= 2;
+                }
                 p->tileBytes = tile;
+                p->threadsPerCta = (int)std::min<size_t>(vc::kOnePassThreads, std::max<size_t>(64, tile / 32));
                 maxPer = div_up(chElems * esz, tile) * blocks;
             }
         }

@@ -248,3 +248,23 @@ def test_tree_plan():
     assert plan(algo=V.vAlgoTree, count=16 << 20, persistentGrid=1).gridCtas == 304
     assert plan(algo=V.vAlgoTree, count=16 << 20, coll=V.vCollReduceScatter).algo == V.vAlgoOnePass
     assert plan(algo=V.vAlgoTree, count=100, nRanks=1).algo == V.vAlgoOnePass
+
+
+def test_small_work_spreads_over_more_smaller_ctas():
+    # 16 KiB fp32 per rank, 8 ranks, 32-byte vectors: 512 units -> 64-thread CTAs, 8 of them
+    p = plan(count=4096, aligned32=1)
+    assert p.threadsPerCta == 64 and p.gridCtas == 8
+    # 256 KiB: 8192 units -> 64-thread CTAs (128 of them, still fewer than the 152 SMs at 128)
+    p = plan(count=65536, aligned32=1)
+    assert p.threadsPerCta == 64 and p.gridCtas == 128
+    # enough work for every SM at 512 threads: unchanged
+    p = plan(count=16 << 20, aligned32=1)
+    assert p.threadsPerCta == 512
+    # copies: tiles shrink to 2 KiB and CTAs to tile / 32 threads until every SM has a tile
+    p = plan(coll=V.vCollAllGather, count=1024, aligned32=1, noBulkCopy=1)     # 4 KiB blocks
+    assert p.tileBytes == 2048 and p.threadsPerCta == 64 and p.gridCtas == 2 * 8
+    p = plan(coll=V.vCollAllGather, count=1 << 20, aligned32=1, noBulkCopy=1)  # 4 MiB blocks
+    assert p.tileBytes == 16384 and p.threadsPerCta == 512
+    # the persistent shape keeps 512-thread CTAs and 64 KiB tiles
+    p = plan(count=4096, aligned32=1, persistentGrid=1)
+    assert p.threadsPerCta == 512

@@ -59,7 +59,7 @@ const RingFit kRingFit[3] = {
     {{33.1, 37.5, 38.3}, {6821.0, 46568.0, 107373.0}},       // LL
     {{50.8, 51.4, 56.0}, {6184.0, 42541.0, 103539.0}},       // LL128
 };
-const double kOnePassLatUs = 2.1;
+const double kOnePassLatUs = 1.5;
 const double kOnePassBytesPerUs = 7.05e6;                    // minimum bytes / (time - latency)
 
 double interp_ch(const double v[3], int ch) {

@@ -286,7 +286,15 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     p->nChannels = q->nChannels;
     p->ctasPerChannel = N;
     p->gridCtas = N * q->nChannels;
-    p->threadsPerCta = vc::kRingThreads;
+    // Threads per (channel, rank) CTA: the per-protocol thread thresholds (NCCL book
+    // section 2.4, comm.h: LL 8, LL128 8, Simple 64), read as the fewest payload bytes of
+    // one step that each thread should carry -- a small step runs on fewer threads (never
+    // fewer than two warps), which makes the per-slot barriers cheaper.
+    const size_t threshold = proto == vProtoSimple ? 64 : 8;
+    const size_t stepBytes = std::min(p->chunkElems, std::max<size_t>(1, std::min(p->channelElems, B))) * esz;
+    int nt = vc::kRingThreads;
+    while (nt > 64 && stepBytes < (size_t)nt * threshold) nt /= 2;
+    p->threadsPerCta = nt;
     // The 16-byte path of the ring also needs every slot and chunk to start on a vector.
     if (p->slotPayloadElems % VE != 0) p->vectorized = 0;
     p->vecBytes = p->vectorized ? 16 : 0;

@@ -268,3 +268,15 @@ def test_small_work_spreads_over_more_smaller_ctas():
     # the persistent shape keeps 512-thread CTAs and 64 KiB tiles
     p = plan(count=4096, aligned32=1, persistentGrid=1)
     assert p.threadsPerCta == 512
+
+
+def test_ring_threads_follow_the_protocol_thread_thresholds():
+    # comm.h thresholds: Simple 64, LL 8, LL128 8 bytes of a step per thread
+    big = plan(algo=V.vAlgoRing, proto=V.vProtoSimple, count=16 << 20, chunkBytes=1 << 20)
+    assert big.threadsPerCta == 512
+    # 1 KiB per rank: 128-byte blocks -> the floor of two warps for every protocol
+    for proto in (V.vProtoSimple, V.vProtoLL, V.vProtoLL128):
+        assert plan(algo=V.vAlgoRing, proto=proto, count=256).threadsPerCta == 64
+    # 16 KiB per rank, one channel: 2 KiB steps -> Simple wants 32 threads (floor 64), LL 256
+    assert plan(algo=V.vAlgoRing, proto=V.vProtoSimple, count=4096).threadsPerCta == 64
+    assert plan(algo=V.vAlgoRing, proto=V.vProtoLL, count=4096).threadsPerCta == 256

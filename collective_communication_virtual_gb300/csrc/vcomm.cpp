@@ -309,14 +309,16 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
     unsigned int epoch;
     if (capturing) {
         // A captured launch replays with the arguments it was captured with, so it cannot
-        // carry a fresh epoch: the graph clears the control words and FIFOs itself before
-        // every replay and uses epoch 1, which eager launches never use.  FIFOs cannot be
-        // allocated during capture: an eager ring call of at least this size must come first.
+        // carry a fresh epoch: the graph clears the control words before every replay and
+        // uses epoch 1, which eager launches never use.  LL and LL128 keep their flags in
+        // the FIFO lines, so for them the graph clears the FIFOs too; Simple data is
+        // ordered by the counters alone.  FIFOs cannot be allocated during capture: an
+        // eager ring call of at least this size must come first.
         const size_t need = (size_t)c->nChannels * c->nRanks * p.fifoBytes;
         if (!c->ctrl || need > c->fifoCap) return vInvalidUsage;
         const size_t ctrlBytes = (size_t)c->nChannels * c->nRanks * vc::kCtrlStride * sizeof(unsigned long long);
         e = cudaMemsetAsync(c->ctrl, 0, ctrlBytes, stream);
-        if (e == cudaSuccess) e = cudaMemsetAsync(c->fifo, 0, need, stream);
+        if (e == cudaSuccess && p.proto != vProtoSimple) e = cudaMemsetAsync(c->fifo, 0, need, stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(capture)");
         epoch = 1;
     } else {

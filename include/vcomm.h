@@ -35,7 +35,8 @@
  * CUDA graphs: collectives may be captured into a graph.  A ring transfer can be
  * captured only after an eager ring call of at least the same size on the same
  * communicator (its FIFOs are allocated then; capturing it earlier returns
- * vInvalidUsage); the captured transfer clears its FIFOs before every replay.  Graph
+ * vInvalidUsage); the captured transfer clears its control words (and, for LL and LL128,
+ * its FIFOs, whose lines carry the flags) before every replay.  Graph
  * replays are ordered by the caller: vcommDestroy waits only for eager launches.
  *
  * Launch: the one-pass kernels are launched with programmatic stream serialization

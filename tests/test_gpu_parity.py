@@ -391,7 +391,8 @@ def test_moe_dispatch_full(comms):
 
 
 # ---------------------------------------------------------------------------------------
-# CUDA graph capture and replay (the ring clears its FIFOs inside the graph)
+# CUDA graph capture and replay (the ring clears its counters, and for LL and LL128 its
+# FIFOs, inside the graph)
 # ---------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("variant", VARIANTS, ids=VID)

@@ -453,6 +453,15 @@ def other_workloads(torch, V, dev, stream, hbm):
     rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
     t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
     rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    # the staged ring's own reduce-scatter and all-gather (Simple, 32 channels, 1 MiB chunks)
+    ring = V.vcommInit(n, 32, V.vProtoSimple)
+    V.vcommSetAlgo(ring, "ring")
+    V.vcommSetChunkBytes(ring, 1 << 20)
+    t = tm(lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", ring, stream), 10)
+    rec("ring_reduce_scatter_fp32_64MiB_simple_32ch", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    t = tm(lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", ring, stream), 10)
+    rec("ring_allgather_fp32_64MiB_simple_32ch", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    V.vcommDestroy(ring)
     tree = V.vcommInit(n, 1, V.vProtoSimple)
     V.vcommSetAlgo(tree, "tree")
     t = tm(lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", tree, stream))

@@ -12,6 +12,8 @@
 //
 // Every wait is bounded: a load that has not landed after kWaitNs makes the kernel record
 // vTimeout in the status word, stop issuing, drain its own bulk operations and return.
+#include <atomic>
+
 #include "device.cuh"
 
 namespace vc {
@@ -176,12 +178,17 @@ __global__ void __launch_bounds__(32) k_fanout_tma(const __grid_constant__ OnePa
 
 cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast, int grid, Status* st,
                               volatile Status* stHost, cudaStream_t s) {
-    static bool attrSet = false;       // per process; the attribute is per function
-    if (!attrSet) {
-        const cudaError_t e = cudaFuncSetAttribute(k_fanout_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)kTmaSmemBytes);
+    // The shared-memory limit is an attribute of the function on each device: set it once
+    // per device (bit d of the mask).
+    static std::atomic<unsigned long long> attrSet{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attrSet.load() & bit)) {
+        e = cudaFuncSetAttribute(k_fanout_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmemBytes);
         if (e != cudaSuccess) return e;
-        attrSet = true;
+        attrSet.fetch_or(bit);
     }
     return pdl_launch(k_fanout_tma, grid, 32, kTmaSmemBytes, s, a, elemSize, broadcast ? 1 : 0, st,
                       (Status*)stHost);

@@ -348,8 +348,22 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
         const unsigned long long sflag = a.epochHi | (c.sendSeq + 1ull);
         if (kind & kRecv) {
             if (t == 7) {
-                for (size_t L = (size_t)warp * 4 + g; L < lines; L += perIter)
-                    if (!wait_flag64(a, c, rs + L * 128 + 120, rflag, c.recvSeq)) { fail = true; break; }
+                // Flags of this lane's lines, 8 loads in flight at a time; only a flag that
+                // is not yet set is waited for on its own.
+                for (size_t L0 = (size_t)warp * 4 + g; L0 < lines && !fail; L0 += 8 * perIter) {
+                    unsigned long long f[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const size_t L = L0 + (size_t)k * perIter;
+                        f[k] = L < lines ? ld_volatile_u64(rs + L * 128 + 120) : rflag;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const size_t L = L0 + (size_t)k * perIter;
+                        if (f[k] != rflag && !fail && !wait_flag64(a, c, rs + L * 128 + 120, rflag, c.recvSeq))
+                            fail = true;
+                    }
+                }
             }
             __threadfence();
             __syncwarp();

@@ -44,8 +44,9 @@ size_t pow2_floor(size_t x) {
 // The ring model of the NCCL book chapter 5 (ring.cc): time = latency + bus bytes / bus
 // bandwidth, where a collective of S bytes per rank moves S * nSteps / N bus bytes
 // (nSteps = 2(N-1) for all-reduce, N-1 otherwise), and LL / LL128 trade bandwidth for
-// latency.  The constants are refit on a GB300 from CUDA-graph replay times of an fp32
-// all-reduce over 8 virtual ranks, 1 KiB .. 256 MiB per rank: latency = time at 1 KiB;
+// latency.  The constants are refit on a GB300 (collective_communication_virtual_gb300/
+// calibrate.py) from CUDA-graph replay times of an fp32 all-reduce over 8 virtual ranks
+// at 1 KiB and 256 MiB per rank: latency = time at 1 KiB;
 // bus rate from the 256 MiB point, at 1, 8 and 32 channels (interpolated in log2 of the
 // channel count, held flat beyond).  Ring latency grows with the number of steps, so it
 // is scaled by nSteps / 14 (14 steps for an 8-rank all-reduce).  The one-pass kernels are
@@ -54,13 +55,13 @@ struct RingFit {
     double latUs[3];           // at 1, 8, 32 channels
     double busBytesPerUs[3];
 };
-const RingFit kRingFit[3] = {
-    {{43.3, 48.0, 49.4}, {14852.0, 96543.0, 186388.0}},      // Simple
-    {{33.1, 37.5, 38.3}, {6821.0, 46568.0, 107373.0}},       // LL
-    {{50.8, 51.4, 56.0}, {6184.0, 42541.0, 103539.0}},       // LL128
+const RingFit kRingFit[3] = {                                // calibrate.py prints these
+    {{41.0, 37.3, 38.8}, {14825.4, 95615.7, 190124.4}},     // Simple
+    {{32.8, 36.3, 37.2}, {6824.5, 49527.8, 107635.9}},      // LL
+    {{51.6, 52.3, 52.7}, {8464.4, 58441.0, 115475.4}},      // LL128
 };
 const double kOnePassLatUs = 1.5;
-const double kOnePassBytesPerUs = 7.05e6;                    // minimum bytes / (time - latency)
+const double kOnePassBytesPerUs = 7.107e6;                   // minimum bytes / (time - latency)
 
 double interp_ch(const double v[3], int ch) {
     const double x = ch <= 1 ? 0.0 : (ch >= 32 ? 5.0 : std::log2((double)ch));

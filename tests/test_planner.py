@@ -106,12 +106,14 @@ def test_auto_protocol_follows_the_fitted_ring_model():
 
 
 def test_model_reproduces_its_measured_anchor_points():
-    # fp32 all-reduce, 8 ranks: one-pass 1.5 us at 1 KiB, 610.7 us at 256 MiB per rank;
-    # ring Simple at 32 channels 49.4 us and 2569.7 us
+    # fp32 all-reduce, 8 ranks: one-pass 1.5 us at 1 KiB and 1.5 + 4 GiB / 7.107e6 B/us at
+    # 256 MiB per rank; ring Simple at 32 channels 38.8 us and 38.8 + 256 MiB * 14/8 / 190124.4
+    big = 256 << 20
     assert plan(count=256).predictedUs == pytest.approx(1.5, rel=0.01)
-    assert plan(count=64 << 20).predictedUs == pytest.approx(610.7, rel=0.01)
-    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(49.4, rel=0.01)
-    assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=32).predictedUs == pytest.approx(2569.7, rel=0.01)
+    assert plan(count=64 << 20).predictedUs == pytest.approx(1.5 + 16 * big / 7.107e6, rel=0.001)
+    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(38.8, rel=0.01)
+    assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=32).predictedUs == \
+        pytest.approx(38.8 + big * 14 / 8 / 190124.4, rel=0.001)
 
 
 def test_auto_algorithm_picks_the_one_pass_kernels():

@@ -8,6 +8,7 @@
 // like ncclComm so a destroyed or foreign handle is refused.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -16,8 +17,6 @@
 #include <vector>
 
 #include "internal.h"
-
-#include <algorithm>
 
 namespace vc {
 bool& pdl_enabled() {
@@ -29,6 +28,14 @@ bool& pdl_enabled() {
 namespace {
 
 constexpr unsigned long long kMagic = 0x76636F6D6D763031ull;   // "vcommv01"
+constexpr int kTrackedStreams = 16;
+
+// The last launch that used communicator memory on one stream.
+struct StreamEvent {
+    cudaStream_t stream;
+    cudaEvent_t event;
+    bool recorded;
+};
 
 struct Config {
     vAlgo_t algo = vAlgoAuto;
@@ -80,8 +87,8 @@ struct vcomm {
     unsigned long long* ctrl;
     unsigned int epoch;
     int testStallRank;
-    cudaEvent_t lastEvent;
-    bool eventRecorded;
+    StreamEvent tracked[kTrackedStreams];   // per stream; reused round-robin when full
+    unsigned int trackedNext;
     // group batching
     int groupDepth;
     std::vector<GroupRec>* group;
@@ -157,7 +164,8 @@ void read_env(Config* cfg) {
 void free_comm(vcomm* c) {
     delete c->group;
     delete c->groupArgs;
-    if (c->lastEvent) cudaEventDestroy(c->lastEvent);
+    for (auto& t : c->tracked)
+        if (t.event) cudaEventDestroy(t.event);
     if (c->fifo) cudaFree(c->fifo);
     if (c->ctrl) cudaFree(c->ctrl);
     if (c->statusDev) cudaFree(c->statusDev);
@@ -236,6 +244,38 @@ bool stream_capturing(cudaStream_t stream) {
     return cs != cudaStreamCaptureStatusNone;
 }
 
+// Record, on `stream`, the point after the launch just enqueued (one event per stream).
+void track_launch(vcomm* c, cudaStream_t stream) {
+    StreamEvent* slot = nullptr;
+    for (auto& t : c->tracked)
+        if (t.event && t.stream == stream) { slot = &t; break; }
+    if (!slot) {
+        for (auto& t : c->tracked)
+            if (!t.event) { slot = &t; break; }
+    }
+    if (!slot) {                     // every slot in use: retire the oldest-assigned one
+        slot = &c->tracked[c->trackedNext++ % kTrackedStreams];
+        if (slot->recorded) cudaEventSynchronize(slot->event);
+        slot->recorded = false;
+    }
+    if (!slot->event && cudaEventCreateWithFlags(&slot->event, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        cudaStreamSynchronize(stream);           // cannot track it: wait for it instead
+        return;
+    }
+    slot->stream = stream;
+    if (cudaEventRecord(slot->event, stream) == cudaSuccess) slot->recorded = true;
+}
+
+// Wait for every tracked launch (before freeing or replacing communicator memory).
+void wait_tracked(vcomm* c) {
+    for (auto& t : c->tracked)
+        if (t.recorded) {
+            cudaEventSynchronize(t.event);
+            t.recorded = false;
+        }
+}
+
 // usesComm: the kernel touches communicator memory (FIFOs, counters, the status word), so
 // vcommDestroy must wait for it.  Launches that touch only the caller's buffers are not
 // tracked: an event recorded between two kernels would also stop the second from being
@@ -245,10 +285,9 @@ vResult_t finish_launch(vcomm* c, cudaError_t e, cudaStream_t stream, const char
         c->hostError = vUnhandledCudaError;
         return cuda_fail(c, e, what);
     }
-    // Track the last eager launch for vcommDestroy; launches being captured into a graph
-    // run when the graph does, which the caller orders.
-    if (usesComm && !stream_capturing(stream) && cudaEventRecord(c->lastEvent, stream) == cudaSuccess)
-        c->eventRecorded = true;
+    // Eager launches only; launches captured into a graph run when the graph does, which
+    // the caller orders.
+    if (usesComm && !stream_capturing(stream)) track_launch(c, stream);
     return vSuccess;
 }
 
@@ -280,7 +319,7 @@ vResult_t ensure_fifo(vcomm* c, const vPlanInfo_t& p) {
         if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemset(ctrl)");
     }
     if (need <= c->fifoCap) return vSuccess;
-    if (c->eventRecorded) cudaEventSynchronize(c->lastEvent);
+    wait_tracked(c);                 // no launch may still use the FIFOs being replaced
     if (c->fifo) cudaFree(c->fifo);
     c->fifo = nullptr;
     c->fifoCap = 0;
@@ -533,7 +572,6 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
     if ((e = cudaHostAlloc(&c->abortHost, sizeof(unsigned int), cudaHostAllocMapped)) != cudaSuccess) goto fail;
     *c->abortHost = 0;
     if ((e = cudaHostGetDevicePointer(&c->abortHostDev, c->abortHost, 0)) != cudaSuccess) goto fail;
-    if ((e = cudaEventCreateWithFlags(&c->lastEvent, cudaEventDisableTiming)) != cudaSuccess) goto fail;
     c->startMagic = c->endMagic = kMagic;
     *comm = c;
     return vSuccess;
@@ -548,7 +586,7 @@ fail:
 vResult_t vcommDestroy(vcomm_t c) {
     if (!comm_ok(c)) return vInvalidArgument;
     DeviceGuard g(c);
-    if (c->eventRecorded) cudaEventSynchronize(c->lastEvent);
+    wait_tracked(c);
     free_comm(c);
     return vSuccess;
 }

@@ -156,12 +156,14 @@ const char* vcommGetErrorString(vResult_t result);
 
 /* Group batching (NCCL book chapter 6 ncclPrepareTasks and chapter 7 ncclGroupStart /
  * ncclGroupEnd).  Between vcommGroupStart and vcommGroupEnd every collective call on
- * this communicator is checked and recorded (its pointer arrays copied) and returns
- * vSuccess; nothing is enqueued.  vcommGroupEnd enqueues them: one-pass all-reduces of
- * the same type, op, stream and vector width are fused into one kernel launch (each
- * keeping its own block order, so the bits equal separate calls); a launch holds as many
- * as its 32 KiB parameter block fits: 32,496 / (40 + 16 N) of them, 193 at N = 8, and a
- * larger batch takes several launches.  Every other call is enqueued as its own launch,
+ * this communicator is recorded (its pointer arrays copied) and nothing is enqueued.  An
+ * all-reduce is checked at the call, so its argument errors are returned there; the other
+ * collectives return vSuccess and are checked when vcommGroupEnd enqueues them.
+ * vcommGroupEnd enqueues the recorded calls: one-pass all-reduces of the same type, op,
+ * stream and vector width are fused into one kernel launch (each keeping its own block
+ * order, so the bits equal separate calls); a launch holds as many as its 32 KiB
+ * parameter block fits, 32,496 / (40 + 16 N) of them (193 at N = 8), and a larger batch
+ * takes several launches.  Every other call is enqueued as its own launch,
  * in call order.  Calls in one group must not depend on each other's results.  Groups
  * nest; only the outermost end enqueues.  vcommGroupEnd returns the first error of the
  * recorded calls, or vInvalidUsage without a matching start.  The work table travels in

@@ -196,13 +196,22 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         // accesses; measured on GB300 (8 ranks x 64 MiB fp32) it is 8-10 % slower.  It
         // stays selectable (persistentGrid) for comparison.
         p->proto = q->proto == vProtoAuto ? vProtoSimple : q->proto;
+        // Reductions: smaller CTAs fit more threads on an SM beside a kernel's registers
+        // (the 8-rank 32-byte reduce-scatter keeps 84: one 512-thread CTA per SM, but six of
+        // 128 threads).  Measured on GB300, 128-thread CTAs take the 8-rank FSDP bucket's
+        // reduce-scatter from 0.93 to 0.99 of the copy bandwidth, and 256-thread CTAs gain
+        // 1-2 % for all-reduce below 64 MiB per rank.  The persistent shape keeps 512.
         p->threadsPerCta = vc::kOnePassThreads;
+        if (!q->persistentGrid) {
+            if (q->coll == vCollReduceScatter) p->threadsPerCta = 128;
+            else if (q->coll == vCollAllReduce || q->coll == vCollReduce) p->threadsPerCta = 256;
+        }
         // One resident wave (the persistent shape, and the cap for small work): rounded down
         // so it never spills into a second, mostly idle wave.  The 32-byte reduction kernels
-        // hold up to 128 registers, one 512-thread CTA per SM; the copies fit two.
+        // hold up to 128 registers, 512 threads per SM; the copies fit twice that.
         const bool wide = p->vecBytes == 32 && (q->coll == vCollAllReduce || q->coll == vCollReduceScatter ||
                                                 q->coll == vCollReduce);
-        const int target = (wide ? 1 : 2) * smCount;
+        const int target = (wide ? 1 : 2) * smCount * (vc::kOnePassThreads / p->threadsPerCta);
         int per = std::max(1, target / q->nChannels);
         // Never more CTAs than a channel has work items: for the reductions a work item is
         // one thread's unit (a vector of every rank), for the copies a tile.

@@ -165,9 +165,9 @@ def test_traffic_and_bus_factor():
 def test_32_byte_vectors_when_blocks_and_pointers_allow():
     # B = 2M fp32 elements (8 MiB): a multiple of 32 bytes
     p = plan(count=16 << 20, aligned32=1)
-    # flat grid: one 512-thread CTA per 512 vectors of every rank (2M / 8 / 512 = 512 per
+    # flat grid: one 256-thread CTA per 256 vectors of every rank (2M / 8 / 256 = 1024 per
     # block, 8 blocks); the persistent grid is one 512-thread CTA per SM
-    assert p.vecBytes == 32 and p.gridCtas == 4096
+    assert p.vecBytes == 32 and p.threadsPerCta == 256 and p.gridCtas == 8192
     assert plan(count=16 << 20, aligned32=1, persistentGrid=1).gridCtas == 152
     assert plan(count=16 << 20, aligned32=0).vecBytes == 16
     # B = alignUp(513, 4) = 516 elements = 2064 bytes: 16-byte blocks only
@@ -196,13 +196,16 @@ def test_fanout_copies_use_tma_bulk_copies_when_blocks_allow():
 
 
 def test_flat_grid_covers_the_work_once_and_persistent_grid_is_one_wave():
-    # flat (default): one 512-thread CTA per 512 units (a 16-byte vector of every rank)
+    # flat (default): one 256-thread CTA per 256 units (a 16-byte vector of every rank)
     p = plan(count=16 << 20, nChannels=1)
-    assert p.vecBytes == 16 and p.gridCtas == (16 << 20) // 4 // 512
+    assert p.vecBytes == 16 and p.threadsPerCta == 256 and p.gridCtas == (16 << 20) // 4 // 256
     p = plan(count=16 << 20, nChannels=32)
     assert p.nChannels * p.ctasPerChannel == p.gridCtas
-    assert p.ctasPerChannel * 512 * 4 >= (16 << 20) // 32              # every unit has a thread
-    assert (p.ctasPerChannel - 1) * 512 * 4 < (16 << 20) // 32         # and no CTA is idle
+    assert p.ctasPerChannel * 256 * 4 >= (16 << 20) // 32              # every unit has a thread
+    assert (p.ctasPerChannel - 1) * 256 * 4 < (16 << 20) // 32         # and no CTA is idle
+    # reduce-scatter: 128-thread CTAs
+    p = plan(coll=V.vCollReduceScatter, count=2 << 20, aligned32=1)
+    assert p.threadsPerCta == 128 and p.gridCtas == (16 << 20) // 8 // 128
     # persistent: about two resident 512-thread CTAs per SM, one wave, nearly full
     p = plan(count=16 << 20, nChannels=1, persistentGrid=1)
     assert p.gridCtas == 2 * 152
@@ -259,9 +262,9 @@ def test_small_work_spreads_over_more_smaller_ctas():
     # 256 KiB: 8192 units -> 64-thread CTAs (128 of them, still fewer than the 152 SMs at 128)
     p = plan(count=65536, aligned32=1)
     assert p.threadsPerCta == 64 and p.gridCtas == 128
-    # enough work for every SM at 512 threads: unchanged
+    # enough work for every SM: the all-reduce's default 256-thread CTAs
     p = plan(count=16 << 20, aligned32=1)
-    assert p.threadsPerCta == 512
+    assert p.threadsPerCta == 256
     # copies: tiles shrink to 2 KiB and CTAs to tile / 32 threads until every SM has a tile
     p = plan(coll=V.vCollAllGather, count=1024, aligned32=1, noBulkCopy=1)     # 4 KiB blocks
     assert p.tileBytes == 2048 and p.threadsPerCta == 64 and p.gridCtas == 2 * 8

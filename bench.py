@@ -453,6 +453,14 @@ def other_workloads(torch, V, dev, stream, hbm):
     rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
     t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
     rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    # the 16-bit and integer all-reduce paths on the same 64 MiB per rank
+    for dt, op, name in ((torch.bfloat16, "sum", "bf16_sum"), (torch.float16, "max", "fp16_max"),
+                         (torch.int32, "prod", "int32_prod")):
+        xs16 = [t_.view(dt) for t_ in x]
+        ys16 = [t_.view(dt) for t_ in y]
+        cnt16 = xs16[0].numel()
+        t = tm(lambda: V.vAllReduce(xs16, ys16, cnt16, dt, op, comm, stream))
+        rec(f"allreduce_{name}_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, 2 * f1)
     # the staged ring's own reduce-scatter and all-gather (Simple, 32 channels, 1 MiB chunks)
     ring = V.vcommInit(n, 32, V.vProtoSimple)
     V.vcommSetAlgo(ring, "ring")

@@ -453,6 +453,16 @@ def other_workloads(torch, V, dev, stream, hbm):
     rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
     t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
     rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    # rooted collectives: reduce to rank 0, gather to rank 0 (8 MiB sent per rank), scatter
+    # from rank 0 (8 MiB received per rank)
+    out0 = [y[0]] + [None] * (n - 1)
+    t = tm(lambda: V.vReduce(x, out0, COUNT, torch.float32, "sum", 0, comm, stream))
+    rec("reduce_fp32_64MiB", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    t = tm(lambda: V.vGather(part, out0, COUNT // n, torch.float32, 0, comm, stream))
+    rec("gather_fp32_64MiB", t, 2 * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    src0 = [x[0]] + [None] * (n - 1)
+    t = tm(lambda: V.vScatter(src0, part, COUNT // n, torch.float32, 0, comm, stream))
+    rec("scatter_fp32_64MiB", t, 2 * BYTES_PER_RANK, BYTES_PER_RANK, f1)
     # the 16-bit and integer all-reduce paths on the same 64 MiB per rank
     for dt, op, name in ((torch.bfloat16, "sum", "bf16_sum"), (torch.float16, "max", "fp16_max"),
                          (torch.int32, "prod", "int32_prod")):

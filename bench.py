@@ -409,6 +409,13 @@ def other_workloads(torch, V, dev, stream, hbm):
         out[name] = {"us": t * 1e6, "min_bytes": nbytes, "hbm_frac": nbytes / t / 1e9 / hbm,
                      "busbw_gbs": bytes_per_rank / t * factor / 1e9}
 
+    def literal(row, nbytes, t):
+        # The staged ring's own traffic: every block of input read once and of output
+        # written once, plus a FIFO slot written and read at every hop -- (6N-4)·S for an
+        # all-reduce, (3N-1)·S for reduce-scatter and all-gather (S = bytes per rank).
+        row["literal_bytes"] = nbytes
+        row["literal_frac"] = nbytes / t / 1e9 / hbm
+
     n = N_RANKS
     f1 = (n - 1) / n
     # FSDP bucket: bf16 25 MiB per rank, reduce-scatter * 1/8 -> fp32, then all-gather
@@ -477,8 +484,13 @@ def other_workloads(torch, V, dev, stream, hbm):
     V.vcommSetChunkBytes(ring, 1 << 20)
     t = tm(lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", ring, stream), 10)
     rec("ring_reduce_scatter_fp32_64MiB_simple_32ch", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    literal(out["ring_reduce_scatter_fp32_64MiB_simple_32ch"], (3 * n - 1) * BYTES_PER_RANK, t)
     t = tm(lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", ring, stream), 10)
     rec("ring_allgather_fp32_64MiB_simple_32ch", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    literal(out["ring_allgather_fp32_64MiB_simple_32ch"], (3 * n - 1) * BYTES_PER_RANK, t)
+    t = tm(lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 10)
+    rec("ring_allreduce_fp32_64MiB_simple_32ch", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, 2 * f1)
+    literal(out["ring_allreduce_fp32_64MiB_simple_32ch"], (6 * n - 4) * BYTES_PER_RANK, t)
     V.vcommDestroy(ring)
     tree = V.vcommInit(n, 1, V.vProtoSimple)
     V.vcommSetAlgo(tree, "tree")

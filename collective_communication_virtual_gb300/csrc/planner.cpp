@@ -56,12 +56,12 @@ struct RingFit {
     double busBytesPerUs[3];
 };
 const RingFit kRingFit[3] = {                                // calibrate.py prints these
-    {{41.0, 37.3, 38.8}, {14825.4, 95615.7, 190124.4}},     // Simple
-    {{32.8, 36.3, 37.2}, {6824.5, 49527.8, 107635.9}},      // LL
-    {{51.6, 52.3, 52.7}, {8464.4, 58441.0, 115475.4}},      // LL128
+    {{39.1, 37.1, 37.6}, {14987.1, 103612.9, 246451.2}},    // Simple
+    {{29.7, 27.2, 27.7}, {7345.8, 44947.7, 128509.1}},      // LL
+    {{49.2, 43.2, 44.9}, {8382.1, 62053.3, 134930.9}},      // LL128
 };
 const double kOnePassLatUs = 1.5;
-const double kOnePassBytesPerUs = 7.107e6;                   // minimum bytes / (time - latency)
+const double kOnePassBytesPerUs = 7.097e6;                   // minimum bytes / (time - latency)
 
 double interp_ch(const double v[3], int ch) {
     const double x = ch <= 1 ? 0.0 : (ch >= 32 ? 5.0 : std::log2((double)ch));
@@ -100,7 +100,6 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     const size_t VE = 16 / esz;
     const size_t count = q->count;
     const int smCount = q->smCount > 0 ? q->smCount : 152;
-    const size_t l2 = q->l2Bytes > 0 ? q->l2Bytes : (size_t)126 << 20;
 
     // ---- blocks -----------------------------------------------------------------------
     size_t B = 0;          // elements per rank block
@@ -281,8 +280,12 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     p->proto = proto;
     size_t chunk = q->chunkBytes;
     if (chunk == 0) {
-        // Keep all FIFOs (2 chunks per (channel, rank)) within half of L2.
-        const size_t fit = l2 / 2 / (2 * (size_t)q->nChannels * (size_t)N);
+        // 1 MiB chunks, or smaller so that all FIFOs (2 chunks per (channel, rank)) stay
+        // within 1 GiB.  Measured on GB300, large chunks win even when the FIFOs overflow L2:
+        // a ring moves its literal bytes at 0.87 of the copy rate once the per-slot handshake
+        // is amortised, while L2-sized chunks (64-128 KiB at 32 channels) spend the time in
+        // that handshake (8 x 64 MiB, 32 channels: 484 against 644 us for Simple).
+        const size_t fit = ((size_t)1 << 30) / (2 * (size_t)q->nChannels * (size_t)N);
         chunk = std::min<size_t>((size_t)1 << 20, std::max<size_t>(16384, pow2_floor(fit)));
     }
     const size_t slotBytes = chunk / vc::kChunkSlots;   // >= 1 KiB, a multiple of 256

@@ -350,14 +350,22 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
         // A captured launch replays with the arguments it was captured with, so it cannot
         // carry a fresh epoch: the graph clears the control words before every replay and
         // uses epoch 1, which eager launches never use.  LL and LL128 keep their flags in
-        // the FIFO lines, so for them the graph clears the FIFOs too; Simple data is
-        // ordered by the counters alone.  FIFOs cannot be allocated during capture: an
-        // eager ring call of at least this size must come first.
+        // the FIFO lines, so for them the graph also clears the part of every slot that
+        // this transfer can write (its largest per-channel step, in wire bytes); Simple
+        // data is ordered by the counters alone.  FIFOs cannot be allocated during capture:
+        // an eager ring call of at least this size must come first.
         const size_t need = (size_t)c->nChannels * c->nRanks * p.fifoBytes;
         if (!c->ctrl || need > c->fifoCap) return vInvalidUsage;
         const size_t ctrlBytes = (size_t)c->nChannels * c->nRanks * vc::kCtrlStride * sizeof(unsigned long long);
         e = cudaMemsetAsync(c->ctrl, 0, ctrlBytes, stream);
-        if (e == cudaSuccess && p.proto != vProtoSimple) e = cudaMemsetAsync(c->fifo, 0, need, stream);
+        if (e == cudaSuccess && p.proto != vProtoSimple) {
+            const size_t esz = elem_size(dt);
+            const size_t payload = std::min(p.slotPayloadElems, std::max<size_t>(1, p.channelElems)) * esz;
+            size_t wire = p.proto == vProtoLL ? (payload + 7) / 8 * 16 : (payload + 119) / 120 * 128;
+            wire = std::min(p.slotBytes, (wire + 127) / 128 * 128);
+            e = cudaMemset2DAsync(c->fifo, p.slotBytes, 0, wire,
+                                  (size_t)c->nChannels * c->nRanks * vc::kFifoSlots, stream);
+        }
         if (e != cudaSuccess) return cuda_fail(c, e, "cudaMemsetAsync(capture)");
         epoch = 1;
     } else {

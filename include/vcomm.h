@@ -300,7 +300,8 @@ typedef struct {
     size_t chunkBytes;         /* ring chunk bytes per rank (0 = default) */
     int aligned16;             /* 1 if every buffer pointer is 16-byte aligned */
     int smCount;               /* streaming multiprocessors of the device */
-    size_t l2Bytes;            /* L2 cache size of the device */
+    size_t l2Bytes;            /* L2 cache size of the device (kept for callers; the current
+                                  plans do not depend on it) */
     int aligned32;             /* 1 if every buffer pointer is 32-byte aligned */
     int noBulkCopy;            /* 1: never use TMA bulk copies (a communicator sets it unless
                                   VCOMM_COPY_TMA=1) */

@@ -164,8 +164,8 @@ cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, 
 // Bulk-copy (TMA) all-gather / gather / broadcast: blocks must be 16-byte aligned and a
 // multiple of 16 bytes.  Grid: up to 3 single-warp CTAs per SM (64 KiB of stages each).
 constexpr int kTmaCtasPerSm = 3;
-cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast, int grid, Status* st,
-                              volatile Status* stHost, cudaStream_t s);
+cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast, int grid, int stages,
+                              Status* st, volatile Status* stHost, cudaStream_t s);
 cudaError_t launch_scatter_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                    int threads, cudaStream_t s);
 cudaError_t launch_alltoallv(const A2AvArgs& a, int grid, int threads, cudaStream_t s);

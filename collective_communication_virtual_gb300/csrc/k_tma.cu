@@ -72,6 +72,7 @@ struct TmaJob {
     int nBlocks;
     size_t blockBytes;               // bytes per block (a multiple of 16)
     size_t dstStride;                // destination offset between blocks
+    int stages;                      // shared-memory tile stages (1..kTmaStages)
 };
 
 __device__ __forceinline__ void tile_of(const TmaJob& j, size_t tilesPerBlock, size_t t, int* s,
@@ -82,13 +83,17 @@ __device__ __forceinline__ void tile_of(const TmaJob& j, size_t tilesPerBlock, s
     *bytes = (uint32_t)min((size_t)kTmaTileBytes, j.blockBytes - *off);
 }
 
-constexpr size_t kTmaSmemBytes = (size_t)kTmaStages * kTmaTileBytes + kTmaStages * sizeof(uint64_t);
+constexpr size_t tma_smem_bytes(int stages) {
+    return (size_t)stages * kTmaTileBytes + (size_t)stages * sizeof(uint64_t);
+}
+constexpr size_t kTmaSmemBytes = tma_smem_bytes(kTmaStages);
 
 __device__ void tma_fanout(const TmaJob& j, Status* st, volatile Status* stHost) {
-    // dynamic shared memory: kTmaStages tiles, then one mbarrier per stage
+    // dynamic shared memory: j.stages tiles, then one mbarrier per stage
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char (*stage)[kTmaTileBytes] = reinterpret_cast<unsigned char (*)[kTmaTileBytes]>(smem);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)kTmaStages * kTmaTileBytes);
+    const int S = j.stages;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)S * kTmaTileBytes);
     if (threadIdx.x != 0) return;
     const size_t tilesPerBlock = (j.blockBytes + kTmaTileBytes - 1) / kTmaTileBytes;
     const size_t nTiles = tilesPerBlock * (size_t)j.nBlocks;
@@ -96,26 +101,26 @@ __device__ void tma_fanout(const TmaJob& j, Status* st, volatile Status* stHost)
     const size_t first = blockIdx.x;
     if (first >= nTiles) return;
     const size_t mine = (nTiles - first + gridDim.x - 1) / gridDim.x;
-    for (int b = 0; b < kTmaStages; b++) mbar_init(&bar[b], 1);
+    for (int b = 0; b < S; b++) mbar_init(&bar[b], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
     auto issue_load = [&](size_t k) {
         const size_t t = first + k * gridDim.x;
         int s; size_t off; uint32_t bytes;
         tile_of(j, tilesPerBlock, t, &s, &off, &bytes);
-        const int b = (int)(k % kTmaStages);
+        const int b = (int)(k % S);
         mbar_expect_tx(&bar[b], bytes);
         bulk_load(stage[b], j.src[s] + off, bytes, &bar[b]);
     };
-    const size_t pre = min((size_t)kTmaStages, mine);
+    const size_t pre = min((size_t)S, mine);
     for (size_t k = 0; k < pre; k++) issue_load(k);
     size_t issued = pre;
 
     bool failed = false;
     size_t k = 0;
     for (; k < mine; k++) {
-        const int b = (int)(k % kTmaStages);
-        const uint32_t parity = (uint32_t)((k / kTmaStages) & 1);
+        const int b = (int)(k % S);
+        const uint32_t parity = (uint32_t)((k / S) & 1);
         if (!mbar_try_wait(&bar[b], parity)) {
             const unsigned long long t0 = global_timer_ns();
             while (!mbar_try_wait(&bar[b], parity)) {
@@ -132,10 +137,18 @@ __device__ void tma_fanout(const TmaJob& j, Status* st, volatile Status* stHost)
         tile_of(j, tilesPerBlock, t, &s, &off, &bytes);
         for (int d = 0; d < j.ndst; d++) bulk_store(j.dst[d] + (size_t)s * j.dstStride + off, stage[b], bytes);
         bulk_commit();
-        // refill the stage of the previous tile once its stores have read it
-        if (k >= 1 && k - 1 + kTmaStages < mine) {
+        // Refill a stage once the stores that read it are done: with one stage, this
+        // tile's own (then tile k + 1 goes in); otherwise the previous tile's, so this
+        // tile's stores stay in flight (then tile k - 1 + S goes in).
+        if (S == 1) {
+            if (k + 1 < mine) {
+                bulk_wait_read<0>();
+                issue_load(k + 1);
+                issued++;
+            }
+        } else if (k >= 1 && k - 1 + S < mine) {
             bulk_wait_read<1>();
-            issue_load(k - 1 + kTmaStages);
+            issue_load(k - 1 + S);
             issued++;
         }
     }
@@ -144,8 +157,8 @@ __device__ void tma_fanout(const TmaJob& j, Status* st, volatile Status* stHost)
         // Loads still in flight target shared memory that is released when the CTA exits:
         // give each a bounded wait before returning.
         for (size_t q = k; q < issued; q++) {
-            const int b = (int)(q % kTmaStages);
-            const uint32_t parity = (uint32_t)((q / kTmaStages) & 1);
+            const int b = (int)(q % S);
+            const uint32_t parity = (uint32_t)((q / S) & 1);
             const unsigned long long t0 = global_timer_ns();
             while (!mbar_try_wait(&bar[b], parity) && global_timer_ns() - t0 < kWaitNs) {
             }
@@ -156,9 +169,10 @@ __device__ void tma_fanout(const TmaJob& j, Status* st, volatile Status* stHost)
 // All-gather (outRoot < 0) or gather (outRoot = root): blocks s = send[s], sc elements,
 // land at recv[r] + s * sc.  Broadcast: one block send[root] to every recv[r].
 __global__ void __launch_bounds__(32) k_fanout_tma(const __grid_constant__ OnePassArgs a, int esz, int isBroadcast,
-                                                  Status* st, Status* stHost) {
+                                                  int stages, Status* st, Status* stHost) {
     pdl_begin();
     TmaJob j;
+    j.stages = stages;
     const char* const* sends = (const char* const*)a.send;
     j.dst = a.outRoot >= 0 ? (char* const*)&a.recv[a.outRoot] : (char* const*)a.recv;
     j.ndst = a.outRoot >= 0 ? 1 : a.nRanks;
@@ -176,8 +190,9 @@ __global__ void __launch_bounds__(32) k_fanout_tma(const __grid_constant__ OnePa
     tma_fanout(j, st, stHost);
 }
 
-cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast, int grid, Status* st,
-                              volatile Status* stHost, cudaStream_t s) {
+cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast, int grid, int stages,
+                              Status* st, volatile Status* stHost, cudaStream_t s) {
+    if (stages < 1 || stages > kTmaStages) return cudaErrorInvalidValue;
     // The shared-memory limit is an attribute of the function on each device: set it once
     // per device (bit d of the mask).
     static std::atomic<unsigned long long> attrSet{0};
@@ -190,8 +205,8 @@ cudaError_t launch_fanout_tma(const OnePassArgs& a, int elemSize, bool broadcast
         if (e != cudaSuccess) return e;
         attrSet.fetch_or(bit);
     }
-    return pdl_launch(k_fanout_tma, grid, 32, kTmaSmemBytes, s, a, elemSize, broadcast ? 1 : 0, st,
-                      (Status*)stHost);
+    return pdl_launch(k_fanout_tma, grid, 32, tma_smem_bytes(stages), s, a, elemSize, broadcast ? 1 : 0,
+                      stages, st, (Status*)stHost);
 }
 
 }  // namespace vc

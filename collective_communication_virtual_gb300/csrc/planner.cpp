@@ -256,14 +256,18 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         else
             per = (int)std::min<size_t>((size_t)vc::kMaxGridCtas / (size_t)q->nChannels, maxPer);
         // Fan-out copies (all-gather, gather, broadcast) through TMA bulk copies: 16 KiB
-        // tiles through shared memory, single-warp CTAs, up to 3 per SM.
+        // tiles through shared memory, single-warp CTAs.
         const bool fanout = q->coll == vCollAllGather || q->coll == vCollGather || q->coll == vCollBroadcast;
         if (fanout && vec && q->noBulkCopy == 0 && (B * esz) % 16 == 0 && q->nChannels >= 1) {
             const size_t blocks = q->coll == vCollBroadcast ? 1 : (size_t)N;
             const size_t tiles = div_up(B * esz, (size_t)16 * 1024) * blocks;
             p->bulkCopy = 1;
             p->nChannels = 1;
-            p->ctasPerChannel = (int)std::min<size_t>((size_t)vc::kTmaCtasPerSm * smCount, tiles);
+            // Flat: one 16 KiB tile per single-stage CTA (about 13 resident per SM), handed
+            // out in order.  Persistent: three 4-stage CTAs per SM striding over the tiles.
+            p->tmaStages = q->persistentGrid ? 4 : 1;
+            p->ctasPerChannel = q->persistentGrid ? (int)std::min<size_t>((size_t)vc::kTmaCtasPerSm * smCount, tiles)
+                                                  : (int)std::min<size_t>((size_t)vc::kMaxGridCtas, tiles);
             p->gridCtas = p->ctasPerChannel;
             p->threadsPerCta = 32;
             return vSuccess;

@@ -842,7 +842,7 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
     vc::OnePassArgs a;
     fill_onepass(&a, c, send, recv, p, sendcount);
     if (p.bulkCopy)
-        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, c->statusDev,
+        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, p.tmaStages, c->statusDev,
                                                       c->statusHostDev, stream), stream, "allgather", true);
     return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "allgather");
@@ -875,7 +875,7 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
     fill_onepass(&a, c, send, recv, p, count);
     a.root = root;
     if (p.bulkCopy)
-        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), true, p.gridCtas, c->statusDev,
+        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), true, p.gridCtas, p.tmaStages, c->statusDev,
                                                       c->statusHostDev, stream), stream, "broadcast", true);
     return finish_launch(c, vc::launch_broadcast_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "broadcast");
@@ -949,7 +949,7 @@ vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, 
     fill_onepass(&a, c, send, recv, p, sendcount);
     a.outRoot = root;
     if (p.bulkCopy)
-        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, c->statusDev,
+        return finish_launch(c, vc::launch_fanout_tma(a, (int)elem_size(dt), false, p.gridCtas, p.tmaStages, c->statusDev,
                                                       c->statusHostDev, stream), stream, "gather", true);
     return finish_launch(c, vc::launch_allgather_onepass(a, (int)elem_size(dt), p.vecBytes, p.gridCtas,
                                                          p.threadsPerCta, stream), stream, "gather");

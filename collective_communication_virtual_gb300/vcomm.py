@@ -57,7 +57,7 @@ class vPlanInfo_t(ctypes.Structure):
                 ("slotPayloadElems", ctypes.c_size_t), ("slotBytes", ctypes.c_size_t),
                 ("fifoBytes", ctypes.c_size_t), ("minBytes", ctypes.c_double),
                 ("busFactor", ctypes.c_double), ("vecBytes", ctypes.c_int), ("bulkCopy", ctypes.c_int),
-                ("predictedUs", ctypes.c_double), ("tileBytes", ctypes.c_size_t)]
+                ("predictedUs", ctypes.c_double), ("tileBytes", ctypes.c_size_t), ("tmaStages", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

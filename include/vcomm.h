@@ -331,6 +331,7 @@ typedef struct {
     int bulkCopy;              /* 1: all-gather / gather / broadcast through TMA bulk copies */
     double predictedUs;        /* the planner's cost model for this plan (GB300 fit) */
     size_t tileBytes;          /* copies (load/store path): bytes each CTA moves per tile */
+    int tmaStages;             /* bulk-copy fan-out: shared-memory tile stages per CTA */
 } vPlanInfo_t;
 
 /* Compute the plan a collective with these parameters would run.  Pure host

@@ -182,7 +182,11 @@ def test_32_byte_vectors_when_blocks_and_pointers_allow():
 
 def test_fanout_copies_use_tma_bulk_copies_when_blocks_allow():
     p = plan(coll=V.vCollAllGather, count=1 << 21)                   # 8 MiB blocks
-    assert p.bulkCopy == 1 and p.threadsPerCta == 32 and p.gridCtas == 3 * 152
+    # flat: one 16 KiB tile per single-stage CTA (512 tiles per block, 8 blocks)
+    assert p.bulkCopy == 1 and p.threadsPerCta == 32 and p.tmaStages == 1 and p.gridCtas == 4096
+    # persistent: three 4-stage CTAs per SM
+    p = plan(coll=V.vCollAllGather, count=1 << 21, persistentGrid=1)
+    assert p.bulkCopy == 1 and p.tmaStages == 4 and p.gridCtas == 3 * 152
     p = plan(coll=V.vCollBroadcast, count=4096)                      # 16 KiB: one tile
     assert p.bulkCopy == 1 and p.gridCtas == 1
     assert plan(coll=V.vCollGather, count=1 << 20).bulkCopy == 1

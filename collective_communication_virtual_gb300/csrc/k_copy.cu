@@ -9,7 +9,7 @@
 
 namespace vc {
 
-// The copy kernels deal tiles (16, 32 or 64 KiB, 128 bytes per thread, chosen by the
+// The copy kernels deal tiles (2 to 64 KiB, and CTAs of 64 to 512 threads, chosen by the
 // planner) of a channel's block ranges to the channel's CTAs round-robin -- with the
 // default flat grid, one tile per CTA: tile t covers elements [lo + k*T, lo + (k+1)*T) of
 // block p = t / tilesPerBlock.

@@ -180,6 +180,24 @@ def test_32_byte_vectors_when_blocks_and_pointers_allow():
     assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1, persistentGrid=1).gridCtas == 2 * 152
 
 
+def test_copy_threads_follow_how_often_a_loaded_byte_is_stored():
+    # 8 MiB blocks, 8 ranks: 32 KiB tiles.  All-gather and broadcast store every loaded byte
+    # 8 times: 32 bytes of a tile per thread (capped at 512 threads).  Gather, scatter and
+    # all-to-all store it once: 128 bytes per thread.
+    for coll in (V.vCollAllGather, V.vCollBroadcast):
+        p = plan(coll=coll, count=1 << 21, aligned32=1, noBulkCopy=1)
+        assert p.threadsPerCta == 512
+    for coll in (V.vCollGather, V.vCollScatter):
+        p = plan(coll=coll, count=1 << 21, aligned32=1, noBulkCopy=1)
+        assert p.tileBytes == 32768 and p.threadsPerCta == 256 and p.gridCtas == 2048
+    # all-to-all, 4 MiB per rank: 64 blocks of 512 KiB -> 16 KiB tiles of 128 threads
+    p = plan(coll=V.vCollAllToAll, count=(4 << 20) // 8 // 4, aligned32=1)
+    assert p.tileBytes == 16384 and p.threadsPerCta == 128 and p.gridCtas == 2048
+    # the persistent shape keeps 64 KiB tiles and 512-thread CTAs
+    p = plan(coll=V.vCollAllToAll, count=(4 << 20) // 8 // 4, aligned32=1, persistentGrid=1)
+    assert p.tileBytes == 65536 and p.threadsPerCta == 512
+
+
 def test_fanout_copies_use_tma_bulk_copies_when_blocks_allow():
     p = plan(coll=V.vCollAllGather, count=1 << 21)                   # 8 MiB blocks
     # flat: one 16 KiB tile per single-stage CTA (512 tiles per block, 8 blocks)

@@ -446,6 +446,16 @@ def other_workloads(torch, V, dev, stream, hbm):
     b = [torch.empty(cnt, device=dev) for _ in range(n)]
     t = tm(lambda: V.vAllToAll(a, b, cnt // n, torch.float32, "sum", comm, stream), 10)
     rec("alltoall_fp32_1GiB", t, 2 * n * cnt * 4, cnt * 4, f1)
+    # the staged ring all-reduce at 1 GiB per rank (Simple, 32 channels, 1 MiB chunks)
+    for t_ in a:
+        t_.uniform_(-1, 1)
+    ring = V.vcommInit(n, 32, V.vProtoSimple)
+    V.vcommSetAlgo(ring, "ring")
+    V.vcommSetChunkBytes(ring, 1 << 20)
+    t = tm(lambda: V.vAllReduce(a, b, cnt, torch.float32, "sum", ring, stream), 3)
+    rec("ring_allreduce_fp32_1GiB_simple_32ch", t, 2 * n * cnt * 4, cnt * 4, 2 * f1)
+    literal(out["ring_allreduce_fp32_1GiB_simple_32ch"], (6 * n - 4) * cnt * 4, t)
+    V.vcommDestroy(ring)
     del a, b
     torch.cuda.empty_cache()
     # reduce-scatter, all-gather, broadcast at 64 MiB per rank (fp32)

@@ -7,6 +7,7 @@ time (NCCL book chapter 5, ring.cc), plus the fraction of measured HBM bandwidth
 the kernel's minimum traffic (read N*S + write N*S) reaches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
+  python bench.py --workloads [--only NAME]      # the other collectives' workloads only
 
 --impl reference times the CPU oracle (the plain order-matched C implementation) on the
 host cores for the same workload.  With --gpus N > 1 (under torchrun) every GPU runs an
@@ -386,12 +387,19 @@ def e2e_allreduce(torch, V, comm, xs, dev, stream, steps):
             "results_match_device_path": consistent}
 
 
-def other_workloads(torch, V, dev, stream, hbm):
-    """Kernel time and HBM fraction of the other collectives on their workloads."""
+def other_workloads(torch, V, dev, stream, hbm, only=None):
+    """Kernel time and HBM fraction of the other collectives on their workloads.  `only`:
+    a comma-separated list of workload names to run alone (a profiler then sees few
+    launches and little memory)."""
     from collective_communication_virtual_gb300 import inputs
     comm = V.vcommInit(N_RANKS, 1, V.vProtoSimple)
     V.vcommSetAlgo(comm, "onepass")
     out = {}
+
+    chosen = None if only is None else set(only.split(","))
+
+    def want(*names):
+        return chosen is None or any(nm in chosen for nm in names)
 
     def tm(fn, steps=20):
         for _ in range(3):
@@ -419,94 +427,112 @@ def other_workloads(torch, V, dev, stream, hbm):
     n = N_RANKS
     f1 = (n - 1) / n
     # FSDP bucket: bf16 25 MiB per rank, reduce-scatter * 1/8 -> fp32, then all-gather
-    cnt, rc = 13_107_200, 13_107_200 // n
-    g = [x.to(dev) for x in inputs.normal_ranks(n, cnt, 1e-3, torch.bfloat16, 2)]
-    sh = [torch.empty(rc, device=dev) for _ in range(n)]
-    t = tm(lambda: V.vReduceScatterScaleCast(g, sh, rc, torch.bfloat16, "sum", torch.float32, 1.0 / n,
-                                             comm, stream))
-    rec("fsdp_reduce_scatter_scale_cast_bf16_25MiB", t, n * cnt * 2 + n * rc * 4, cnt * 2, f1)
-    shb = [s.to(torch.bfloat16) for s in sh]
-    t = tm(lambda: V.vAllGather(shb, g, rc, torch.bfloat16, "sum", comm, stream))
-    rec("fsdp_allgather_bf16_25MiB", t, n * rc * 2 + n * cnt * 2, cnt * 2, f1)
-    del g, sh, shb
+    if want("fsdp_reduce_scatter_scale_cast_bf16_25MiB", "fsdp_allgather_bf16_25MiB"):
+        cnt, rc = 13_107_200, 13_107_200 // n
+        g = [x.to(dev) for x in inputs.normal_ranks(n, cnt, 1e-3, torch.bfloat16, 2)]
+        sh = [torch.empty(rc, device=dev) for _ in range(n)]
+        t = tm(lambda: V.vReduceScatterScaleCast(g, sh, rc, torch.bfloat16, "sum", torch.float32, 1.0 / n,
+                                                 comm, stream))
+        rec("fsdp_reduce_scatter_scale_cast_bf16_25MiB", t, n * cnt * 2 + n * rc * 4, cnt * 2, f1)
+        shb = [s.to(torch.bfloat16) for s in sh]
+        if want("fsdp_allgather_bf16_25MiB"):
+            t = tm(lambda: V.vAllGather(shb, g, rc, torch.bfloat16, "sum", comm, stream))
+            rec("fsdp_allgather_bf16_25MiB", t, n * rc * 2 + n * cnt * 2, cnt * 2, f1)
+        del g, sh, shb
     # MoE dispatch: variable all-to-all, bf16, 8 x 4096 tokens x 4096, top-2 Zipf(1.2)
-    send, counts, sd, rd, recv_elems = inputs.moe_dispatch()
-    s_d = [x.to(dev) for x in send]
-    r_d = [torch.empty(e, dtype=torch.bfloat16, device=dev) for e in recv_elems]
-    tabs = [x.to(dev) for x in (counts, sd, rd)]
-    t = tm(lambda: V.vAllToAllv(s_d, r_d, *tabs, torch.bfloat16, comm, stream))
-    moved = int(counts.sum()) * 2
-    rec("moe_alltoallv_bf16_8x4096x4096_top2", t, 2 * moved, moved // n, f1)
-    out["moe_alltoallv_bf16_8x4096x4096_top2"]["max_recv_mib"] = max(recv_elems) * 2 / 2**20
-    del s_d, r_d
-    torch.cuda.empty_cache()
+    if want("moe_alltoallv_bf16_8x4096x4096_top2"):
+        send, counts, sd, rd, recv_elems = inputs.moe_dispatch()
+        s_d = [x.to(dev) for x in send]
+        r_d = [torch.empty(e, dtype=torch.bfloat16, device=dev) for e in recv_elems]
+        tabs = [x.to(dev) for x in (counts, sd, rd)]
+        t = tm(lambda: V.vAllToAllv(s_d, r_d, *tabs, torch.bfloat16, comm, stream))
+        moved = int(counts.sum()) * 2
+        rec("moe_alltoallv_bf16_8x4096x4096_top2", t, 2 * moved, moved // n, f1)
+        out["moe_alltoallv_bf16_8x4096x4096_top2"]["max_recv_mib"] = max(recv_elems) * 2 / 2**20
+        del s_d, r_d
+        torch.cuda.empty_cache()
     # uniform all-to-all at 1 GiB per rank
-    cnt = 1 << 28
-    a = [torch.empty(cnt, device=dev) for _ in range(n)]
-    b = [torch.empty(cnt, device=dev) for _ in range(n)]
-    t = tm(lambda: V.vAllToAll(a, b, cnt // n, torch.float32, "sum", comm, stream), 10)
-    rec("alltoall_fp32_1GiB", t, 2 * n * cnt * 4, cnt * 4, f1)
-    # the staged ring all-reduce at 1 GiB per rank (Simple, 32 channels, 1 MiB chunks)
-    for t_ in a:
-        t_.uniform_(-1, 1)
-    ring = V.vcommInit(n, 32, V.vProtoSimple)
-    V.vcommSetAlgo(ring, "ring")
-    V.vcommSetChunkBytes(ring, 1 << 20)
-    t = tm(lambda: V.vAllReduce(a, b, cnt, torch.float32, "sum", ring, stream), 3)
-    rec("ring_allreduce_fp32_1GiB_simple_32ch", t, 2 * n * cnt * 4, cnt * 4, 2 * f1)
-    literal(out["ring_allreduce_fp32_1GiB_simple_32ch"], (6 * n - 4) * cnt * 4, t)
-    V.vcommDestroy(ring)
-    del a, b
-    torch.cuda.empty_cache()
-    # reduce-scatter, all-gather, broadcast at 64 MiB per rank (fp32)
+    if want("alltoall_fp32_1GiB", "ring_allreduce_fp32_1GiB_simple_32ch"):
+        cnt = 1 << 28
+        a = [torch.empty(cnt, device=dev) for _ in range(n)]
+        b = [torch.empty(cnt, device=dev) for _ in range(n)]
+        if want("alltoall_fp32_1GiB"):
+            t = tm(lambda: V.vAllToAll(a, b, cnt // n, torch.float32, "sum", comm, stream), 10)
+            rec("alltoall_fp32_1GiB", t, 2 * n * cnt * 4, cnt * 4, f1)
+        # the staged ring all-reduce at 1 GiB per rank (Simple, 32 channels, 1 MiB chunks)
+        if want("ring_allreduce_fp32_1GiB_simple_32ch"):
+            for t_ in a:
+                t_.uniform_(-1, 1)
+            ring = V.vcommInit(n, 32, V.vProtoSimple)
+            V.vcommSetAlgo(ring, "ring")
+            V.vcommSetChunkBytes(ring, 1 << 20)
+            t = tm(lambda: V.vAllReduce(a, b, cnt, torch.float32, "sum", ring, stream), 3)
+            rec("ring_allreduce_fp32_1GiB_simple_32ch", t, 2 * n * cnt * 4, cnt * 4, 2 * f1)
+            literal(out["ring_allreduce_fp32_1GiB_simple_32ch"], (6 * n - 4) * cnt * 4, t)
+            V.vcommDestroy(ring)
+        del a, b
+        torch.cuda.empty_cache()
+    def row(name, fn, nbytes, bytes_per_rank, factor, steps=20):
+        if want(name):
+            rec(name, tm(fn, steps), nbytes, bytes_per_rank, factor)
+
+    # reduce-scatter, all-gather, broadcast, all-to-all at 64 MiB per rank (fp32)
+    S = BYTES_PER_RANK
     x = [torch.rand(COUNT, device=dev) for _ in range(n)]
     y = [torch.empty(COUNT, device=dev) for _ in range(n)]
     part = [torch.empty(COUNT // n, device=dev) for _ in range(n)]
-    t = tm(lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", comm, stream))
-    rec("reduce_scatter_fp32_64MiB", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    t = tm(lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", comm, stream))
-    rec("allgather_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    t = tm(lambda: V.vBroadcast(x, y, COUNT, torch.float32, "sum", 0, comm, stream))
-    rec("broadcast_fp32_64MiB", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    t = tm(lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream))
-    rec("alltoall_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    # rooted collectives: reduce to rank 0, gather to rank 0 (8 MiB sent per rank), scatter
-    # from rank 0 (8 MiB received per rank)
+    row("reduce_scatter_fp32_64MiB", lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", comm, stream),
+        n * S + S, S, f1)
+    row("allgather_fp32_64MiB", lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", comm, stream),
+        S + n * S, S, f1)
+    row("broadcast_fp32_64MiB", lambda: V.vBroadcast(x, y, COUNT, torch.float32, "sum", 0, comm, stream),
+        S + n * S, S, f1)
+    row("alltoall_fp32_64MiB", lambda: V.vAllToAll(x, y, COUNT // n, torch.float32, "sum", comm, stream),
+        2 * n * S, S, f1)
+    # rooted collectives: reduce to rank 0; gather to and scatter from rank 0 with 64 MiB
+    # per rank (512 MiB at the root, so the working set is far larger than L2)
     out0 = [y[0]] + [None] * (n - 1)
-    t = tm(lambda: V.vReduce(x, out0, COUNT, torch.float32, "sum", 0, comm, stream))
-    rec("reduce_fp32_64MiB", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    t = tm(lambda: V.vGather(part, out0, COUNT // n, torch.float32, 0, comm, stream))
-    rec("gather_fp32_64MiB", t, 2 * BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    src0 = [x[0]] + [None] * (n - 1)
-    t = tm(lambda: V.vScatter(src0, part, COUNT // n, torch.float32, 0, comm, stream))
-    rec("scatter_fp32_64MiB", t, 2 * BYTES_PER_RANK, BYTES_PER_RANK, f1)
+    row("reduce_fp32_64MiB", lambda: V.vReduce(x, out0, COUNT, torch.float32, "sum", 0, comm, stream),
+        n * S + S, S, f1)
+    if want("gather_fp32_8x64MiB", "scatter_fp32_8x64MiB"):
+        root = [torch.empty(n * COUNT, device=dev)] + [None] * (n - 1)
+        row("gather_fp32_8x64MiB", lambda: V.vGather(x, root, COUNT, torch.float32, 0, comm, stream),
+            2 * n * S, S, f1)
+        row("scatter_fp32_8x64MiB", lambda: V.vScatter(root, y, COUNT, torch.float32, 0, comm, stream),
+            2 * n * S, S, f1)
+        del root
     # the 16-bit and integer all-reduce paths on the same 64 MiB per rank
     for dt, op, name in ((torch.bfloat16, "sum", "bf16_sum"), (torch.float16, "max", "fp16_max"),
                          (torch.int32, "prod", "int32_prod")):
         xs16 = [t_.view(dt) for t_ in x]
         ys16 = [t_.view(dt) for t_ in y]
         cnt16 = xs16[0].numel()
-        t = tm(lambda: V.vAllReduce(xs16, ys16, cnt16, dt, op, comm, stream))
-        rec(f"allreduce_{name}_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, 2 * f1)
+        row(f"allreduce_{name}_64MiB", lambda: V.vAllReduce(xs16, ys16, cnt16, dt, op, comm, stream),
+            2 * n * S, S, 2 * f1)
     # the staged ring's own reduce-scatter and all-gather (Simple, 32 channels, 1 MiB chunks)
     ring = V.vcommInit(n, 32, V.vProtoSimple)
     V.vcommSetAlgo(ring, "ring")
     V.vcommSetChunkBytes(ring, 1 << 20)
-    t = tm(lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", ring, stream), 10)
-    rec("ring_reduce_scatter_fp32_64MiB_simple_32ch", t, n * BYTES_PER_RANK + BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    literal(out["ring_reduce_scatter_fp32_64MiB_simple_32ch"], (3 * n - 1) * BYTES_PER_RANK, t)
-    t = tm(lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", ring, stream), 10)
-    rec("ring_allgather_fp32_64MiB_simple_32ch", t, BYTES_PER_RANK + n * BYTES_PER_RANK, BYTES_PER_RANK, f1)
-    literal(out["ring_allgather_fp32_64MiB_simple_32ch"], (3 * n - 1) * BYTES_PER_RANK, t)
-    t = tm(lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 10)
-    rec("ring_allreduce_fp32_64MiB_simple_32ch", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, 2 * f1)
-    literal(out["ring_allreduce_fp32_64MiB_simple_32ch"], (6 * n - 4) * BYTES_PER_RANK, t)
+    for name, fn, nbytes, factor, lit in (
+            ("ring_reduce_scatter_fp32_64MiB_simple_32ch",
+             lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", ring, stream), n * S + S, f1, 3 * n - 1),
+            ("ring_allgather_fp32_64MiB_simple_32ch",
+             lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", ring, stream), S + n * S, f1, 3 * n - 1),
+            ("ring_allreduce_fp32_64MiB_simple_32ch",
+             lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 2 * n * S, 2 * f1, 6 * n - 4)):
+        row(name, fn, nbytes, S, factor, 10)
+        if name in out:
+            literal(out[name], lit * S, out[name]["us"] / 1e6)
     V.vcommDestroy(ring)
     tree = V.vcommInit(n, 1, V.vProtoSimple)
     V.vcommSetAlgo(tree, "tree")
-    t = tm(lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", tree, stream))
-    rec("allreduce_double_binary_tree_fp32_64MiB", t, 2 * n * BYTES_PER_RANK, BYTES_PER_RANK, 2 * f1)
+    row("allreduce_double_binary_tree_fp32_64MiB", lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", tree, stream),
+        2 * n * S, S, 2 * f1)
     V.vcommDestroy(tree)
+    del x, y, part
+    if not want("ddp_64_buckets_64KiB_fp32"):
+        V.vcommDestroy(comm)
+        return out
     # group batching: 64 gradient buckets of 64 KiB fp32, separate calls vs one group
     nb, bc = 64, 16384
     bx = [[torch.rand(bc, device=dev) for _ in range(n)] for _ in range(nb)]
@@ -683,7 +709,7 @@ def channel_sweep(torch, V, send, recv, stream):
     return out
 
 
-def run_workloads():
+def run_workloads(only=None):
     import torch
 
     from collective_communication_virtual_gb300 import build, vcomm as V
@@ -691,7 +717,7 @@ def run_workloads():
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     hbm, _ = peaks()
-    print(json.dumps({"other_workloads": other_workloads(torch, V, dev, torch.cuda.current_stream(), hbm)}))
+    print(json.dumps({"other_workloads": other_workloads(torch, V, dev, torch.cuda.current_stream(), hbm, only)}))
     return 0
 
 
@@ -705,6 +731,8 @@ def main():
     ap.add_argument("--workloads", action="store_true",
                     help="only time the other collectives (FSDP bucket, MoE dispatch, all-to-all, "
                          "reduce-scatter, all-gather, broadcast) and print them as one JSON line")
+    ap.add_argument("--only", default=None,
+                    help="with --workloads: a comma-separated list of the workload names to run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -712,7 +740,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
     if args.workloads:
-        return run_workloads()
+        return run_workloads(args.only)
     return run_ours(args)
 
 

@@ -599,6 +599,12 @@ vResult_t vcommDestroy(vcomm_t c) {
     return vSuccess;
 }
 
+vResult_t vcommCount(vcomm_t c, int* nRanks) {
+    if (!comm_ok(c) || !nRanks) return vInvalidArgument;
+    *nRanks = c->nRanks;
+    return vSuccess;
+}
+
 vResult_t vcommGetAsyncError(vcomm_t c, vResult_t* err) {
     if (!comm_ok(c) || !err) return vInvalidArgument;
     *err = sticky(c);

@@ -97,6 +97,7 @@ _SIGNATURES = {
                     ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vAllToAll": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vcommCount": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vAllToAllv": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vReduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -158,13 +159,39 @@ def _addr(x) -> int | None:
     return x.data_ptr()
 
 
-def _ptr_array(bufs):
-    """A C array of the buffers' device addresses (None for NULL)."""
+def _ptr_array(bufs, n_ranks: int):
+    """A C array of the buffers' device addresses (None for NULL).  The library reads
+    exactly n_ranks entries, so a list of another length is refused here."""
     n = len(bufs)
+    if n != n_ranks:
+        raise VcommError(vInvalidArgument, f"expected {n_ranks} buffers (one per rank), got {n}")
     arr_t = _ARRAY_TYPES.get(n)
     if arr_t is None:
         arr_t = _ARRAY_TYPES[n] = ctypes.c_void_p * n
     return arr_t(*[None if b is None else (b if isinstance(b, int) else b.data_ptr()) for b in bufs])
+
+
+_N_RANKS: dict = {}
+
+
+def _handle(comm) -> int | None:
+    return comm.value if isinstance(comm, ctypes.c_void_p) else comm
+
+
+def _n_ranks(comm) -> int:
+    """The communicator's rank count, asked of the library once per handle."""
+    key = _handle(comm)
+    n = _N_RANKS.get(key)
+    if n is None:
+        v = ctypes.c_int(0)
+        _check(lib().vcommCount(comm, ctypes.byref(v)), "vcommCount")
+        n = _N_RANKS[key] = v.value
+    return n
+
+
+def _pair(comm, sendbuffs, recvbuffs):
+    n = _n_ranks(comm)
+    return _ptr_array(sendbuffs, n), _ptr_array(recvbuffs, n)
 
 
 def _stream(stream) -> int | None:
@@ -187,11 +214,19 @@ def vcommInit(n_ranks: int, n_channels: int = 1, protocol=vProtoSimple) -> ctype
     comm = ctypes.c_void_p()
     proto = PROTOCOLS[protocol] if isinstance(protocol, str) else protocol
     _check(lib().vcommInit(ctypes.byref(comm), n_ranks, n_channels, proto), "vcommInit")
+    _N_RANKS[comm.value] = n_ranks
     return comm
 
 
 def vcommDestroy(comm) -> None:
+    _N_RANKS.pop(_handle(comm), None)
     _check(lib().vcommDestroy(comm), "vcommDestroy")
+
+
+def vcommCount(comm) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().vcommCount(comm, ctypes.byref(v)), "vcommCount")
+    return v.value
 
 
 def vcommGetAsyncError(comm) -> int:
@@ -269,55 +304,55 @@ def vPlanChannelRange(plan: vPlanInfo_t, count: int, channel: int, block: int) -
 
 
 def vAllReduce(sendbuffs, recvbuffs, count: int, datatype, op, comm, stream=None) -> None:
-    _check(lib().vAllReduce(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+    _check(lib().vAllReduce(*_pair(comm, sendbuffs, recvbuffs), count, _dtype_code(datatype),
                             _op_code(op), comm, _stream(stream)), "vAllReduce")
 
 
 def vReduceScatter(sendbuffs, recvbuffs, recvcount: int, datatype, op, comm, stream=None) -> None:
-    _check(lib().vReduceScatter(_ptr_array(sendbuffs), _ptr_array(recvbuffs), recvcount,
+    _check(lib().vReduceScatter(*_pair(comm, sendbuffs, recvbuffs), recvcount,
                                 _dtype_code(datatype), _op_code(op), comm, _stream(stream)), "vReduceScatter")
 
 
 def vReduceScatterScaleCast(sendbuffs, recvbuffs, recvcount: int, datatype, op, out_type, scale: float,
                             comm, stream=None) -> None:
-    _check(lib().vReduceScatterScaleCast(_ptr_array(sendbuffs), _ptr_array(recvbuffs), recvcount,
+    _check(lib().vReduceScatterScaleCast(*_pair(comm, sendbuffs, recvbuffs), recvcount,
                                          _dtype_code(datatype), _op_code(op), _dtype_code(out_type),
                                          ctypes.c_float(scale), comm, _stream(stream)),
            "vReduceScatterScaleCast")
 
 
 def vAllGather(sendbuffs, recvbuffs, sendcount: int, datatype, op, comm, stream=None) -> None:
-    _check(lib().vAllGather(_ptr_array(sendbuffs), _ptr_array(recvbuffs), sendcount, _dtype_code(datatype),
+    _check(lib().vAllGather(*_pair(comm, sendbuffs, recvbuffs), sendcount, _dtype_code(datatype),
                             _op_code(op), comm, _stream(stream)), "vAllGather")
 
 
 def vBroadcast(sendbuffs, recvbuffs, count: int, datatype, op, root: int, comm, stream=None) -> None:
-    _check(lib().vBroadcast(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+    _check(lib().vBroadcast(*_pair(comm, sendbuffs, recvbuffs), count, _dtype_code(datatype),
                             _op_code(op), root, comm, _stream(stream)), "vBroadcast")
 
 
 def vAllToAll(sendbuffs, recvbuffs, count: int, datatype, op, comm, stream=None) -> None:
-    _check(lib().vAllToAll(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+    _check(lib().vAllToAll(*_pair(comm, sendbuffs, recvbuffs), count, _dtype_code(datatype),
                            _op_code(op), comm, _stream(stream)), "vAllToAll")
 
 
 def vReduce(sendbuffs, recvbuffs, count: int, datatype, op, root: int, comm, stream=None) -> None:
-    _check(lib().vReduce(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+    _check(lib().vReduce(*_pair(comm, sendbuffs, recvbuffs), count, _dtype_code(datatype),
                          _op_code(op), root, comm, _stream(stream)), "vReduce")
 
 
 def vGather(sendbuffs, recvbuffs, sendcount: int, datatype, root: int, comm, stream=None) -> None:
-    _check(lib().vGather(_ptr_array(sendbuffs), _ptr_array(recvbuffs), sendcount, _dtype_code(datatype),
+    _check(lib().vGather(*_pair(comm, sendbuffs, recvbuffs), sendcount, _dtype_code(datatype),
                          root, comm, _stream(stream)), "vGather")
 
 
 def vScatter(sendbuffs, recvbuffs, recvcount: int, datatype, root: int, comm, stream=None) -> None:
-    _check(lib().vScatter(_ptr_array(sendbuffs), _ptr_array(recvbuffs), recvcount, _dtype_code(datatype),
+    _check(lib().vScatter(*_pair(comm, sendbuffs, recvbuffs), recvcount, _dtype_code(datatype),
                           root, comm, _stream(stream)), "vScatter")
 
 
 def vAllToAllv(sendbuffs, recvbuffs, counts, sdispls, rdispls, datatype, comm, stream=None) -> None:
-    _check(lib().vAllToAllv(_ptr_array(sendbuffs), _ptr_array(recvbuffs), _addr(counts), _addr(sdispls),
+    _check(lib().vAllToAllv(*_pair(comm, sendbuffs, recvbuffs), _addr(counts), _addr(sdispls),
                             _addr(rdispls), _dtype_code(datatype), comm, _stream(stream)), "vAllToAllv")
 
 
@@ -325,6 +360,6 @@ def vAllReduceNoAlloc(sendbuffs, recvbuffs, count: int, datatype, op, n_ranks: i
                       protocol=vProtoSimple, stream=None) -> None:
     """The ring all-reduce that allocates nothing (see include/vcomm.h)."""
     proto = PROTOCOLS[protocol] if isinstance(protocol, str) else protocol
-    _check(lib().vAllReduceNoAlloc(_ptr_array(sendbuffs), _ptr_array(recvbuffs), count, _dtype_code(datatype),
+    _check(lib().vAllReduceNoAlloc(_ptr_array(sendbuffs, n_ranks), _ptr_array(recvbuffs, n_ranks), count, _dtype_code(datatype),
                                    _op_code(op), n_ranks, n_channels, proto, _stream(stream)),
            "vAllReduceNoAlloc")

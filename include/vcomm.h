@@ -144,6 +144,11 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
  * A NULL or already destroyed communicator gives vInvalidArgument. */
 vResult_t vcommDestroy(vcomm_t comm);
 
+/* Store the communicator's rank count N in *nRanks: the length that every sendbuffs and
+ * recvbuffs array of a call on it must have (the communicator's nRanks field, NCCL book
+ * section 2.1).  Host only.  A NULL pointer or a bad communicator gives vInvalidArgument. */
+vResult_t vcommCount(vcomm_t comm, int* nRanks);
+
 /* Store the sticky asynchronous error (vSuccess if none) in *asyncError.  Reads host
  * memory that the kernels write; it does not synchronize any stream. */
 vResult_t vcommGetAsyncError(vcomm_t comm, vResult_t* asyncError);

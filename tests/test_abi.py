@@ -87,6 +87,30 @@ def test_null_or_garbage_comm_is_refused(lib):
         assert lib.vcommAbort(comm) == V.vInvalidArgument
         err = ctypes.c_int()
         assert lib.vcommGetAsyncError(comm, ctypes.byref(err)) == V.vInvalidArgument
+        assert lib.vcommCount(comm, ctypes.byref(err)) == V.vInvalidArgument
+
+
+def test_binding_refuses_a_buffer_list_of_the_wrong_length(monkeypatch):
+    # the library reads exactly N pointers from each array, so the binding checks the
+    # lengths against the communicator's rank count before calling it
+    calls = []
+
+    class FakeLib:
+        def vAllReduce(self, *args):
+            calls.append(args)
+            return V.vSuccess
+
+    monkeypatch.setattr(V, "lib", lambda: FakeLib())
+    monkeypatch.setitem(V._N_RANKS, 0x1234, 4)
+    comm = ctypes.c_void_p(0x1234)
+    with pytest.raises(V.VcommError) as e:
+        V.vAllReduce([1, 2, 3], [4, 5, 6, 7], 16, V.vFloat32, "sum", comm, stream=0)
+    assert e.value.code == V.vInvalidArgument and not calls
+    with pytest.raises(V.VcommError):
+        V.vAllReduce([1, 2, 3, 4], [4, 5, 6, 7, 8], 16, V.vFloat32, "sum", comm, stream=0)
+    assert not calls
+    V.vAllReduce([1, 2, 3, 4], [5, 6, 7, 8], 16, V.vFloat32, "sum", comm, stream=0)
+    assert len(calls) == 1 and list(calls[0][0]) == [1, 2, 3, 4] and list(calls[0][1]) == [5, 6, 7, 8]
 
 
 def test_error_strings(lib):

@@ -340,6 +340,10 @@ def test_invalid_arguments_launch_nothing(comms):
     with pytest.raises(V.VcommError) as e:
         V.vBroadcast(x, x, 16, torch.float32, "sum", 4, c)
     assert e.value.code == V.vInvalidArgument
+    with pytest.raises(V.VcommError) as e:        # one buffer short: refused by the binding
+        V.vAllReduce(x[:3], x[:3], 16, torch.float32, "sum", c)
+    assert e.value.code == V.vInvalidArgument
+    assert V.vcommCount(c) == 4
     odd = [torch.zeros(17, device=DEV)[1:].view(torch.int16)[1:9] for _ in range(4)]
     with pytest.raises(V.VcommError) as e:        # 2-byte aligned pointer for a 4-byte type
         V.vAllReduce(odd, odd, 4, torch.float32, "sum", c)

@@ -112,6 +112,10 @@ __device__ __forceinline__ uint16_t op_16(uint16_t a, uint16_t b) {
 // the fp32 add does not round; with a larger gap the smaller operand is below half an
 // ulp of the larger in the 16-bit type, and both routes return the larger operand.
 // (Products are not done this way: a bf16 product in the subnormal range can round twice.)
+// fp16/bf16 min and max compare both lanes at once and select bits by the lane mask.
+// The packed compare is ordered, like the widened fp32 compare of the definition, and
+// comparing two 16-bit floats gives the same answer as comparing their exact fp32
+// values: a NaN on either side keeps the running partial a, and so does a tie (-0 / +0).
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t op_word(uint32_t a, uint32_t b) {
     if (DT == kF32) return __float_as_uint(op_f32<OP>(__uint_as_float(a), __uint_as_float(b)));
@@ -123,6 +127,30 @@ __device__ __forceinline__ uint32_t op_word(uint32_t a, uint32_t b) {
     }
     if (OP == kSum && DT == kF16) {
         const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+        return *reinterpret_cast<const uint32_t*>(&r);
+    }
+    if ((OP == kMin || OP == kMax) && DT == kBF16) {
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(&b);
+        const uint32_t m = OP == kMax ? __hgt2_mask(y, x) : __hlt2_mask(y, x);
+        return (b & m) | (a & ~m);
+    }
+    if ((OP == kMin || OP == kMax) && DT == kF16) {
+        const __half2 x = *reinterpret_cast<const __half2*>(&a);
+        const __half2 y = *reinterpret_cast<const __half2*>(&b);
+        const uint32_t m = OP == kMax ? __hgt2_mask(y, x) : __hlt2_mask(y, x);
+        return (b & m) | (a & ~m);
+    }
+    if (OP == kProd) {
+        // widen each lane, one fp32 multiply per lane, then both lanes rounded back by one
+        // packed convert (round to nearest even, as narrow16 does lane by lane)
+        const float lo = __fmul_rn(widen16<DT>((uint16_t)(a & 0xFFFFu)), widen16<DT>((uint16_t)(b & 0xFFFFu)));
+        const float hi = __fmul_rn(widen16<DT>((uint16_t)(a >> 16)), widen16<DT>((uint16_t)(b >> 16)));
+        if (DT == kBF16) {
+            const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+            return *reinterpret_cast<const uint32_t*>(&r);
+        }
+        const __half2 r = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<const uint32_t*>(&r);
     }
     const uint32_t lo = op_16<DT, OP>((uint16_t)(a & 0xFFFFu), (uint16_t)(b & 0xFFFFu));

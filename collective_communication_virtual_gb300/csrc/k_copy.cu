@@ -19,6 +19,34 @@ namespace vc {
 // stores.  Only the end of a block can cut a vector short; those elements are copied one
 // by one.
 
+// Element by element: a warp copies 32 * K consecutive elements at a time, lane l taking
+// elements e0 + 32 * k, so each warp instruction is coalesced and a warp's K stores to one
+// destination cover one contiguous stretch.  A thread loads its K elements before it
+// stores any.  A plain loop could not do that: the compiler must assume a store may alias
+// the next load, so every load would wait for the previous store.
+template <int ESZ>
+__device__ __forceinline__ void elem_copy(const char* src, char* const* dst, size_t dstOff, int ndst,
+                                          size_t lo, size_t hi) {
+    constexpr int K = 8;
+    const size_t first = lo + (size_t)(threadIdx.x >> 5) * 32 * K + (threadIdx.x & 31);
+    for (size_t e0 = first; e0 < hi; e0 += (size_t)K * blockDim.x) {
+        uint32_t w[K];
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            const size_t e = e0 + 32 * (size_t)k;
+            w[k] = e < hi ? ld_elem<ESZ>(src, e) : 0u;
+        }
+        for (int d = 0; d < ndst; d++) {
+            char* o = dst[d] + dstOff * ESZ;
+#pragma unroll
+            for (int k = 0; k < K; k++) {
+                const size_t e = e0 + 32 * (size_t)k;
+                if (e < hi) st_elem<ESZ>(o, e, w[k]);
+            }
+        }
+    }
+}
+
 // Copy [lo, hi) elements from src to every dst[0..ndst) (ndst = 1 for all-to-all).
 // VB: bytes per vector (16 or 32; 0 = element by element).  A thread keeps 128 bytes of
 // loads in flight: 8 vectors of 16 bytes or 4 of 32.
@@ -47,16 +75,9 @@ __device__ __forceinline__ void tile_copy(const char* src, char* const* dst, siz
                 }
             }
         }
-        const size_t tail = lo + nv * VE;
-        for (size_t e = tail + threadIdx.x; e < hi; e += blockDim.x) {
-            const uint32_t w = ld_elem<ESZ>(src, e);
-            for (int d = 0; d < ndst; d++) st_elem<ESZ>(dst[d] + dstOff * ESZ, e, w);
-        }
+        elem_copy<ESZ>(src, dst, dstOff, ndst, lo + nv * VE, hi);
     } else {
-        for (size_t e = lo + threadIdx.x; e < hi; e += blockDim.x) {
-            const uint32_t w = ld_elem<ESZ>(src, e);
-            for (int d = 0; d < ndst; d++) st_elem<ESZ>(dst[d] + dstOff * ESZ, e, w);
-        }
+        elem_copy<ESZ>(src, dst, dstOff, ndst, lo, hi);
     }
 }
 

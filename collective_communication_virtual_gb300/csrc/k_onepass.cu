@@ -50,8 +50,32 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
     const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
-    const ChannelSpan sp = channel_span(a, ch, U);
     const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, a.blockElems);
+    const int r0 = a.outRoot >= 0 ? a.outRoot : 0;
+    const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
+    if (VB == 0) {
+        // element path: warp tiles of 32 * kElemsPerThread elements of one block
+        constexpr int TILE = 32 * kElemsPerThread;
+        const size_t lo = min((size_t)ch * a.chanElems, a.blockElems);
+        const size_t tiles = (chEnd - lo + TILE - 1) / TILE;
+        const int lane = threadIdx.x & 31;
+        for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride / 32) {
+            const int b = (int)(w / tiles);
+            const size_t base = (size_t)b * a.blockElems;
+            const size_t e0 = base + lo + (w - (size_t)b * tiles) * TILE + lane;
+            const size_t end = min(base + chEnd, a.count);
+            const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
+            uint32_t acc[kElemsPerThread];
+            reduce_elems_ring<DT, OP>(a.send, N, ob + 1 == N ? 0 : ob + 1, e0, end, acc);
+            for (int r = r0; r < r1; r++) {
+#pragma unroll
+                for (int k = 0; k < kElemsPerThread; k++)
+                    if (e0 + 32 * (size_t)k < end) st_elem<ESZ>(a.recv[r], e0 + 32 * (size_t)k, acc[k]);
+            }
+        }
+        return;
+    }
+    const ChannelSpan sp = channel_span(a, ch, U);
     const size_t total = sp.units * (size_t)N;
     for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < total; j += stride) {
         const int b = (int)(j / sp.units);
@@ -62,8 +86,6 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
         if (e >= hi) continue;
         const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
         const int first = ob + 1 == N ? 0 : ob + 1;
-        const int r0 = a.outRoot >= 0 ? a.outRoot : 0;
-        const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
         if (VB && e + U <= hi) {
             const size_t boff = e * ESZ;
             const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16, NF>(a.send, N, first, boff);
@@ -155,8 +177,27 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
     const size_t rc = a.blockElems;
     const bool hasScale = a.hasScale != 0;
-    const ChannelSpan sp = channel_span(a, ch, U);
     const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, rc);
+    if (VB == 0) {
+        // element path: warp tiles of 32 * kElemsPerThread elements of one block
+        constexpr int TILE = 32 * kElemsPerThread;
+        const size_t lo = min((size_t)ch * a.chanElems, rc);
+        const size_t tiles = (chEnd - lo + TILE - 1) / TILE;
+        const int lane = threadIdx.x & 31;
+        for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride / 32) {
+            const int r = (int)(w / tiles);
+            const size_t t0 = lo + (w - (size_t)r * tiles) * TILE + lane;    // element within block r
+            const size_t base = (size_t)r * rc;
+            uint32_t acc[kElemsPerThread];
+            reduce_elems_ring<DT, OP>(a.send, N, r + 1 == N ? 0 : r + 1, base + t0, base + chEnd, acc);
+#pragma unroll
+            for (int k = 0; k < kElemsPerThread; k++)
+                if (t0 + 32 * (size_t)k < chEnd)
+                    store_epilogue_elem<DT, OUT>(a.recv[r], t0 + 32 * (size_t)k, acc[k], hasScale, a.scale);
+        }
+        return;
+    }
+    const ChannelSpan sp = channel_span(a, ch, U);
     const size_t total = sp.units * (size_t)N;
     for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < total; j += stride) {
         const int r = (int)(j / sp.units);

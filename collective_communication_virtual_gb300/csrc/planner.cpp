@@ -220,7 +220,9 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         } else {
             const size_t chElems = std::min(p->channelElems, B);
             if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter || q->coll == vCollReduce) {
-                const size_t unit = p->vecBytes ? p->vecBytes / esz : 1;
+                // a thread's unit: one vector of every rank, or on the element path 8
+                // elements of every rank (32 of a warp's lanes times 8 per warp tile)
+                const size_t unit = p->vecBytes ? p->vecBytes / esz : 8;
                 const size_t units = div_up(chElems, unit) * (size_t)N;
                 // Small work: smaller CTAs (down to 64 threads) spread it over more SMs
                 // instead of loading a few SMs with 512 threads each.

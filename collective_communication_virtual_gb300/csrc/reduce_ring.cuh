@@ -47,6 +47,48 @@ __device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const void* con
     return acc;
 }
 
+// Element path (pointers or blocks that 16-byte vectors cannot cover): a warp reduces 32*K
+// consecutive elements, lane l taking elements e0 + 32*k (k < K, e0 = tile start + l), so
+// every load and store instruction of the warp is coalesced.  The K elements of up to four
+// ranks are loaded before any is folded: plain element loads cannot be moved past the
+// stores by the compiler, so one element at a time would wait out a full memory latency
+// per rank.  Elements at or beyond `end` are neither loaded nor used.
+constexpr int kElemsPerThread = 8;
+
+template <int DT, int OP>
+__device__ __forceinline__ void reduce_elems_ring(const void* const* send, int N, int first, size_t e0,
+                                                  size_t end, uint32_t (&acc)[kElemsPerThread]) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    constexpr int K = kElemsPerThread;
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        const size_t e = e0 + 32 * (size_t)k;
+        acc[k] = e < end ? ld_elem<ESZ>(send[first], e) : 0u;
+    }
+    int rk = first + 1 == N ? 0 : first + 1;
+    for (int n = 1; n < N; n += 4) {
+        uint32_t v[4][K];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (n + j < N) {
+#pragma unroll
+                for (int k = 0; k < K; k++) {
+                    const size_t e = e0 + 32 * (size_t)k;
+                    v[j][k] = e < end ? ld_elem<ESZ>(send[rk], e) : 0u;
+                }
+                rk = rk + 1 == N ? 0 : rk + 1;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (n + j < N) {
+#pragma unroll
+                for (int k = 0; k < K; k++) acc[k] = op_elem<DT, OP>(acc[k], v[j][k]);
+            }
+        }
+    }
+}
+
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t reduce_elem_ring(const void* const* send, int N, int first, size_t e) {
     constexpr int ESZ = DTypeOf<DT>::size;

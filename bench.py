@@ -35,6 +35,7 @@ METRIC = "allreduce busBW GB/s & % of HBM peak vs bytes/rank, N=8 virtual ranks,
 WORKLOAD = "ring all-reduce, sum, fp32, N=8 virtual ranks, 64 MiB per rank"
 PROFILE = os.path.join(ROOT, "profiles", "allreduce_onepass_fp32_8x64MiB.md")
 KERNEL_SOURCES = ["collective_communication_virtual_gb300/csrc/k_onepass.cu",
+                  "collective_communication_virtual_gb300/csrc/onepass.cuh",
                   "collective_communication_virtual_gb300/csrc/reduce_ring.cuh",
                   "collective_communication_virtual_gb300/csrc/device.cuh"]
 

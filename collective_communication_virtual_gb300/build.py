@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libvcomm.so")
 
-SOURCES = ["vcomm.cpp", "planner.cpp", "ring_launch.cu", "k_onepass.cu", "k_group.cu", "k_tree.cu",
+SOURCES = ["vcomm.cpp", "planner.cpp", "ring_launch.cu", "k_onepass.cu", "k_onepass_small.cu", "k_group.cu", "k_tree.cu", "k_tree_more.cu",
            "k_copy.cu", "k_ring_simple.cu", "k_ring_ll.cu", "k_ring_ll128.cu", "noalloc.cu", "k_tma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -1,302 +1,25 @@
-// k_onepass.cu -- one-pass reduction kernels: all-reduce and reduce-scatter.
-//
-// Every virtual rank's buffer is addressable from one kernel, so instead of moving
-// partials from rank to rank (2(N-1) ring steps, "NCCL book" section 2.3) each thread
-// reads element e of all N ranks once, reduces them in the ring's order, and writes the
-// result once per output: 2*N*S bytes for an all-reduce, the minimum.  This is the
-// virtual-rank form of the symmetric-memory kernels that read peers' buffers directly
-// (NCCL book chapter 5 section 5; "AI Systems Performance Engineering (3)", NVLS and
-// symmetric memory).
-//
-// Order: block b of the buffer is reduced as ranks b+1, b+2, ..., b (mod N), each partial
-// rounded to the data type -- exactly the partial a ring reduce-scatter accumulates
-// (RingARAlgorithm::getNextSendAddr: at stage s rank r handles chunk (r + N - 1 - s) mod N).
-// Channels own contiguous sub-ranges of every block (NCCL book section 2.2); a channel's
-// CTAs stride over its sub-range.  Blocks, channel ranges and 16-byte vectors all start
-// on 16-byte boundaries, so a vector never straddles two blocks.
-#include "reduce_ring.cuh"
+// k_onepass.cu -- launch of the one-pass all-reduce (and reduce to root) and reduce-scatter
+// kernels of onepass.cuh: compile-time instances for 8 ranks here, for 2 to 4 ranks in
+// k_onepass_small.cu, the run-time rank count for every other case and the element path.
+#include "onepass.cuh"
 
 namespace vc {
 
-// Per channel the work is (block, unit) pairs, flattened so that small buffers still
-// spread over all threads: unit i of block b covers elements [lo_b + i*U, lo_b + (i+1)*U)
-// with U = 16 / esz on the vector path (1 otherwise) and lo_b = b*B + ch*Lc.  Only the
-// very end of the buffer can cut a vector short; its elements go element by element.
-struct ChannelSpan {
-    size_t lo;       // first element of this channel's range in block 0
-    size_t units;    // units per block (of the full-length range)
-};
-
-__device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch, size_t unit) {
-    ChannelSpan s;
-    const size_t lo = min((size_t)ch * a.chanElems, a.blockElems);
-    const size_t hi = min((size_t)(ch + 1) * a.chanElems, a.blockElems);
-    s.lo = lo;
-    s.units = (hi - lo + unit - 1) / unit;
-    return s;
-}
-
-// All-reduce, and reduce to root.  grid = nChannels * ctasPerChannel.  VB: 0 (element
-// path), 16 or 32 bytes per vector; the 32-byte kernel keeps twice the registers, so it
-// runs one 512-thread CTA per SM instead of two.  Reduce to root (a.orderRoot = a.outRoot
-// = root) reduces every block in the root's order and writes only recv[root].
-template <int DT, int OP, int VB, int NF = 0>
-__global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
-k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
-    pdl_begin();
-    constexpr int ESZ = DTypeOf<DT>::size;
-    constexpr int U = VB ? VB / ESZ : 1;
-    const int N = NF ? NF : a.nRanks;
-    const int ch = blockIdx.x / a.ctasPerChannel;
-    const int cta = blockIdx.x - ch * a.ctasPerChannel;
-    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
-    const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, a.blockElems);
-    const int r0 = a.outRoot >= 0 ? a.outRoot : 0;
-    const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
-    if (VB == 0) {
-        // element path: warp tiles of 32 * kElemsPerThread elements of one block
-        constexpr int TILE = 32 * kElemsPerThread;
-        const size_t lo = min((size_t)ch * a.chanElems, a.blockElems);
-        const size_t tiles = (chEnd - lo + TILE - 1) / TILE;
-        const int lane = threadIdx.x & 31;
-        for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride / 32) {
-            const int b = (int)(w / tiles);
-            const size_t base = (size_t)b * a.blockElems;
-            const size_t e0 = base + lo + (w - (size_t)b * tiles) * TILE + lane;
-            const size_t end = min(base + chEnd, a.count);
-            const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
-            uint32_t acc[kElemsPerThread];
-            reduce_elems_ring<DT, OP>(a.send, N, ob + 1 == N ? 0 : ob + 1, e0, end, acc);
-            for (int r = r0; r < r1; r++) {
-#pragma unroll
-                for (int k = 0; k < kElemsPerThread; k++)
-                    if (e0 + 32 * (size_t)k < end) st_elem<ESZ>(a.recv[r], e0 + 32 * (size_t)k, acc[k]);
-            }
-        }
-        return;
-    }
-    const ChannelSpan sp = channel_span(a, ch, U);
-    const size_t total = sp.units * (size_t)N;
-    for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < total; j += stride) {
-        const int b = (int)(j / sp.units);
-        const size_t i = j - (size_t)b * sp.units;
-        const size_t base = (size_t)b * a.blockElems;
-        const size_t e = base + sp.lo + i * U;
-        const size_t hi = min(base + chEnd, a.count);
-        if (e >= hi) continue;
-        const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
-        const int first = ob + 1 == N ? 0 : ob + 1;
-        if (VB && e + U <= hi) {
-            const size_t boff = e * ESZ;
-            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16, NF>(a.send, N, first, boff);
-            if (NF && a.outRoot < 0) {
-#pragma unroll
-                for (int r = 0; r < (NF ? NF : 1); r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
-            } else {
-                for (int r = r0; r < r1; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + boff, acc);
-            }
-        } else {
-            for (size_t x = e; x < min(e + U, hi); x++) {
-                const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, x);
-                for (int r = r0; r < r1; r++) st_elem<ESZ>(a.recv[r], x, acc);
-            }
-        }
-    }
-}
-
-// Store a reduced 16-byte vector of DT elements as OUT elements, out = (float)acc * scale
-// when hasScale (or a plain store when OUT == DT and no scale).
-template <int DT, int OUT>
-__device__ __forceinline__ void store_epilogue_vec(void* outBase, size_t outElem, uint4 acc,
-                                                   bool hasScale, float scale) {
-    constexpr int ESZ = DTypeOf<DT>::size;
-    constexpr int OSZ = DTypeOf<OUT>::size;
-    if (DT == OUT && !hasScale) {
-        st_stream((char*)outBase + outElem * OSZ, acc);
-        return;
-    }
-    constexpr int VE = 16 / ESZ;
-    uint32_t w[4] = {acc.x, acc.y, acc.z, acc.w};
-    uint32_t o[VE];
-#pragma unroll
-    for (int i = 0; i < VE; i++) {
-        const uint32_t bits = ESZ == 4 ? w[i] : ((w[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
-        float f = elem_to_f32<DT>(bits);
-        if (hasScale) f = __fmul_rn(f, scale);
-        o[i] = f32_to_elem<OUT>(f);
-    }
-    if (OSZ == 4) {
-#pragma unroll
-        for (int q = 0; q < VE / 4; q++)
-            st_stream((char*)outBase + (outElem + 4 * q) * 4,
-                      make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
-    } else {
-        st_stream((char*)outBase + outElem * 2,
-                  make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16),
-                             o[6] | (o[7] << 16)));
-    }
-}
-
-template <int DT, int OUT>
-__device__ __forceinline__ void store_epilogue_vec(void* outBase, size_t outElem, const V32& acc,
-                                                   bool hasScale, float scale) {
-    constexpr int VE = 16 / DTypeOf<DT>::size;
-    if (DT == OUT && !hasScale) {
-        st_stream32((char*)outBase + outElem * DTypeOf<DT>::size, acc);
-        return;
-    }
-    store_epilogue_vec<DT, OUT>(outBase, outElem, acc.lo, hasScale, scale);
-    store_epilogue_vec<DT, OUT>(outBase, outElem + VE, acc.hi, hasScale, scale);
-}
-
-template <int DT, int OUT>
-__device__ __forceinline__ void store_epilogue_elem(void* outBase, size_t outElem, uint32_t acc,
-                                                    bool hasScale, float scale) {
-    constexpr int OSZ = DTypeOf<OUT>::size;
-    if (DT == OUT && !hasScale) {
-        st_elem<OSZ>(outBase, outElem, acc);
-        return;
-    }
-    float f = elem_to_f32<DT>(acc);
-    if (hasScale) f = __fmul_rn(f, scale);
-    st_elem<OSZ>(outBase, outElem, f32_to_elem<OUT>(f));
-}
-
-// Reduce-scatter: block r = [r*rc, (r+1)*rc) of every send buffer lands in recv[r].
-// a.count = N * rc, a.blockElems = rc.  VB > 0 requires rc * esz % VB == 0.  NF > 0 fixes
-// the rank count at compile time (the loads and the fold unroll completely).
-template <int DT, int OP, int OUT, int VB, int NF = 0>
-__global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
-k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
-    pdl_begin();
-    constexpr int ESZ = DTypeOf<DT>::size;
-    constexpr int U = VB ? VB / ESZ : 1;
-    const int N = NF ? NF : a.nRanks;
-    const int ch = blockIdx.x / a.ctasPerChannel;
-    const int cta = blockIdx.x - ch * a.ctasPerChannel;
-    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x;
-    const size_t rc = a.blockElems;
-    const bool hasScale = a.hasScale != 0;
-    const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, rc);
-    if (VB == 0) {
-        // element path: warp tiles of 32 * kElemsPerThread elements of one block
-        constexpr int TILE = 32 * kElemsPerThread;
-        const size_t lo = min((size_t)ch * a.chanElems, rc);
-        const size_t tiles = (chEnd - lo + TILE - 1) / TILE;
-        const int lane = threadIdx.x & 31;
-        for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride / 32) {
-            const int r = (int)(w / tiles);
-            const size_t t0 = lo + (w - (size_t)r * tiles) * TILE + lane;    // element within block r
-            const size_t base = (size_t)r * rc;
-            uint32_t acc[kElemsPerThread];
-            reduce_elems_ring<DT, OP>(a.send, N, r + 1 == N ? 0 : r + 1, base + t0, base + chEnd, acc);
-#pragma unroll
-            for (int k = 0; k < kElemsPerThread; k++)
-                if (t0 + 32 * (size_t)k < chEnd)
-                    store_epilogue_elem<DT, OUT>(a.recv[r], t0 + 32 * (size_t)k, acc[k], hasScale, a.scale);
-        }
-        return;
-    }
-    const ChannelSpan sp = channel_span(a, ch, U);
-    const size_t total = sp.units * (size_t)N;
-    for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < total; j += stride) {
-        const int r = (int)(j / sp.units);
-        const size_t i = j - (size_t)r * sp.units;
-        const size_t t = sp.lo + i * U;                 // element within block r
-        if (t >= chEnd) continue;
-        const size_t base = (size_t)r * rc;
-        const int first = r + 1 == N ? 0 : r + 1;
-        if (VB && t + U <= chEnd) {
-            const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16, NF>(a.send, N, first, (base + t) * ESZ);
-            store_epilogue_vec<DT, OUT>(a.recv[r], t, acc, hasScale, a.scale);
-        } else {
-            for (size_t x = t; x < min(t + U, chEnd); x++) {
-                const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, base + x);
-                store_epilogue_elem<DT, OUT>(a.recv[r], x, acc, hasScale, a.scale);
-            }
-        }
-    }
-}
-
-// ---- dispatch --------------------------------------------------------------------------
-
-template <int DT, int OP>
-static cudaError_t ar_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
-                                   cudaStream_t s) {
-    if (a.nRanks == 8 && vb == 32) (void)pdl_launch(k_allreduce_onepass<DT, OP, 32, 8>,
-            grid, threads, 0, s, a);
-    else if (a.nRanks == 8 && vb == 16) (void)pdl_launch(k_allreduce_onepass<DT, OP, 16, 8>,
-            grid, threads, 0, s, a);
-    else if (vb == 32) (void)pdl_launch(k_allreduce_onepass<DT, OP, 32>, grid, threads, 0, s, a);
-    else if (vb == 16) (void)pdl_launch(k_allreduce_onepass<DT, OP, 16>, grid, threads, 0, s, a);
-    else (void)pdl_launch(k_allreduce_onepass<DT, OP, 0>, grid, threads, 0, s, a);
-    return cudaGetLastError();
-}
-
-template <int DT>
-static cudaError_t ar_dispatch_op(const OnePassArgs& a, vRedOp_t op, int vb, int grid, int threads,
-                                  cudaStream_t s) {
-    switch (op) {
-    case vSum: return ar_dispatch_vec<DT, kSum>(a, vb, grid, threads, s);
-    case vProd: return ar_dispatch_vec<DT, kProd>(a, vb, grid, threads, s);
-    case vMin: return ar_dispatch_vec<DT, kMin>(a, vb, grid, threads, s);
-    case vMax: return ar_dispatch_vec<DT, kMax>(a, vb, grid, threads, s);
-    }
-    return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op, int vb,
                                      int grid, int threads, cudaStream_t s) {
-    switch (dt) {
-    case vFloat32: return ar_dispatch_op<kF32>(a, op, vb, grid, threads, s);
-    case vFloat16: return ar_dispatch_op<kF16>(a, op, vb, grid, threads, s);
-    case vBFloat16: return ar_dispatch_op<kBF16>(a, op, vb, grid, threads, s);
-    case vInt32: return ar_dispatch_op<kI32>(a, op, vb, grid, threads, s);
-    }
-    return cudaErrorInvalidValue;
-}
-
-template <int DT, int OP, int OUT>
-static cudaError_t rs_dispatch_vec(const OnePassArgs& a, int vb, int grid, int threads,
-                                   cudaStream_t s) {
-    if (a.nRanks == 8 && vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32, 8>,
-            grid, threads, 0, s, a);
-    else if (a.nRanks == 8 && vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16, 8>,
-            grid, threads, 0, s, a);
-    else if (vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32>, grid, threads, 0, s, a);
-    else if (vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16>, grid, threads, 0, s, a);
-    else (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0>, grid, threads, 0, s, a);
-    return cudaGetLastError();
-}
-
-template <int DT, int OUT>
-static cudaError_t rs_dispatch_op(const OnePassArgs& a, vRedOp_t op, int vb, int grid,
-                                  int threads, cudaStream_t s) {
-    switch (op) {
-    case vSum: return rs_dispatch_vec<DT, kSum, OUT>(a, vb, grid, threads, s);
-    case vProd: return rs_dispatch_vec<DT, kProd, OUT>(a, vb, grid, threads, s);
-    case vMin: return rs_dispatch_vec<DT, kMin, OUT>(a, vb, grid, threads, s);
-    case vMax: return rs_dispatch_vec<DT, kMax, OUT>(a, vb, grid, threads, s);
-    }
-    return cudaErrorInvalidValue;
+    if (vb != 0 && a.nRanks == 8) return ar_launch<8>(a, dt, op, vb, grid, threads, s);
+    if (vb != 0 && (a.nRanks >= 2 && a.nRanks <= 4))
+        return launch_allreduce_onepass_small(a, dt, op, vb, grid, threads, s);
+    return ar_launch<0>(a, dt, op, vb, grid, threads, s);
 }
 
 cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
                                           vDataType_t outType, int vb, int grid, int threads,
                                           cudaStream_t s) {
-    const bool toF32 = outType == vFloat32 && dt != vFloat32;
-    if (outType != dt && !toF32) return cudaErrorInvalidValue;
-    switch (dt) {
-    case vFloat32: return rs_dispatch_op<kF32, kF32>(a, op, vb, grid, threads, s);
-    case vFloat16:
-        return toF32 ? rs_dispatch_op<kF16, kF32>(a, op, vb, grid, threads, s)
-                     : rs_dispatch_op<kF16, kF16>(a, op, vb, grid, threads, s);
-    case vBFloat16:
-        return toF32 ? rs_dispatch_op<kBF16, kF32>(a, op, vb, grid, threads, s)
-                     : rs_dispatch_op<kBF16, kBF16>(a, op, vb, grid, threads, s);
-    case vInt32: return rs_dispatch_op<kI32, kI32>(a, op, vb, grid, threads, s);
-    }
-    return cudaErrorInvalidValue;
+    if (vb != 0 && a.nRanks == 8) return rs_launch<8>(a, dt, op, outType, vb, grid, threads, s);
+    if (vb != 0 && (a.nRanks >= 2 && a.nRanks <= 4))
+        return launch_reduce_scatter_onepass_small(a, dt, op, outType, vb, grid, threads, s);
+    return rs_launch<0>(a, dt, op, outType, vb, grid, threads, s);
 }
 
 }  // namespace vc

@@ -39,7 +39,8 @@ def run_tree(comms, xs, op, pad=0, inplace=False):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16, torch.int32],
                          ids=lambda d: str(d).split(".")[1])
 def test_tree_allreduce_parity(comms, dtype, op):
-    for n, count in [(2, 1), (3, 7), (8, 4099), (5, 33_333), (8, 100_003), (7, 65_536), (16, 20_000)]:
+    for n, count in [(2, 1), (3, 7), (8, 4099), (5, 33_333), (8, 100_003), (7, 65_536), (16, 20_000),
+                     (2, 50_000), (4, 40_000), (4, 4_097), (16, 70_001)]:
         xs = inputs.uniform_ranks(n, count, dtype, seed=n * 31 + count)
         got = run_tree(comms, xs, op)
         assert_bits_equal(got, oracle.allreduce_tree(xs, op), f"tree n={n} count={count}")

@@ -49,6 +49,20 @@ def normal_ranks(n_ranks: int, count: int, std: float, dtype: torch.dtype, seed:
             for _ in range(n_ranks)]
 
 
+def index_pattern(rank: int, start: int, count: int, dtype: torch.dtype, device="cpu") -> torch.Tensor:
+    """Elements [start, start + count) of rank ``rank`` of a deterministic pattern for
+    buffers too large to draw on the host: a hash of (rank, index) mapped to k / 256 with
+    integer k in [-255, 255] (exact in fp16, bf16 and fp32), or to the integer k for
+    int32.  The hash stays below 2^63 for indices below 2^40.  Any slice can be rebuilt
+    anywhere from its indices alone, so a test fills a multi-GiB buffer on the device and
+    recomputes sampled elements on the host."""
+    e = torch.arange(start, start + count, dtype=torch.int64, device=device)
+    k = (e * 40503 + (e >> 11) * 977 + (rank + 1) * 97531) % 511 - 255
+    if dtype == torch.int32:
+        return k.to(torch.int32)
+    return (k.to(torch.float32) / 256).to(dtype)
+
+
 def small_int_ranks(n_ranks: int, count: int, dtype: torch.dtype, seed: int, lo: int = -8,
                     hi: int = 8) -> list[torch.Tensor]:
     """N buffers of small integers stored in ``dtype`` (exact in every supported type).

@@ -458,3 +458,23 @@ def test_tree_allreduce_library_special_cases():
     # a different order than the ring: random fp32 sums differ somewhere
     zs = inputs.uniform_ranks(8, 4096, torch.float32, 1)
     assert not _same_bits(oracle.allreduce_tree(zs, "sum")[0], oracle.allreduce(zs, "sum")[0])
+
+
+def test_index_pattern_is_a_function_of_rank_and_index_only():
+    # slices rebuilt from any start agree with the whole; values are exact in every type
+    whole = inputs.index_pattern(1, 0, 5000, torch.float32)
+    for start in (0, 1, 511, 2047, 4999):
+        part = inputs.index_pattern(1, start, 5000 - start, torch.float32)
+        assert torch.equal(part, whole[start:])
+    k = whole * 256
+    assert torch.equal(k, k.round()) and k.abs().max() <= 255
+    for dt in (torch.float16, torch.bfloat16):
+        assert torch.equal(inputs.index_pattern(1, 0, 5000, dt).float(), whole)
+    assert torch.equal(inputs.index_pattern(1, 0, 5000, torch.int32).float(), k)
+    # far past 2^31 and 2^32 the pattern still differs from the one 2^31 or 2^32 earlier
+    for e in (1 << 31, (1 << 32) + 7, (1 << 33) + 1):
+        far = inputs.index_pattern(0, e, 64, torch.float32)
+        for back in (1 << 31, 1 << 32):
+            if e >= back:
+                assert not torch.equal(far, inputs.index_pattern(0, e - back, 64, torch.float32)), (e, back)
+    assert not torch.equal(inputs.index_pattern(0, 0, 64, torch.float32), inputs.index_pattern(1, 0, 64, torch.float32))

@@ -4,22 +4,69 @@
 // child 1's, and the root's result is written to every rank.
 #pragma once
 
+#include <algorithm>
+
 #include "device.cuh"
 
 namespace vc {
 
-// Double-binary-tree all-reduce, one pass.  A thread loads its vector of every rank
-// (8 loads in flight at a time) into a per-thread array, then evaluates the tree in
-// post-order with a small stack: a node's partial is its own vector, then OP with child
-// 0's partial, then with child 1's.  Both arrays live in local memory (their indices are
-// data-independent but known only at run time); the kernel stays HBM-bound.
+// Double-binary-tree all-reduce, one pass, for a rank count known only at run time.  A
+// thread walks the tree's post-order program (a node's partial is its own value, then OP
+// with child 0's partial, then with child 1's) eight steps at a time: it loads the eight
+// nodes' values first, then folds them.  The newest partial stays in registers; the
+// partials still waiting for their parent sit on a per-thread stack in shared memory
+// (at most 6 deep for N <= 64), since their positions are known only at run time.  The
+// vector path moves 16 bytes per rank and runs in CTAs of at most kTreeThreads threads.
+constexpr int kTreeThreads = 256;
+constexpr int kTreeStackDepth = 8;
+
+template <int DT, int OP, typename T>
+__device__ __forceinline__ T tree_op(T a, T b) {
+    if constexpr (sizeof(T) == 4) return op_elem<DT, OP>(a, b);
+    else return op_vec<DT, OP>(a, b);
+}
+
+// Fold one tree's program over the values load(rank) yields; returns the root's partial.
+template <int DT, int OP, typename T, typename Load>
+__device__ __forceinline__ T eval_tree_runtime(const TreeArgs& a, int t, T (*stk)[kTreeThreads], Load load) {
+    const int N = a.nRanks;
+    T top{};
+    int sp = 0;                       // partials below `top`
+    for (int i0 = 0; i0 < N; i0 += 8) {
+        T v[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            if (i0 + q < N) v[q] = load(a.prog[t][i0 + q]);
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            if (i0 + q < N) {
+                const int c = a.nchild[t][i0 + q];
+                T acc = v[q];
+                if (c == 2) {
+                    acc = tree_op<DT, OP>(acc, stk[--sp][threadIdx.x]);   // child 0, below the top
+                    acc = tree_op<DT, OP>(acc, top);                      // child 1, the top
+                } else if (c == 1) {
+                    acc = tree_op<DT, OP>(acc, top);
+                } else if (i0 + q > 0) {
+                    stk[sp++][threadIdx.x] = top;                         // a leaf: keep the old top
+                }
+                top = acc;
+            }
+        }
+    }
+    return top;
+}
+
 template <int DT, int OP, int VB>
-__global__ void __launch_bounds__(kOnePassThreads, 2)
+__global__ void __launch_bounds__(kTreeThreads, 4)
 k_allreduce_tree(const __grid_constant__ TreeArgs a) {
+    static_assert(VB == 0 || VB == 16, "the run-time tree moves 16-byte vectors or elements");
     pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int U = VB ? VB / ESZ : 1;
-    using VT = typename VecOf<VB ? VB : 16>::T;
+    using VT = typename VecOf<16>::T;
+    __shared__ VT vstk[VB ? kTreeStackDepth : 1][kTreeThreads];
+    __shared__ uint32_t estk[kTreeStackDepth][kTreeThreads];
     const int N = a.nRanks;
     const size_t u0 = (a.split + U - 1) / U;
     const size_t u1 = (a.count - a.split + U - 1) / U;
@@ -29,38 +76,16 @@ k_allreduce_tree(const __grid_constant__ TreeArgs a) {
         const size_t lo = t == 0 ? 0 : a.split, hi = t == 0 ? a.split : a.count;
         const size_t e = lo + (j - (t == 0 ? 0 : u0)) * U;
         if (VB && e + U <= hi) {
-            VT xs[VCOMM_MAX_RANKS];
-            for (int k0 = 0; k0 < N; k0 += 8) {
-                VT v[8];
-#pragma unroll
-                for (int q = 0; q < 8; q++)
-                    if (k0 + q < N) v[q] = VecOf<VB ? VB : 16>::ld((const char*)a.send[k0 + q] + e * ESZ);
-#pragma unroll
-                for (int q = 0; q < 8; q++)
-                    if (k0 + q < N) xs[k0 + q] = v[q];
-            }
-            VT stk[kTreeMaxStack];
-            int sp = 0;
-            for (int i = 0; i < N; i++) {
-                const int c = a.nchild[t][i];
-                VT acc = xs[a.prog[t][i]];
-                for (int q = 0; q < c; q++) acc = op_vec<DT, OP>(acc, stk[sp - c + q]);
-                sp -= c;
-                stk[sp++] = acc;
-            }
-            for (int r = 0; r < N; r++) VecOf<VB ? VB : 16>::st((char*)a.recv[r] + e * ESZ, stk[0]);
+            const VT acc = eval_tree_runtime<DT, OP, VT>(a, t, vstk, [&](int r) {
+                return VecOf<16>::ld((const char*)a.send[r] + e * ESZ);
+            });
+            for (int r = 0; r < N; r++) VecOf<16>::st((char*)a.recv[r] + e * ESZ, acc);
         } else {
             for (size_t x = e; x < min(e + U, hi); x++) {
-                uint32_t stk[kTreeMaxStack];
-                int sp = 0;
-                for (int i = 0; i < N; i++) {
-                    const int c = a.nchild[t][i];
-                    uint32_t acc = ld_elem<ESZ>(a.send[a.prog[t][i]], x);
-                    for (int q = 0; q < c; q++) acc = op_elem<DT, OP>(acc, stk[sp - c + q]);
-                    sp -= c;
-                    stk[sp++] = acc;
-                }
-                for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], x, stk[0]);
+                const uint32_t acc = eval_tree_runtime<DT, OP, uint32_t>(a, t, estk, [&](int r) {
+                    return ld_elem<ESZ>(a.send[r], x);
+                });
+                for (int r = 0; r < N; r++) st_elem<ESZ>(a.recv[r], x, acc);
             }
         }
     }
@@ -215,9 +240,13 @@ static cudaError_t tree_launch_vec(const TreeArgs& a, int vb, int grid, int thre
         else if (vb == 16) (void)pdl_launch(k_allreduce_tree_fixed<DT, OP, 16, NF>, grid, threads, 0, s, a);
         else return cudaErrorInvalidValue;
     } else {
-        if (vb == 32) (void)pdl_launch(k_allreduce_tree<DT, OP, 32>, grid, threads, 0, s, a);
-        else if (vb == 16) (void)pdl_launch(k_allreduce_tree<DT, OP, 16>, grid, threads, 0, s, a);
-        else (void)pdl_launch(k_allreduce_tree<DT, OP, 0>, grid, threads, 0, s, a);
+        // 16-byte vectors (32-byte alignment implies 16) in CTAs of at most kTreeThreads
+        // threads, with the grid grown to keep the same number of threads per vector
+        const long long scale = (long long)(vb == 32 ? 2 : 1) * (threads > kTreeThreads ? threads / kTreeThreads : 1);
+        const int g = (int)std::min<long long>((long long)grid * scale, (long long)kMaxGridCtas);
+        const int th = threads > kTreeThreads ? kTreeThreads : threads;
+        if (vb != 0) (void)pdl_launch(k_allreduce_tree<DT, OP, 16>, g, th, 0, s, a);
+        else (void)pdl_launch(k_allreduce_tree<DT, OP, 0>, g, th, 0, s, a);
     }
     return cudaGetLastError();
 }
@@ -245,7 +274,7 @@ static cudaError_t tree_launch(const TreeArgs& a, vDataType_t dt, vRedOp_t op, i
     return cudaErrorInvalidValue;
 }
 
-// The 2-, 4- and 16-rank vector kernels (k_tree_more.cu).
+// The 2- and 4-rank vector kernels (k_tree_more.cu).
 cudaError_t launch_allreduce_tree_more(const TreeArgs& a, vDataType_t dt, vRedOp_t op, int vb, int grid,
                                        int threads, cudaStream_t s);
 

@@ -47,10 +47,82 @@ __device__ __forceinline__ void elem_copy(const char* src, char* const* dst, siz
     }
 }
 
+// Bytes [sh, sh + 16) of the 32 bytes a, b (little endian), for sh in [0, 16).
+__device__ __forceinline__ uint4 shift_bytes(const uint4& a, const uint4& b, unsigned sh) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const unsigned r = (sh & 3u) * 8u;
+    uint32_t o[4];
+    switch (sh >> 2) {
+#define VC_SHIFT_CASE(Q)                                                                   \
+    case Q:                                                                                \
+        _Pragma("unroll") for (int k = 0; k < 4; k++) o[k] = __funnelshift_r(w[k + Q], w[k + Q + 1], r); \
+        break;
+        VC_SHIFT_CASE(0)
+        VC_SHIFT_CASE(1)
+        VC_SHIFT_CASE(2)
+        default:
+        _Pragma("unroll") for (int k = 0; k < 3; k++) o[k] = __funnelshift_r(w[k + 3], w[k + 4], r);
+        o[3] = __funnelshift_r(w[6], w[7], r);
+        break;
+#undef VC_SHIFT_CASE
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Copy [lo, hi) when 16-byte vectors cannot cover source and destinations at the same
+// offsets (a ragged block, or pointers off 16 bytes).  The destinations set the vectors:
+// the elements up to their first 16-byte boundary go one by one, then every 16-byte
+// destination vector is cut from the two aligned 16-byte source vectors that hold its
+// bytes, shifted by the source's offset against the destination; the rest go one by one.
+// The second source vector always holds some of the copied bytes, so no load leaves the
+// aligned 16-byte blocks the copy reads from.  Destinations at different offsets from a
+// 16-byte boundary go element by element.
+template <int ESZ>
+__device__ __forceinline__ void realign_copy(const char* src, char* const* dst, size_t dstOff, int ndst,
+                                             size_t lo, size_t hi) {
+    if (hi <= lo) return;
+    const uintptr_t d0 = (uintptr_t)(dst[0] + (dstOff + lo) * ESZ);
+    for (int d = 1; d < ndst; d++)
+        if ((((uintptr_t)(dst[d] + (dstOff + lo) * ESZ)) ^ d0) & 15u) {
+            elem_copy<ESZ>(src, dst, dstOff, ndst, lo, hi);
+            return;
+        }
+    constexpr int VE = 16 / ESZ;
+    const size_t head = min((size_t)(((16u - (d0 & 15u)) & 15u) / ESZ), hi - lo);
+    const size_t m0 = lo + head;
+    const size_t nv = (hi - m0) / VE;
+    elem_copy<ESZ>(src, dst, dstOff, ndst, lo, m0);
+    const char* s0 = src + m0 * ESZ;
+    const unsigned sh = (unsigned)((uintptr_t)s0 & 15u);
+    const uint4* sa = reinterpret_cast<const uint4*>(s0 - sh);
+    constexpr int UN = 4;
+    for (size_t i0 = threadIdx.x; i0 < nv; i0 += (size_t)UN * blockDim.x) {
+        uint4 v[UN];
+#pragma unroll
+        for (int u = 0; u < UN; u++) {
+            const size_t i = i0 + (size_t)u * blockDim.x;
+            if (i < nv) {
+                const uint4 x = sa[i];
+                v[u] = sh ? shift_bytes(x, sa[i + 1], sh) : x;
+            }
+        }
+        for (int d = 0; d < ndst; d++) {
+            uint4* o = reinterpret_cast<uint4*>(dst[d] + (dstOff + m0) * ESZ);
+#pragma unroll
+            for (int u = 0; u < UN; u++) {
+                const size_t i = i0 + (size_t)u * blockDim.x;
+                if (i < nv) st_stream(o + i, v[u]);
+            }
+        }
+    }
+    elem_copy<ESZ>(src, dst, dstOff, ndst, m0 + nv * VE, hi);
+}
+
 // Copy [lo, hi) elements from src to every dst[0..ndst) (ndst = 1 for all-to-all).
-// VB: bytes per vector (16 or 32; 0 = element by element).  A thread keeps 128 bytes of
-// loads in flight: 8 vectors of 16 bytes or 4 of 32.
-template <int ESZ, int VB>
+// VB: bytes per vector (16 or 32; 0 = misaligned: realigned 16-byte vectors for 2-byte
+// elements when REALIGN, else element by element).  A thread keeps 128 bytes of loads in flight: 8 vectors of 16
+// bytes or 4 of 32.
+template <int ESZ, int VB, bool REALIGN = true>
 __device__ __forceinline__ void tile_copy(const char* src, char* const* dst, size_t dstOff, int ndst,
                                           size_t lo, size_t hi) {
     if (VB) {
@@ -76,6 +148,11 @@ __device__ __forceinline__ void tile_copy(const char* src, char* const* dst, siz
             }
         }
         elem_copy<ESZ>(src, dst, dstOff, ndst, lo + nv * VE, hi);
+    } else if (REALIGN && ESZ == 2) {
+        // measured on GB300: realigned vectors beat 2-byte element copies (ragged bf16
+        // all-gather 0.71 -> 0.82 of the copy bandwidth) but lose to 4-byte ones (fp32
+        // 0.88 -> 0.87, 3-rank all-to-all 0.85 -> 0.69)
+        realign_copy<ESZ>(src, dst, dstOff, ndst, lo, hi);
     } else {
         elem_copy<ESZ>(src, dst, dstOff, ndst, lo, hi);
     }
@@ -227,7 +304,7 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
         const uintptr_t al = ((uintptr_t)src | (uintptr_t)dst) & 31;
         if (al == 0) tile_copy<ESZ, 32>(src, &dst, 0, 1, lo, hi);
         else if ((al & 15) == 0) tile_copy<ESZ, 16>(src, &dst, 0, 1, lo, hi);
-        else tile_copy<ESZ, 0>(src, &dst, 0, 1, lo, hi);
+        else tile_copy<ESZ, 0, false>(src, &dst, 0, 1, lo, hi);   // element by element: no spills
     }
     // Every CTA has taken its last tile number; the last one out clears the counter.
     if (threadIdx.x == 0 && atomicAdd(&a.tileCounter[1], 1u) == gridDim.x - 1) {

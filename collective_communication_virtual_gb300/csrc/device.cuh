@@ -247,6 +247,28 @@ template <> struct VecOf<32> {
     static __device__ __forceinline__ void st(void* p, const V32& v) { st_stream32(p, v); }
 };
 
+// Bytes [sh, sh + 16) of the 32 bytes a, b (little endian), for sh in [0, 16).
+__device__ __forceinline__ uint4 shift_bytes(const uint4& a, const uint4& b, unsigned sh) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const unsigned r = (sh & 3u) * 8u;
+    uint32_t o[4];
+    switch (sh >> 2) {
+#define VC_SHIFT_CASE(Q)                                                                   \
+    case Q:                                                                                \
+        _Pragma("unroll") for (int k = 0; k < 4; k++) o[k] = __funnelshift_r(w[k + Q], w[k + Q + 1], r); \
+        break;
+        VC_SHIFT_CASE(0)
+        VC_SHIFT_CASE(1)
+        VC_SHIFT_CASE(2)
+        default:
+        _Pragma("unroll") for (int k = 0; k < 3; k++) o[k] = __funnelshift_r(w[k + 3], w[k + 4], r);
+        o[3] = __funnelshift_r(w[6], w[7], r);
+        break;
+#undef VC_SHIFT_CASE
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Element loads/stores for the scalar paths (esz = 2 or 4).
 template <int ESZ>
 __device__ __forceinline__ uint32_t ld_elem(const void* base, size_t e) {

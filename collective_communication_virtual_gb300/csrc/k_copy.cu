@@ -5,6 +5,8 @@
 //
 // All-gather and broadcast read each source vector once and write it to all N receive
 // buffers: (N+1)*S bytes, the minimum.  All-to-all copies each of the N*N blocks once.
+#include <type_traits>
+
 #include "device.cuh"
 
 namespace vc {
@@ -47,28 +49,6 @@ __device__ __forceinline__ void elem_copy(const char* src, char* const* dst, siz
     }
 }
 
-// Bytes [sh, sh + 16) of the 32 bytes a, b (little endian), for sh in [0, 16).
-__device__ __forceinline__ uint4 shift_bytes(const uint4& a, const uint4& b, unsigned sh) {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    const unsigned r = (sh & 3u) * 8u;
-    uint32_t o[4];
-    switch (sh >> 2) {
-#define VC_SHIFT_CASE(Q)                                                                   \
-    case Q:                                                                                \
-        _Pragma("unroll") for (int k = 0; k < 4; k++) o[k] = __funnelshift_r(w[k + Q], w[k + Q + 1], r); \
-        break;
-        VC_SHIFT_CASE(0)
-        VC_SHIFT_CASE(1)
-        VC_SHIFT_CASE(2)
-        default:
-        _Pragma("unroll") for (int k = 0; k < 3; k++) o[k] = __funnelshift_r(w[k + 3], w[k + 4], r);
-        o[3] = __funnelshift_r(w[6], w[7], r);
-        break;
-#undef VC_SHIFT_CASE
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // Copy [lo, hi) when 16-byte vectors cannot cover source and destinations at the same
 // offsets (a ragged block, or pointers off 16 bytes).  The destinations set the vectors:
 // the elements up to their first 16-byte boundary go one by one, then every 16-byte
@@ -96,25 +76,30 @@ __device__ __forceinline__ void realign_copy(const char* src, char* const* dst, 
     const unsigned sh = (unsigned)((uintptr_t)s0 & 15u);
     const uint4* sa = reinterpret_cast<const uint4*>(s0 - sh);
     constexpr int UN = 4;
-    for (size_t i0 = threadIdx.x; i0 < nv; i0 += (size_t)UN * blockDim.x) {
-        uint4 v[UN];
-#pragma unroll
-        for (int u = 0; u < UN; u++) {
-            const size_t i = i0 + (size_t)u * blockDim.x;
-            if (i < nv) {
-                const uint4 x = sa[i];
-                v[u] = sh ? shift_bytes(x, sa[i + 1], sh) : x;
-            }
-        }
-        for (int d = 0; d < ndst; d++) {
-            uint4* o = reinterpret_cast<uint4*>(dst[d] + (dstOff + m0) * ESZ);
+    // sh is the same for the whole tile: two loops, so that every load is unconditional
+    auto body = [&](auto shifted) {
+        for (size_t i0 = threadIdx.x; i0 < nv; i0 += (size_t)UN * blockDim.x) {
+            uint4 v[UN];
 #pragma unroll
             for (int u = 0; u < UN; u++) {
                 const size_t i = i0 + (size_t)u * blockDim.x;
-                if (i < nv) st_stream(o + i, v[u]);
+                if (i < nv) {
+                    if constexpr (decltype(shifted)::value) v[u] = shift_bytes(sa[i], sa[i + 1], sh);
+                    else v[u] = ld_stream(sa + i);
+                }
+            }
+            for (int d = 0; d < ndst; d++) {
+                uint4* o = reinterpret_cast<uint4*>(dst[d] + (dstOff + m0) * ESZ);
+#pragma unroll
+                for (int u = 0; u < UN; u++) {
+                    const size_t i = i0 + (size_t)u * blockDim.x;
+                    if (i < nv) st_stream(o + i, v[u]);
+                }
             }
         }
-    }
+    };
+    if (sh) body(std::true_type{});
+    else body(std::false_type{});
     elem_copy<ESZ>(src, dst, dstOff, ndst, m0 + nv * VE, hi);
 }
 

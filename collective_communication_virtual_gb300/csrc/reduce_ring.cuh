@@ -101,4 +101,54 @@ __device__ __forceinline__ uint32_t reduce_elem_ring(const void* const* send, in
     return acc;
 }
 
+// 16 bytes at byte offset `boff` of every rank, reduced in ring order from rank `first`,
+// for offsets that need not be 16-byte aligned: each rank's bytes are cut from the two
+// aligned 16-byte blocks that hold them.  The second block always holds some of the 16
+// bytes, so no load leaves the aligned blocks of the reduced range.  When every rank sits
+// at the same offset from a 16-byte boundary (the usual case: equally aligned buffers) the
+// loads are unconditional, so four ranks' loads are in flight before any is folded.
+template <int DT, int OP, typename Load>
+__device__ __forceinline__ uint4 fold_ring4(int N, int first, Load load) {
+    uint4 acc = load(first);
+    int rk = first + 1 == N ? 0 : first + 1;
+    for (int k = 1; k < N; k += 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (k + j < N) {
+                v[j] = load(rk);
+                rk = rk + 1 == N ? 0 : rk + 1;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            if (k + j < N) acc = op_vec<DT, OP>(acc, v[j]);
+    }
+    return acc;
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint4 reduce_vec_ring_realign(const void* const* send, int N, int first, size_t boff) {
+    const unsigned sh = (unsigned)(((uintptr_t)send[first] + boff) & 15u);
+    bool uniform = true;
+    for (int k = 0; k < N; k++) uniform = uniform && (unsigned)(((uintptr_t)send[k] + boff) & 15u) == sh;
+    if (!uniform) {
+        // ranks at different offsets from a 16-byte boundary: element by element
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        constexpr int ESZ = DTypeOf<DT>::size;
+        for (int i = 0; i < 16 / ESZ; i++) {
+            const uint32_t e = reduce_elem_ring<DT, OP>(send, N, first, boff / ESZ + i);
+            if (ESZ == 4) w[i] = e;
+            else w[i >> 1] |= e << (16 * (i & 1));
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (sh == 0)
+        return fold_ring4<DT, OP>(N, first, [&](int rk) { return ld_stream((const char*)send[rk] + boff); });
+    return fold_ring4<DT, OP>(N, first, [&](int rk) {
+        const uint4* q = reinterpret_cast<const uint4*>((const char*)send[rk] + boff - sh);
+        return shift_bytes(q[0], q[1], sh);
+    });
+}
+
 }  // namespace vc

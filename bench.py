@@ -237,6 +237,47 @@ def cpu_baseline_sample(torch):
             "kind": "oracle", "sample": f"the whole workload (8 x 64 MiB fp32 sum), {reps} runs"}
 
 
+def cpu_baseline_workloads(torch):
+    """The oracle as it stands on the other collectives' workloads, once each, on all host
+    cores where it takes a thread count: minimum bytes per second, the GPU rows' basis."""
+    import oracle
+    from collective_communication_virtual_gb300 import inputs
+    cores = len(os.sched_getaffinity(0))
+    n, out = N_RANKS, {}
+
+    def row(name, fn, nbytes):
+        t0 = time.perf_counter()
+        fn()
+        t = time.perf_counter() - t0
+        out[name] = {"us": t * 1e6, "min_bytes": nbytes, "gbs": nbytes / t / 1e9}
+
+    cnt, rc = 13_107_200, 13_107_200 // n
+    g = inputs.normal_ranks(n, cnt, 1e-3, torch.bfloat16, 2)
+    row("fsdp_reduce_scatter_scale_cast_bf16_25MiB",
+        lambda: oracle.reduce_scatter_scale(g, "sum", 1.0 / n, nthreads=cores), n * cnt * 2 + n * rc * 4)
+    sh = [x[:rc].clone() for x in g]
+    row("fsdp_allgather_bf16_25MiB", lambda: oracle.allgather(sh), n * rc * 2 + n * cnt * 2)
+    del g, sh
+    send, counts, sd, rd, recv_elems = inputs.moe_dispatch()
+    moved = int(counts.sum()) * 2
+    row("moe_alltoallv_bf16_8x4096x4096_top2", lambda: oracle.alltoallv(send, counts, sd, rd, recv_elems), 2 * moved)
+    del send
+    S = BYTES_PER_RANK
+    xs = inputs.uniform_ranks(n, COUNT, torch.float32, 1)
+    parts = [x[:COUNT // n].clone() for x in xs]
+    row("reduce_scatter_fp32_64MiB", lambda: oracle.reduce_scatter(xs, "sum", nthreads=cores), n * S + S)
+    row("allgather_fp32_64MiB", lambda: oracle.allgather(parts), S + n * S)
+    row("broadcast_fp32_64MiB", lambda: oracle.broadcast(xs, 0), S + n * S)
+    row("alltoall_fp32_64MiB", lambda: oracle.alltoall(xs), 2 * n * S)
+    row("reduce_fp32_64MiB", lambda: oracle.reduce(xs, "sum", 0, nthreads=cores), n * S + S)
+    row("gather_fp32_8x64MiB", lambda: oracle.gather(xs, 0), 2 * n * S)
+    big = torch.cat(xs)
+    row("scatter_fp32_8x64MiB", lambda: oracle.scatter(big, n, 0), 2 * n * S)
+    row("allreduce_double_binary_tree_fp32_64MiB", lambda: oracle.allreduce_tree(xs, "sum", nthreads=cores),
+        2 * n * S)
+    return {"cores": cores, "kind": "oracle", "runs": 1, "workloads": out}
+
+
 def run_ours(args):
     import torch
 
@@ -308,6 +349,7 @@ def run_ours(args):
         line["channel_sweep"] = channel_sweep(torch, V, send, recv, stream)
         line["other_workloads"] = other_workloads(torch, V, dev, stream, hbm)
         line["cpu_baseline"] = cpu_baseline_sample(torch)
+        line["cpu_baseline"]["other_workloads"] = cpu_baseline_workloads(torch)
     elif not args.no_extras:
         line["e2e"] = None
     V.vcommDestroy(comm)

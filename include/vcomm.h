@@ -192,9 +192,12 @@ vResult_t vcommSetTimeoutMs(vcomm_t comm, int timeoutMs);
 /* device can access (device allocations, pinned or managed host memory: the kernels */
 /* read and write it directly, so host buffers need no staging copies).              */
 /* Any element-aligned pointer is accepted; when every pointer and the sizes allow   */
-/* 16-byte vectors the vector path runs, otherwise an element-wise path; the output  */
-/* bits are the same.  count == 0 returns vSuccess and launches nothing (NCCL book   */
-/* chapter 6, taskAppend).  With nRanks == 1 every collective is a copy.             */
+/* 16-byte (or 32-byte) vectors the vector path runs, otherwise an element path (for */
+/* 2-byte types, 16-byte vectors realigned to the outputs where the offsets allow);  */
+/* the output bits are the same.  The element paths read no byte outside the 16-byte */
+/* aligned blocks that hold a buffer's own elements.  count == 0 returns vSuccess    */
+/* and launches nothing (NCCL book chapter 6, taskAppend).  With nRanks == 1 every   */
+/* collective is a copy.                                                             */
 /* ------------------------------------------------------------------------------- */
 
 /* recvbuffs[r][e] = the reduction over all ranks of sendbuffs[.][e], e < count, for

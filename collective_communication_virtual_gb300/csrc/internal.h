@@ -105,6 +105,9 @@ struct TreeArgs {
     size_t split;                    // elements [0, split) use tree 0
 };
 constexpr int kTreeMaxStack = 16;
+// Elements a thread reduces at once on the element paths (buffers that 16-byte vectors
+// cannot cover); the planner and the group batcher size their work units by it.
+constexpr int kElemsPerThread = 8;
 
 cudaError_t launch_allreduce_tree(const TreeArgs& a, vDataType_t dt, vRedOp_t op, int vb, int grid,
                                   int threads, cudaStream_t s);

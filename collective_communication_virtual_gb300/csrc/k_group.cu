@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(kOnePassThreads, VB == 32 ? 1 : 2)
 k_allreduce_group(const __grid_constant__ GroupArgs a) {
     pdl_begin();
     constexpr int ESZ = DTypeOf<DT>::size;
-    constexpr int U = VB ? VB / ESZ : 1;
+    constexpr int U = VB ? VB / ESZ : kElemsPerThread;    // a unit: a vector, or 8 elements
     const GroupItem* items = reinterpret_cast<const GroupItem*>(a.table);
     const void* const* ptrs = reinterpret_cast<const void* const*>(a.table + a.ptrByteOff);
     __shared__ unsigned long long sStart[kMaxGroupItems];
@@ -43,10 +43,19 @@ k_allreduce_group(const __grid_constant__ GroupArgs a) {
             const size_t boff = e * ESZ;
             const auto acc = reduce_vec_ring<DT, OP, VB ? VB : 16>(send, N, first, boff);
             for (int r = 0; r < N; r++) VecOf<VB ? VB : 16>::st((char*)recv[r] + boff, acc);
-        } else {
+        } else if (VB) {
             for (size_t x = e; x < min(e + U, bend); x++) {
                 const uint32_t acc = reduce_elem_ring<DT, OP>(send, N, first, x);
                 for (int r = 0; r < N; r++) st_elem<ESZ>(recv[r], x, acc);
+            }
+        } else {
+            // element path: 8 consecutive elements of up to four ranks loaded before folding
+            uint32_t acc[kElemsPerThread];
+            reduce_elems_ring<DT, OP, 1>(send, N, first, e, bend, acc);
+            for (int r = 0; r < N; r++) {
+#pragma unroll
+                for (int k = 0; k < kElemsPerThread; k++)
+                    if (e + k < bend) st_elem<ESZ>(recv[r], e + k, acc[k]);
             }
         }
     }

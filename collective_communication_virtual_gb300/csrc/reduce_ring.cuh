@@ -53,16 +53,15 @@ __device__ __forceinline__ typename VecOf<VB>::T reduce_vec_ring(const void* con
 // ranks are loaded before any is folded: plain element loads cannot be moved past the
 // stores by the compiler, so one element at a time would wait out a full memory latency
 // per rank.  Elements at or beyond `end` are neither loaded nor used.
-constexpr int kElemsPerThread = 8;
-
-template <int DT, int OP>
+// STRIDE: element spacing of a thread's K elements (32: warp tiles; 1: K consecutive).
+template <int DT, int OP, int STRIDE = 32>
 __device__ __forceinline__ void reduce_elems_ring(const void* const* send, int N, int first, size_t e0,
                                                   size_t end, uint32_t (&acc)[kElemsPerThread]) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int K = kElemsPerThread;
 #pragma unroll
     for (int k = 0; k < K; k++) {
-        const size_t e = e0 + 32 * (size_t)k;
+        const size_t e = e0 + STRIDE * (size_t)k;
         acc[k] = e < end ? ld_elem<ESZ>(send[first], e) : 0u;
     }
     int rk = first + 1 == N ? 0 : first + 1;
@@ -73,7 +72,7 @@ __device__ __forceinline__ void reduce_elems_ring(const void* const* send, int N
             if (n + j < N) {
 #pragma unroll
                 for (int k = 0; k < K; k++) {
-                    const size_t e = e0 + 32 * (size_t)k;
+                    const size_t e = e0 + STRIDE * (size_t)k;
                     v[j][k] = e < end ? ld_elem<ESZ>(send[rk], e) : 0u;
                 }
                 rk = rk + 1 == N ? 0 : rk + 1;

@@ -439,7 +439,7 @@ vResult_t launch_group_batch(vcomm* c, const std::vector<const GroupRec*>& items
     vc::GroupItem* it = reinterpret_cast<vc::GroupItem*>(a.table);
     const void** ptrs = reinterpret_cast<const void**>(a.table + itemBytes);
     const size_t esz = elem_size(r0.dt);
-    const size_t U = r0.vecBytes ? (size_t)r0.vecBytes / esz : 1;
+    const size_t U = r0.vecBytes ? (size_t)r0.vecBytes / esz : (size_t)vc::kElemsPerThread;
     unsigned long long units = 0;
     for (size_t i = 0; i < n; i++) {
         const GroupRec& g = *items[i];

@@ -41,6 +41,27 @@ def test_group_of_mixed_all_reduces_matches_oracle(comm):
         assert_bits_equal(recv, oracle.allreduce(xs, op), f"group allreduce {xs[0].dtype} {op}")
 
 
+def test_group_of_all_reduces_off_16_bytes(comm):
+    # pointers one or three elements off a 16-byte boundary: the batched element path
+    n = 8
+    cases = []
+    V.vcommGroupStart(comm)
+    # items of one type and op fuse into one launch: fp32 sum, bf16 sum and int32 max pairs
+    for i, (count, dtype, op, pad) in enumerate([(5, torch.float32, "sum", 1), (40_001, torch.float32, "sum", 1),
+                                                 (33_333, torch.bfloat16, "sum", 3), (70_000, torch.bfloat16, "sum", 1),
+                                                 (9_999, torch.int32, "max", 3), (257, torch.int32, "max", 1)]):
+        xs = inputs.uniform_ranks(n, count, dtype, seed=40 + i)
+        send = to_dev(xs, pad)
+        recv = empty_dev(n, count, dtype, pad)
+        V.vAllReduce(send, recv, count, dtype, op, comm)
+        cases.append((xs, op, send, recv))           # the inputs must live until the group ends
+    V.vcommGroupEnd(comm)
+    torch.cuda.synchronize()
+    assert V.vcommGetAsyncError(comm) == V.vSuccess
+    for xs, op, _, recv in cases:
+        assert_bits_equal(recv, oracle.allreduce(xs, op), f"group element path {xs[0].dtype} {op}")
+
+
 def test_group_runs_nothing_before_end(comm):
     n, count = 8, 4096
     xs = inputs.uniform_ranks(n, count, torch.float32, 3)

@@ -90,6 +90,8 @@ struct RingArgs {
     Status* status;                  // device copy
     volatile Status* statusHost;     // pinned mirror
     int testStallRank;               // test hook: this rank never posts data (-1 = off)
+    unsigned int testJitterNs;       // test hook: random sleeps up to this long where the
+                                     // protocols publish or observe a slot (0 = off)
 };
 
 // Double-binary-tree all-reduce.  prog[t] lists tree t's ranks in post-order (children

@@ -143,6 +143,7 @@ extern "C" vResult_t vAllReduceNoAlloc(const void* const* sendbuffs, void* const
     a.status = reinterpret_cast<vc::Status*>(base);
     a.statusHost = nullptr;
     a.testStallRank = -1;
+    a.testJitterNs = 0;
     const cudaError_t e =
         vc::launch_ring(a, datatype, op, datatype, (vProto_t)p.proto, p.gridCtas, p.threadsPerCta, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {

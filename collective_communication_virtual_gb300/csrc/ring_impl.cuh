@@ -142,6 +142,19 @@ struct RingCtx {
     unsigned int sendSeq, recvSeq;
 };
 
+// Test hook (RingArgs::testJitterNs): a pseudo-random sleep of up to testJitterNs
+// nanoseconds, different per thread and call, so that tests see other interleavings of
+// data stores, flag stores and flag reads than the usual ones.  Off (one uniform branch)
+// when testJitterNs is 0.
+__device__ __forceinline__ void test_jitter(const RingArgs& a, unsigned salt) {
+    if (a.testJitterNs == 0u) return;
+    unsigned h = (unsigned)clock() ^ (salt * 0x9E3779B9u) ^ (threadIdx.x * 0x85EBCA6Bu) ^ (blockIdx.x * 0xC2B2AE35u);
+    h ^= h >> 15;
+    h *= 0x2C1B3C6Du;
+    h ^= h >> 12;
+    __nanosleep(h % a.testJitterNs);
+}
+
 // Spin until *p >= target (monotonic 64-bit counters).  Bounded.
 static __device__ __noinline__ bool wait_counter(const RingArgs& a, const RingCtx& c,
                                           const unsigned long long* p, unsigned long long target,
@@ -224,6 +237,7 @@ __device__ __forceinline__ bool wait_ll(const RingArgs& a, const RingCtx& c, con
 // then agrees on success.
 template <int PROTO>
 __device__ __forceinline__ bool slot_begin(const RingArgs& a, const RingCtx& c, int kind) {
+    test_jitter(a, c.recvSeq * 3u + c.sendSeq);
     bool fail = false;
     if (threadIdx.x == 0) {
         if (PROTO == vProtoSimple && (kind & kRecv))
@@ -294,6 +308,7 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
                     store_unit<DT, OUT, 16, 16>(out + u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
                 if (kind & kSend) st_cg(ss + u * 16, x);
             }
+            test_jitter(a, (unsigned)u0);
         }
     } else if (PROTO == vProtoLL) {
         // 8 payload bytes per unit, stored as two {data, flag} 64-bit words.
@@ -336,6 +351,7 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
                     store_unit<DT, OUT, 8, 8>(out + u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
                 if (kind & kSend) st_volatile_u64x2(ss + u * 16, sflag | x.x, sflag | x.y);
             }
+            test_jitter(a, (unsigned)u0);
         }
     } else {
         // LL128: 128-byte lines of 120 payload bytes + an 8-byte flag.  Eight lanes share a
@@ -408,8 +424,10 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
                         if (kind & kSend) st_cg8(ss + L * 128 + 112, make_uint2(x.x, x.y));
                     }
                 }
+                test_jitter(a, (unsigned)L0);
             }
             if (kind & kSend) {
+                test_jitter(a, 0x5157u);
                 __syncwarp();
                 __threadfence();
                 if (t == 7)

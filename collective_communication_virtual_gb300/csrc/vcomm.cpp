@@ -7,6 +7,7 @@
 // (NCCL book section 2.1, asyncResult).  The communicator carries start/end magic words
 // like ncclComm so a destroyed or foreign handle is refused.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdio>
@@ -87,6 +88,7 @@ struct vcomm {
     unsigned long long* ctrl;
     unsigned int epoch;
     int testStallRank;
+    unsigned int testJitterNs;
     StreamEvent tracked[kTrackedStreams];   // per stream; reused round-robin when full
     unsigned int trackedNext;
     // group batching
@@ -107,6 +109,16 @@ size_t elem_size(int dt) {
     default: return 0;
     }
 }
+
+// An NVTX range around every entry point that enqueues work, named after it, for Nsight
+// Systems and other NVTX-aware tools (NCCL marks its API the same way, NCCL book section
+// 2.1).  Header-only NVTX: with no tool attached a range costs a few nanoseconds.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool comm_ok(const vcomm* c) {
     return c != nullptr && c->startMagic == kMagic && c->endMagic == kMagic;
@@ -414,6 +426,7 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
     a.status = c->statusDev;
     a.statusHost = c->statusHostDev;
     a.testStallRank = c->testStallRank;
+    a.testJitterNs = c->testJitterNs;
     e = vc::launch_ring(a, dt, op, outType, (vProto_t)p.proto, p.gridCtas, p.threadsPerCta, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
@@ -625,6 +638,7 @@ vResult_t vcommGroupStart(vcomm_t c) {
 }
 
 vResult_t vcommGroupEnd(vcomm_t c) {
+    NvtxRange nvtx_("vcommGroupEnd");
     if (!comm_ok(c)) return vInvalidArgument;
     if (c->groupDepth == 0) return vInvalidUsage;
     if (--c->groupDepth > 0) return vSuccess;
@@ -705,6 +719,12 @@ vResult_t vcommTestSetStallRank(vcomm_t c, int rank) {
     return vSuccess;
 }
 
+vResult_t vcommTestSetJitterNs(vcomm_t c, unsigned int maxNs) {
+    if (!comm_ok(c) || maxNs > 1000000u) return vInvalidArgument;
+    c->testJitterNs = maxNs;
+    return vSuccess;
+}
+
 vResult_t vcommQueryPlan(vcomm_t c, vColl_t coll, size_t count, vDataType_t dt, int aligned,
                          vPlanInfo_t* plan) {
     if (!comm_ok(c) || !plan) return vInvalidArgument;
@@ -713,6 +733,7 @@ vResult_t vcommQueryPlan(vcomm_t c, vColl_t coll, size_t count, vDataType_t dt, 
 
 vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
                      vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vAllReduce");
     Front f = front(c, send, recv, count, dt, 0, true);
     if (f.res != vSuccess || count == 0) return f.res;
     if (!valid_op(op)) return vInvalidArgument;
@@ -786,6 +807,7 @@ vResult_t vAllReduce(const void* const* send, void* const* recv, size_t count, v
 static vResult_t reduce_scatter_impl(const void* const* send, void* const* recv, size_t rc,
                                      vDataType_t dt, vRedOp_t op, vDataType_t outType, bool hasScale,
                                      float scale, vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vReduceScatter");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -829,6 +851,7 @@ vResult_t vReduceScatterScaleCast(const void* const* send, void* const* recv, si
 
 vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcount, vDataType_t dt,
                      vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vAllGather");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -856,6 +879,7 @@ vResult_t vAllGather(const void* const* send, void* const* recv, size_t sendcoun
 
 vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
                      vRedOp_t op, int root, vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vBroadcast");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -889,6 +913,7 @@ vResult_t vBroadcast(const void* const* send, void* const* recv, size_t count, v
 
 vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vDataType_t dt,
                     vRedOp_t op, vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vAllToAll");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -911,6 +936,7 @@ vResult_t vAllToAll(const void* const* send, void* const* recv, size_t count, vD
 
 vResult_t vReduce(const void* const* send, void* const* recv, size_t count, vDataType_t dt, vRedOp_t op,
                   int root, vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vReduce");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -936,6 +962,7 @@ vResult_t vReduce(const void* const* send, void* const* recv, size_t count, vDat
 
 vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, vDataType_t dt, int root,
                   vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vGather");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -963,6 +990,7 @@ vResult_t vGather(const void* const* send, void* const* recv, size_t sendcount, 
 
 vResult_t vScatter(const void* const* send, void* const* recv, size_t recvcount, vDataType_t dt, int root,
                    vcomm_t c, cudaStream_t stream) {
+    NvtxRange nvtx_("vScatter");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);
@@ -988,6 +1016,7 @@ vResult_t vScatter(const void* const* send, void* const* recv, size_t recvcount,
 vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* counts,
                      const int32_t* sdispls, const int32_t* rdispls, vDataType_t dt, vcomm_t c,
                      cudaStream_t stream) {
+    NvtxRange nvtx_("vAllToAllv");
     if (comm_ok(c) && c->groupDepth > 0) {
         auto s_ = copy_ptrs(send, c->nRanks);
         auto r_ = copy_ptrs(recv, c->nRanks);

@@ -98,6 +98,7 @@ _SIGNATURES = {
     "vAllToAll": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vcommCount": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "vcommTestSetJitterNs": ([ctypes.c_void_p, ctypes.c_uint], ctypes.c_int),
     "vAllToAllv": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vReduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -270,6 +271,10 @@ def vcommSetTimeoutMs(comm, ms: int) -> None:
 
 def vcommTestSetStallRank(comm, rank: int) -> None:
     _check(lib().vcommTestSetStallRank(comm, rank), "vcommTestSetStallRank")
+
+
+def vcommTestSetJitterNs(comm, max_ns: int) -> None:
+    _check(lib().vcommTestSetJitterNs(comm, max_ns), "vcommTestSetJitterNs")
 
 
 def vcommQueryPlan(comm, coll: int, count: int, datatype, aligned: int = 32) -> dict:

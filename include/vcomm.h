@@ -357,6 +357,12 @@ vResult_t vPlanChannelRange(const vPlanInfo_t* plan, size_t count, int channel, 
  * transfer ends with the sticky error vTimeout.  -1 turns the hook off. */
 vResult_t vcommTestSetStallRank(vcomm_t comm, int rank);
 
+/* Test hook: staged ring transfers sleep for pseudo-random times of up to maxNs
+ * nanoseconds (0 = off, at most 1,000,000) where a producer publishes a slot and where a
+ * consumer observes one, so that tests exercise orderings of stores and flag reads that
+ * rarely occur on their own.  Results must not change. */
+vResult_t vcommTestSetJitterNs(vcomm_t comm, unsigned int maxNs);
+
 /* Links of `rank` in tree `tree` (0 or 1) of the double binary tree over nRanks ranks
  * (NCCL book chapter 4, ncclGetBtree / ncclGetDtree): tree 0 hangs from rank 0, a
  * rank's lowest set bit fixes its level; tree 1 mirrors it (rank r -> nRanks-1-r) for an

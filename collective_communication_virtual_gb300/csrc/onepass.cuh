@@ -39,6 +39,42 @@ __device__ __forceinline__ ChannelSpan channel_span(const OnePassArgs& a, int ch
     return s;
 }
 
+// The all-reduce element path for 2-byte types whose outputs all sit at one offset from a
+// 16-byte boundary: 16-byte vectors aligned to the outputs, cut from the inputs
+// (reduce_vec_ring_realign).  A (block, channel) range has one item per vector plus item 0,
+// which takes the elements before the first output boundary and after the last vector.
+template <int DT, int OP>
+__device__ __forceinline__ void allreduce_realigned16(const OnePassArgs& a, int N, int ch, int cta, size_t stride,
+                                                      size_t chEnd, int r0, int r1) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    const size_t lo = min((size_t)ch * a.chanElems, a.blockElems);
+    const size_t items = (chEnd - lo) / 8 + 2;
+    for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < items * (size_t)N; j += stride) {
+        const int b = (int)(j / items);
+        const size_t i = j - (size_t)b * items;
+        const size_t base = (size_t)b * a.blockElems;
+        const size_t x0 = base + lo, x1 = min(base + chEnd, a.count);
+        if (x0 >= x1) continue;
+        const uintptr_t d0 = (uintptr_t)((const char*)a.recv[r0] + x0 * ESZ);
+        const size_t head = min((size_t)(((16u - (d0 & 15u)) & 15u) / ESZ), x1 - x0);
+        const size_t nv = (x1 - x0 - head) / 8;
+        const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
+        const int first = ob + 1 == N ? 0 : ob + 1;
+        if (i == 0) {
+            for (size_t x = x0; x < x1; x++) {
+                if (x == x0 + head) x += 8 * nv;
+                if (x >= x1) break;
+                const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, x);
+                for (int r = r0; r < r1; r++) st_elem<ESZ>(a.recv[r], x, acc);
+            }
+        } else if (i - 1 < nv) {
+            const size_t e = x0 + head + 8 * (i - 1);
+            const uint4 acc = reduce_vec_ring_realign<DT, OP>(a.send, N, first, e * ESZ);
+            for (int r = r0; r < r1; r++) st_stream((char*)a.recv[r] + e * ESZ, acc);
+        }
+    }
+}
+
 // All-reduce, and reduce to root.  grid = nChannels * ctasPerChannel.  VB: 0 (element
 // path), 16 or 32 bytes per vector; the 32-byte kernel keeps twice the registers, so it
 // runs one 512-thread CTA per SM instead of two.  Reduce to root (a.orderRoot = a.outRoot
@@ -57,41 +93,13 @@ k_allreduce_onepass(const __grid_constant__ OnePassArgs a) {
     const int r0 = a.outRoot >= 0 ? a.outRoot : 0;
     const int r1 = a.outRoot >= 0 ? a.outRoot + 1 : N;
     if constexpr (VB == 0 && ESZ == 2) {
-      bool sameOut = true;         // every output at the same offset from a 16-byte boundary
-      for (int r = r0 + 1; r < r1; r++)
-          sameOut = sameOut && ((((uintptr_t)a.recv[r]) ^ (uintptr_t)a.recv[r0]) & 15u) == 0;
-      if (sameOut) {
-        // 2-byte elements off 16 bytes: 16-byte vectors aligned to the outputs, cut from the
-        // inputs (reduce_vec_ring_realign).  Item 0 of a (block, channel) range takes the
-        // elements before the first output boundary and after the last whole vector.
-        const size_t lo = min((size_t)ch * a.chanElems, a.blockElems);
-        const size_t items = (chEnd - lo) / 8 + 2;
-        for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < items * (size_t)N; j += stride) {
-            const int b = (int)(j / items);
-            const size_t i = j - (size_t)b * items;
-            const size_t base = (size_t)b * a.blockElems;
-            const size_t x0 = base + lo, x1 = min(base + chEnd, a.count);
-            if (x0 >= x1) continue;
-            const uintptr_t d0 = (uintptr_t)((const char*)a.recv[r0] + x0 * ESZ);
-            const size_t head = min((size_t)(((16u - (d0 & 15u)) & 15u) / ESZ), x1 - x0);
-            const size_t nv = (x1 - x0 - head) / 8;
-            const int ob = a.orderRoot >= 0 ? a.orderRoot : b;
-            const int first = ob + 1 == N ? 0 : ob + 1;
-            if (i == 0) {
-                for (size_t x = x0; x < x1; x++) {
-                    if (x == x0 + head) x += 8 * nv;
-                    if (x >= x1) break;
-                    const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, x);
-                    for (int r = r0; r < r1; r++) st_elem<ESZ>(a.recv[r], x, acc);
-                }
-            } else if (i - 1 < nv) {
-                const size_t e = x0 + head + 8 * (i - 1);
-                const uint4 acc = reduce_vec_ring_realign<DT, OP>(a.send, N, first, e * ESZ);
-                for (int r = r0; r < r1; r++) st_stream((char*)a.recv[r] + e * ESZ, acc);
-            }
+        bool sameOut = true;       // every output at the same offset from a 16-byte boundary
+        for (int r = r0 + 1; r < r1; r++)
+            sameOut = sameOut && ((((uintptr_t)a.recv[r]) ^ (uintptr_t)a.recv[r0]) & 15u) == 0;
+        if (sameOut) {
+            allreduce_realigned16<DT, OP>(a, N, ch, cta, stride, chEnd, r0, r1);
+            return;
         }
-        return;
-      }
     }
     if (VB == 0) {
         // element path: warp tiles of 32 * kElemsPerThread elements of one block

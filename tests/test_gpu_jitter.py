@@ -61,7 +61,9 @@ def test_ring_results_do_not_depend_on_timing(proto, n, channels):
 
 
 def test_jitter_hook_reaches_the_kernels():
-    # sleeps of up to 20 us at every slot make the ring measurably slower; the limits hold
+    # sleeps of up to 200 us at every slot make the ring measurably slower (a sleep lasts
+    # anywhere from 0 to about twice its request, so the check leaves wide room); the
+    # limits hold
     n, count = 8, 65_536
     c = V.vcommInit(n, 1, V.vProtoSimple)
     try:
@@ -83,10 +85,10 @@ def test_jitter_hook_reaches_the_kernels():
             return a.elapsed_time(b)
 
         plain = timed()
-        V.vcommTestSetJitterNs(c, 20_000)
+        V.vcommTestSetJitterNs(c, 200_000)
         jittered = timed()
         V.vcommTestSetJitterNs(c, 0)
-        assert jittered > 2 * plain, (plain, jittered)
+        assert jittered > 1.5 * plain, (plain, jittered)
         assert V.vcommGetAsyncError(c) == V.vSuccess
     finally:
         V.vcommDestroy(c)

@@ -566,6 +566,13 @@ def other_workloads(torch, V, dev, stream, hbm, only=None):
         row(name, fn, nbytes, S, factor, 10)
         if name in out:
             literal(out[name], lit * S, out[name]["us"] / 1e6)
+    # the same all-reduce with 128 KiB chunks: FIFOs small enough to stay in L2
+    V.vcommSetChunkBytes(ring, 128 << 10)
+    row("ring_allreduce_fp32_64MiB_simple_32ch_128KiB_chunks",
+        lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 2 * n * S, S, 2 * f1, 10)
+    if "ring_allreduce_fp32_64MiB_simple_32ch_128KiB_chunks" in out:
+        row_ = out["ring_allreduce_fp32_64MiB_simple_32ch_128KiB_chunks"]
+        literal(row_, (6 * n - 4) * S, row_["us"] / 1e6)
     V.vcommDestroy(ring)
     tree = V.vcommInit(n, 1, V.vProtoSimple)
     V.vcommSetAlgo(tree, "tree")

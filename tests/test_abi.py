@@ -44,6 +44,10 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
     for n in declared_functions():
         assert getattr(lib, n) is not None
+    # and the other way round: every unmangled function the library exports is declared
+    text_syms = {line.split()[-1] for line in out.splitlines() if len(line.split()) == 3 and line.split()[1] == "T"}
+    undeclared = sorted(n for n in text_syms if not n.startswith("_Z") and n not in declared_functions())
+    assert not undeclared, undeclared
 
 
 def test_header_compiles_as_plain_c(tmp_path):

@@ -336,6 +336,24 @@ def test_scale_cast_epilogue():
         assert torch.equal(a.float() * n, b.float())
 
 
+def test_scale_cast_epilogue_rounds_once_in_fp32():
+    # a scale that is not a power of two rounds: out = fp32(acc) * fp32(scale), one RNE
+    # multiply, which numpy's float32 product computes independently of the oracle
+    import numpy as np
+    n = 3
+    xs = inputs.uniform_ranks(n, n * 4000, torch.bfloat16, 13)
+    rs = oracle.reduce_scatter(xs, "sum")
+    scale = float(np.float32(1.0) / np.float32(3.0))
+    out = oracle.reduce_scatter_scale(xs, "sum", scale, torch.float32)
+    for a, b in zip(out, rs):
+        want = b.float().numpy().astype(np.float32) * np.float32(scale)
+        assert np.array_equal(a.numpy().view(np.int32), want.view(np.int32))
+    # and the bf16 output is that fp32 value rounded to bf16 (torch's RNE converter)
+    out_bf = oracle.reduce_scatter_scale(xs, "sum", scale, torch.bfloat16)
+    for a, b in zip(out_bf, out):
+        assert torch.equal(a.view(torch.int16), b.to(torch.bfloat16).view(torch.int16))
+
+
 def test_threads_do_not_change_bits():
     xs = inputs.uniform_ranks(8, 100_003, torch.bfloat16, 6)
     a = oracle.allreduce(xs, "sum", nthreads=1)

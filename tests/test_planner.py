@@ -180,6 +180,17 @@ def test_32_byte_vectors_when_blocks_and_pointers_allow():
     assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1, persistentGrid=1).gridCtas == 2 * 152
 
 
+def test_element_path_threads_take_8_elements_of_every_rank():
+    # pointers off 16 bytes: no vectors; one thread per 8 elements of every rank
+    p = plan(count=1 << 20, aligned16=0)                       # B = 131,072
+    assert p.vecBytes == 0 and p.threadsPerCta == 256
+    assert p.gridCtas == (131_072 // 8) * 8 // 256
+    # a ragged reduce-scatter block of 1,048,577 elements: 131,073 threads per block
+    p = plan(coll=V.vCollReduceScatter, count=(1 << 20) + 1)
+    assert p.vecBytes == 0 and p.threadsPerCta == 128
+    assert p.gridCtas == -(-131_073 * 8 // 128)
+
+
 def test_copy_threads_follow_how_often_a_loaded_byte_is_stored():
     # 8 MiB blocks, 8 ranks: 32 KiB tiles.  All-gather and broadcast store every loaded byte
     # 8 times: 32 bytes of a tile per thread (capped at 512 threads).  Gather, scatter and

@@ -180,6 +180,37 @@ def test_32_byte_vectors_when_blocks_and_pointers_allow():
     assert plan(coll=V.vCollAllGather, count=1 << 24, aligned32=1, noBulkCopy=1, persistentGrid=1).gridCtas == 2 * 152
 
 
+def test_tree_programs_fit_the_run_time_kernels_stack():
+    # The run-time tree kernel keeps the newest partial in registers and the partials
+    # waiting for their parent on a shared-memory stack of 8 entries per thread.  Walk
+    # both trees' post-order programs for every rank count up to 64 and bound that stack.
+    worst = 0
+    for n in range(1, 65):
+        for t in range(2):
+            links = {v: V.vPlanTreeLinks(n, v, t) for v in range(n)}
+            roots = [v for v in range(n) if links[v][0] < 0]
+            assert len(roots) == 1
+            prog = []
+
+            def visit(v):
+                kids = [k for k in links[v][1:] if k >= 0]
+                for k in kids:
+                    visit(k)
+                prog.append(len(kids))
+
+            visit(roots[0])
+            assert len(prog) == n
+            below = 0                 # partials below the register-held top
+            for i, c in enumerate(prog):
+                if c == 2:
+                    below -= 1
+                elif c == 0 and i > 0:
+                    below += 1
+                assert below >= 0
+                worst = max(worst, below)
+    assert worst <= 8, worst
+
+
 def test_element_path_threads_take_8_elements_of_every_rank():
     # pointers off 16 bytes: no vectors; one thread per 8 elements of every rank
     p = plan(count=1 << 20, aligned16=0)                       # B = 131,072

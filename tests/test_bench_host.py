@@ -1,5 +1,6 @@
 """Host logic of bench.py that needs no GPU: the multi-replica time aggregation (two gloo
-ranks on CPU) and the JSON contract of the reference arm's helpers."""
+ranks on CPU), the clock summary, and the JSON line of the reference arm (the oracle on
+the host cores)."""
 from __future__ import annotations
 
 import os
@@ -53,3 +54,23 @@ def test_clock_summary_parses_nvidia_smi_lines():
                "garbage"]
     s = c.summary()
     assert s["samples"] == 2 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    import argparse
+    import json
+
+    import oracle
+    oracle.build()
+    args = argparse.Namespace(gpus=1, steps=1, warmup=3, impl="reference")
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["value"] > 0
+    assert line["config"]["workload"] == bench.WORKLOAD
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0

@@ -226,6 +226,52 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     const size_t rc = a.blockElems;
     const bool hasScale = a.hasScale != 0;
     const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, rc);
+    if constexpr (VB == 0 && ESZ == 2) {
+        // 2-byte blocks off 16 bytes (a ragged block): 16-byte vectors aligned to the
+        // inputs, which every rank shares when its buffer starts on a 16-byte boundary, so
+        // the loads are those of the vector path; the 8 results are stored one by one (the
+        // outputs are 1/N of the traffic).  Item 0 of a (block, channel) range takes the
+        // elements before the first input boundary and after the last whole vector.
+        const size_t lo = min((size_t)ch * a.chanElems, rc);
+        const size_t span = chEnd - lo;
+        const size_t items = span / 8 + 2;
+        for (size_t j = (size_t)cta * blockDim.x + threadIdx.x; j < items * (size_t)N; j += stride) {
+            const int r = (int)(j / items);
+            const size_t i = j - (size_t)r * items;
+            const size_t base = (size_t)r * rc;
+            const int first = r + 1 == N ? 0 : r + 1;
+            const uintptr_t s0 = (uintptr_t)a.send[first] + (base + lo) * ESZ;
+            const size_t head = min((size_t)(((16u - (s0 & 15u)) & 15u) / ESZ), span);
+            const size_t nv = (span - head) / 8;
+            if (i == 0) {
+                for (size_t t = lo; t < chEnd; t++) {
+                    if (t == lo + head) t += 8 * nv;
+                    if (t >= chEnd) break;
+                    const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, base + t);
+                    store_epilogue_elem<DT, OUT>(a.recv[r], t, acc, hasScale, a.scale);
+                }
+            } else if (i - 1 < nv) {
+                const size_t t = lo + head + 8 * (i - 1);
+                const size_t boff = (base + t) * ESZ;
+                bool aligned = true;
+                for (int k = 0; k < N; k++) aligned = aligned && (((uintptr_t)a.send[k] + boff) & 15u) == 0;
+                if (aligned) {
+                    const uint4 acc = reduce_vec_ring<DT, OP, 16>(a.send, N, first, boff);
+                    const uint32_t w[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                    for (int k = 0; k < 8; k++)
+                        store_epilogue_elem<DT, OUT>(a.recv[r], t + k, (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu,
+                                                     hasScale, a.scale);
+                } else {
+                    for (int k = 0; k < 8; k++) {
+                        const uint32_t acc = reduce_elem_ring<DT, OP>(a.send, N, first, base + t + k);
+                        store_epilogue_elem<DT, OUT>(a.recv[r], t + k, acc, hasScale, a.scale);
+                    }
+                }
+            }
+        }
+        return;
+    }
     if (VB == 0) {
         // element path: warp tiles of 32 * kElemsPerThread elements of one block
         constexpr int TILE = 32 * kElemsPerThread;

@@ -350,3 +350,46 @@ def test_ring_threads_follow_the_protocol_thread_thresholds():
     # 16 KiB per rank, one channel: 2 KiB steps -> Simple wants 32 threads (floor 64), LL 256
     assert plan(algo=V.vAlgoRing, proto=V.vProtoSimple, count=4096).threadsPerCta == 64
     assert plan(algo=V.vAlgoRing, proto=V.vProtoLL, count=4096).threadsPerCta == 256
+
+
+def test_every_plan_is_launchable():
+    # Sweep collectives, rank counts, channel counts, sizes, types, alignment and grid
+    # shape: every plan must describe a launch the kernels accept.
+    colls = [V.vCollAllReduce, V.vCollReduceScatter, V.vCollAllGather, V.vCollBroadcast, V.vCollAllToAll,
+             V.vCollAllToAllv, V.vCollReduce, V.vCollGather, V.vCollScatter]
+    counts = [1, 7, 1000, 4097, 65_536, 1_000_003, 1 << 24, (1 << 31) + 5]
+    n_checked = 0
+    for coll in colls:
+        for n in (1, 2, 3, 8, 16, 64):
+            for nch in (1, 3, 32):
+                for count in counts:
+                    for dt in (V.vFloat32, V.vBFloat16):
+                        for a16, a32, persistent in ((1, 1, 0), (1, 0, 0), (0, 0, 0), (1, 1, 1)):
+                            for algo in (V.vAlgoAuto, V.vAlgoRing, V.vAlgoTree):
+                                p = plan(coll=coll, nRanks=n, nChannels=nch, count=count, datatype=dt,
+                                         aligned16=a16, aligned32=a32, persistentGrid=persistent, algo=algo,
+                                         noBulkCopy=1)
+                                n_checked += 1
+                                assert 1 <= p.gridCtas <= (1 << 30), (coll, n, nch, count)
+                                assert p.threadsPerCta in (32, 64, 128, 256, 512), p.threadsPerCta
+                                assert p.vecBytes in (0, 16, 32)
+                                if not a16:
+                                    assert p.vecBytes == 0
+                                if not a32:
+                                    assert p.vecBytes != 32
+                                if p.algo == V.vAlgoRing:
+                                    assert p.gridCtas == p.nChannels * n
+                                    assert p.slotBytes >= 1024 and p.slotBytes % 256 == 0
+                                    assert p.fifoBytes == 8 * p.slotBytes
+                                    assert p.slotPayloadElems >= 1 and p.chunkElems >= p.slotPayloadElems
+                                elif p.algo == V.vAlgoOnePass and coll in (V.vCollAllGather, V.vCollBroadcast,
+                                                                           V.vCollAllToAll, V.vCollGather,
+                                                                           V.vCollScatter):
+                                    assert 2048 <= p.tileBytes <= 65_536
+                                    assert p.tileBytes & (p.tileBytes - 1) == 0
+                                if p.vecBytes and coll in (V.vCollAllReduce, V.vCollReduce):
+                                    # all-reduce blocks follow alignUp(ceil(count/N), 16/esz), so a
+                                    # vector never straddles two blocks
+                                    esz = 4 if dt == V.vFloat32 else 2
+                                    assert (p.blockElems * esz) % 16 == 0
+    assert n_checked > 10_000

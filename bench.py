@@ -9,6 +9,12 @@ the kernel's minimum traffic (read N*S + write N*S) reaches.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
   python bench.py --workloads [--only NAME]      # the other collectives' workloads only
 
+Output: one JSON line per side measurement (size sweeps, the staged ring's protocol and
+channel grids, the other collectives' workloads, the oracle's per-workload timings), each
+{"extra": name, ...}, then the headline as the LAST line: the contract keys, the
+roofline of the all-reduce kernel, the clocks, e2e and cpu_baseline, under 2,000
+characters.
+
 --impl reference times the CPU oracle (the plain order-matched C implementation) on the
 host cores for the same workload.  With --gpus N > 1 (under torchrun) every GPU runs an
 independent replica of the workload (the virtual ranks never span GPUs); the value is
@@ -157,6 +163,27 @@ def job_busbw(world, t_max):
     return world * BYTES_PER_RANK / t_max * bus_factor(N_RANKS) / 1e9
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), e.g. "Neoverse-V2"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                name = line.split(":", 1)[1].strip()
+                if name and name != "-":
+                    return name
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -190,7 +217,8 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
             "config": {"workload": WORKLOAD, "n_ranks": N_RANKS, "bytes_per_rank": BYTES_PER_RANK},
             "cpu_baseline": {"value": busbw, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": "the whole workload per step (8 x 64 MiB fp32)"},
+                             "sample": "the whole workload per step (8 x 64 MiB fp32)",
+                             "cpu_model": cpu_model()},
             "e2e": {"value": busbw, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -222,19 +250,30 @@ def load(V, torch, comm, send, recv, stream, seconds):
         torch.cuda.synchronize()
 
 
-def cpu_baseline_sample(torch):
+def oracle_rate(torch, xs, nthreads, seconds):
+    """busBW of the oracle's all-reduce over `xs` on `nthreads` host threads, repeated for
+    about `seconds` (at least twice): (GB/s, runs)."""
     import oracle
+    oracle.allreduce(xs, "sum", nthreads=nthreads)
+    reps, t0 = 0, time.perf_counter()
+    while reps < 2 or (time.perf_counter() - t0 < seconds and reps < 1000):
+        oracle.allreduce(xs, "sum", nthreads=nthreads)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    return BYTES_PER_RANK / dt * bus_factor(N_RANKS) / 1e9, reps
+
+
+def cpu_baseline_sample(torch):
+    """The oracle on the whole workload (8 x 64 MiB fp32 sum): on every host core the
+    process may use, and on one core; about 8 s of CPU work each."""
     from collective_communication_virtual_gb300 import inputs
     cores = len(os.sched_getaffinity(0))
     xs = inputs.uniform_ranks(N_RANKS, COUNT, torch.float32, 1)
-    oracle.allreduce(xs, "sum", nthreads=cores)
-    reps, t0 = 0, time.perf_counter()
-    while reps < 3 or (time.perf_counter() - t0 < 10.0 and reps < 1000):     # about 10 s of CPU work
-        oracle.allreduce(xs, "sum", nthreads=cores)
-        reps += 1
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": BYTES_PER_RANK / dt * bus_factor(N_RANKS) / 1e9, "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "sample": f"the whole workload (8 x 64 MiB fp32 sum), {reps} runs"}
+    value, reps = oracle_rate(torch, xs, cores, 8.0)
+    one, reps1 = oracle_rate(torch, xs, 1, 8.0)
+    return {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"whole workload (8 x 64 MiB fp32 sum), {reps} runs on {cores} threads, {reps1} on 1",
+            "single_thread": {"value": one, "cores": 1}, "cpu_model": cpu_model()}
 
 
 def cpu_baseline_workloads(torch):
@@ -278,12 +317,54 @@ def cpu_baseline_workloads(torch):
     return {"cores": cores, "kind": "oracle", "runs": 1, "workloads": out}
 
 
+HEADLINE_MAX_CHARS = 2000
+
+
+def make_headline(*, value, t_max, steps, warmup, world, plan, achieved, hbm, peak_kind, traffic, clocks,
+                  e2e, cpu_baseline, sample_ok, async_error):
+    """The contract line: the keys the driver reads, the roofline of the all-reduce kernel,
+    clocks, e2e and cpu_baseline -- nothing of the side measurements, which go on lines
+    of their own, so that it stays short."""
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_ranks": N_RANKS, "bytes_per_rank": BYTES_PER_RANK,
+                       "algo": "onepass", "grid_ctas": plan["gridCtas"],
+                       "threads_per_cta": plan["threadsPerCta"], "vector_bytes": plan["vecBytes"],
+                       "l2": "inputs larger than L2 (8 x 64 MiB read + 8 x 64 MiB written per step)",
+                       "parallelism": f"{world} independent replica(s) of 8 virtual ranks"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": plan["minBytes"],
+                         "kernel": "k_allreduce_onepass<f32,sum,32B,8 ranks>"},
+            "gpu_launches": steps,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu_baseline,
+            "parity_sample_ok": sample_ok,
+            "async_error": async_error}
+    return line
+
+
+def emit(extras, headline, out=None):
+    """Print every side measurement as its own JSON line, then the headline last."""
+    out = out or sys.stdout
+    for name, data in extras:
+        print(json.dumps({"extra": name, "data": data}), file=out)
+    text = json.dumps(headline)
+    if len(text) > HEADLINE_MAX_CHARS:
+        raise RuntimeError(f"headline is {len(text)} characters, over {HEADLINE_MAX_CHARS}")
+    print(text, file=out)
+    out.flush()
+
+
 def run_ours(args):
     import torch
 
     from collective_communication_virtual_gb300 import build, inputs, vcomm as V
 
     rank, world, local = dist_env()
+    dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
@@ -316,48 +397,36 @@ def run_ours(args):
         load(V, torch, comm, send, recv, stream, seconds=1.0)
         t = time_allreduce(V, torch, comm, send, recv, COUNT, args.steps, args.warmup, stream)
         load(V, torch, comm, send, recv, stream, seconds=0.5)
-        t_max = max_over_ranks(t, dist if world > 1 else None, dev)
+        t_max = max_over_ranks(t, dist, dev)
     err = V.vcommGetAsyncError(comm)
-    busbw_one = BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9
     value = job_busbw(world, t_max)
     achieved = plan["minBytes"] / t / 1e9
 
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "n_ranks": N_RANKS, "bytes_per_rank": BYTES_PER_RANK,
-                       "algo": "onepass", "channels": plan["nChannels"], "grid_ctas": plan["gridCtas"],
-                       "threads_per_cta": plan["threadsPerCta"], "vector_bytes": plan["vecBytes"],
-                       "l2": "inputs larger than L2 (8 x 64 MiB read + 8 x 64 MiB written per step)",
-                       "parallelism": f"{world} independent replica(s) of 8 virtual ranks"},
-            "hbm_frac": achieved / hbm,
-            "alg_bw_gbs": BYTES_PER_RANK / t / 1e9,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "traffic": profiled_traffic(),
-                         "algorithmic_bytes_per_launch": plan["minBytes"],
-                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
-            "gpu_launches": args.steps,
-            "clocks": clocks.summary(),
-            "parity_sample_ok": sample_ok,
-            "async_error": err}
-
+    # end to end through the public API with host buffers, every replica, slowest one
+    e2e = e2e_allreduce(torch, V, comm, xs, dev, stream, steps=max(3, min(args.steps, 10)), dist=dist,
+                        world=world)
+    extras = []
+    cpu = None
     if rank == 0 and not args.no_extras:
-        line["e2e"] = e2e_allreduce(torch, V, comm, xs, dev, stream, steps=max(3, min(args.steps, 10)))
-        line["sweep"] = sweep(torch, V, dev, stream, hbm)
-        line["sweep_collectives"] = sweep_collectives(torch, V, dev, hbm)
-        line["channel_sweep"] = channel_sweep(torch, V, send, recv, stream)
-        line["other_workloads"] = other_workloads(torch, V, dev, stream, hbm)
-        line["cpu_baseline"] = cpu_baseline_sample(torch)
-        line["cpu_baseline"]["other_workloads"] = cpu_baseline_workloads(torch)
-    elif not args.no_extras:
-        line["e2e"] = None
+        extras.append(("sweep_allreduce_onepass", sweep(torch, V, dev, stream, hbm)))
+        extras.append(("sweep_collectives_onepass", sweep_collectives(torch, V, dev, hbm)))
+        extras.append(("ring_sweep", ring_sweep(torch, V, dev)))
+        extras.append(("ring_allreduce_chunk_channel_grid", ring_grid(torch, V, send, recv, stream)))
+        extras.append(("other_workloads", other_workloads(torch, V, dev, stream, hbm)))
+    if rank == 0 and world == 1:
+        cpu = cpu_baseline_sample(torch)
+        if not args.no_extras:
+            extras.append(("cpu_baseline_other_workloads", cpu_baseline_workloads(torch)))
     V.vcommDestroy(comm)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
-        print(json.dumps(line))
+        line = make_headline(value=value, t_max=t_max, steps=args.steps, warmup=args.warmup, world=world,
+                             plan=plan, achieved=achieved, hbm=hbm, peak_kind=peak_kind,
+                             traffic=profiled_traffic(), clocks=clocks.summary(), e2e=e2e,
+                             cpu_baseline=cpu, sample_ok=sample_ok, async_error=err)
+        emit(extras, line)
     return 0
 
 
@@ -384,13 +453,16 @@ def check_sample(torch, V, xs, recv, n_samples=4096):
     return True
 
 
-def e2e_allreduce(torch, V, comm, xs, dev, stream, steps):
-    """Host buffers in, host buffers out, through vAllReduce.
+def e2e_allreduce(torch, V, comm, xs, dev, stream, steps, dist=None, world=1):
+    """The headline metric end to end: host buffers in, host buffers out, through
+    vAllReduce, on every replica; the slowest replica's time.
 
-    zero_copy (reported): the caller passes pinned host buffers straight to vAllReduce; the
-    kernel reads every rank's input from host memory and writes every rank's result back
-    over NVLink-C2C, all inside the timed region.  explicit_copies: H2D of all 8 inputs,
-    the kernel on device buffers, D2H of all 8 results, serialized on one stream."""
+    value (mode "zero-copy"): the caller hands vAllReduce pinned host buffers, which the
+    library accepts as they are; every step the kernel reads all 8 ranks' inputs from host
+    memory and writes all 8 results back to host memory over NVLink-C2C, inside the timed
+    region.  explicit_copies: per step, cudaMemcpyAsync of the 8 inputs to device buffers,
+    vAllReduce on them, and cudaMemcpyAsync of the 8 results back, serialised on one
+    stream.  Both move 8 x 64 MiB each way per step."""
     host_in = [x.pin_memory() for x in xs]
     host_out = [torch.empty_like(x).pin_memory() for x in xs]
     d_in = [torch.empty_like(x, device=dev) for x in xs]
@@ -409,24 +481,25 @@ def e2e_allreduce(torch, V, comm, xs, dev, stream, steps):
     def timed(fn):
         fn()
         torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for _ in range(steps):
             fn()
         stop.record(stream)
         torch.cuda.synchronize()
-        return start.elapsed_time(stop) / 1e3 / steps
+        return max_over_ranks(start.elapsed_time(stop) / 1e3 / steps, dist, dev)
 
     t = timed(zero_copy)
     t_copy = timed(explicit)
     consistent = all(torch.equal(host_out[r], d_out[r].cpu()) for r in range(N_RANKS))
     nbytes = N_RANKS * BYTES_PER_RANK
-    return {"value": BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9, "unit": "GB/s",
+    return {"value": job_busbw(world, t), "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "ms_per_step": t * 1e3,
-            "steps": steps, "mode": "zero-copy: kernel reads pinned host inputs and writes pinned "
-                                    "host outputs over NVLink-C2C",
-            "explicit_copies": {"value": BYTES_PER_RANK / t_copy * bus_factor(N_RANKS) / 1e9,
-                                "ms_per_step": t_copy * 1e3},
+            "steps": steps, "mode": "zero-copy: vAllReduce on pinned host buffers over NVLink-C2C",
+            "explicit_copies": {"value": job_busbw(world, t_copy), "ms_per_step": t_copy * 1e3},
             "results_match_device_path": consistent}
 
 
@@ -566,6 +639,15 @@ def other_workloads(torch, V, dev, stream, hbm, only=None):
         row(name, fn, nbytes, S, factor, 10)
         if name in out:
             literal(out[name], lit * S, out[name]["us"] / 1e6)
+    # the flag protocols on the same all-reduce (32 channels, 1 MiB chunks)
+    for proto, pname in ((V.vProtoLL, "ll"), (V.vProtoLL128, "ll128")):
+        name = f"ring_allreduce_fp32_64MiB_{pname}_32ch"
+        if want(name):
+            V.vcommSetProtocol(ring, proto)
+            row(name, lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 2 * n * S, S,
+                2 * f1, 10)
+            literal(out[name], (6 * n - 4) * S, out[name]["us"] / 1e6)
+    V.vcommSetProtocol(ring, V.vProtoSimple)
     # the same all-reduce with 128 KiB chunks: FIFOs small enough to stay in L2
     V.vcommSetChunkBytes(ring, 128 << 10)
     row("ring_allreduce_fp32_64MiB_simple_32ch_128KiB_chunks",
@@ -733,30 +815,124 @@ def sweep_collectives(torch, V, dev, hbm):
     return out
 
 
-def channel_sweep(torch, V, send, recv, stream):
-    """busBW of the one-pass kernel and the staged ring per channel count (and ring chunk
-    size); every configuration gives the same bits."""
-    out = []
-    cases = [("onepass", V.vProtoSimple, "simple", None)]
+RING_COLLS = ("allreduce", "reduce_scatter", "allgather", "broadcast")
+
+
+def ring_call(V, torch, coll, comm, send, recv, nbytes, n):
+    """(enqueue function, count argument, vColl_t) of one staged-ring collective whose
+    bytes per rank are `nbytes` (the send size; the receive size for all-gather)."""
+    elems = nbytes // 4
+    if coll == "allreduce":
+        s_, r_ = [x[:elems] for x in send], [x[:elems] for x in recv]
+        return (lambda st=None: V.vAllReduce(s_, r_, elems, torch.float32, "sum", comm, st)), elems, V.vCollAllReduce
+    if coll == "reduce_scatter":
+        s_, r_ = [x[:elems] for x in send], [x[:elems // n] for x in recv]
+        return (lambda st=None: V.vReduceScatter(s_, r_, elems // n, torch.float32, "sum", comm, st)), elems // n, \
+            V.vCollReduceScatter
+    if coll == "allgather":
+        s_, r_ = [x[:elems // n] for x in send], [x[:elems] for x in recv]
+        return (lambda st=None: V.vAllGather(s_, r_, elems // n, torch.float32, "sum", comm, st)), elems // n, \
+            V.vCollAllGather
+    s_, r_ = [x[:elems] for x in send], [x[:elems] for x in recv]
+    return (lambda st=None: V.vBroadcast(s_, r_, elems, torch.float32, "sum", 0, comm, st)), elems, V.vCollBroadcast
+
+
+def graph_us(torch, fn, launches, reps):
+    """Device time of one call: `launches` calls captured into a CUDA graph, replayed
+    `reps` times after one untimed replay (no host gaps between the kernels)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(launches):
+            fn(torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) * 1e3 / (reps * launches)
+
+
+def eager_us(torch, fn, warm, reps):
+    """Time of one call from CUDA events around `reps` back-to-back calls after `warm`."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st = torch.cuda.current_stream()
+    a.record(st)
+    for _ in range(reps):
+        fn(st)
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def ring_sweep(torch, V, dev, channels=(1, 8, 32), max_bytes=1 << 30):
+    """The staged ring (fp32 sum, 8 virtual ranks, the planner's default chunk) for
+    all-reduce, reduce-scatter, all-gather and broadcast x Simple/LL/LL128 x channel counts
+    x bytes per rank 1 KiB .. 1 GiB in powers of 4: device time (CUDA-graph replays up to
+    4 MiB per rank, back-to-back eager calls above) beside the planner's predictedUs.  The
+    data behind the planner's ring cost model."""
+    n = N_RANKS
+    top = max_bytes // 4
+    send = [torch.rand(top, device=dev) for _ in range(n)]
+    recv = [torch.empty(top, device=dev) for _ in range(n)]
+    rows = []
     for proto, pname in ((V.vProtoSimple, "simple"), (V.vProtoLL, "ll"), (V.vProtoLL128, "ll128")):
-        cases += [("ring", proto, pname, 128 << 10), ("ring", proto, pname, 2 << 20)]
-    for algo, proto, pname, chunk in cases:
+        for ch in channels:
+            comm = V.vcommInit(n, ch, proto)
+            V.vcommSetAlgo(comm, "ring")
+            for coll in RING_COLLS:
+                nbytes = 1024
+                while nbytes <= max_bytes:
+                    fn, count, code = ring_call(V, torch, coll, comm, send, recv, nbytes, n)
+                    try:
+                        if nbytes <= (4 << 20):
+                            t = graph_us(torch, fn, 20, 5)
+                        else:
+                            # Milliseconds per call: launch gaps do not matter, and an eager
+                            # call skips the FIFO clearing a captured LL/LL128 transfer does
+                            # before every replay.
+                            t = eager_us(torch, fn, 2 if nbytes <= (64 << 20) else 1, 3 if nbytes <= (64 << 20) else 2)
+                        pred = V.vcommQueryPlan(comm, code, count, torch.float32, 32)["predictedUs"]
+                        rows.append([coll, pname, ch, nbytes, round(t, 2), round(pred, 2)])
+                    except V.VcommError as e:
+                        rows.append([coll, pname, ch, nbytes, None, str(e)])
+                    nbytes *= 4
+            V.vcommDestroy(comm)
+    del send, recv
+    torch.cuda.empty_cache()
+    return {"columns": ["coll", "proto", "channels", "bytes_per_rank", "device_us", "model_us"],
+            "n_ranks": n, "dtype": "f32", "op": "sum", "chunk": "planner default", "rows": rows}
+
+
+def ring_grid(torch, V, send, recv, stream):
+    """The staged ring all-reduce at 8 x 64 MiB fp32 for every protocol x channels
+    {1, 8, 16, 32} x chunk bytes {128K .. 2M}: measured time (CUDA events, 3 calls after
+    one) beside the planner's predictedUs.  Every cell gives the same bits."""
+    rows = []
+    for proto, pname in ((V.vProtoSimple, "simple"), (V.vProtoLL, "ll"), (V.vProtoLL128, "ll128")):
         for ch in (1, 8, 16, 32):
             comm = V.vcommInit(N_RANKS, ch, proto)
-            V.vcommSetAlgo(comm, algo)
-            if chunk:
+            V.vcommSetAlgo(comm, "ring")
+            for chunk in (128 << 10, 256 << 10, 512 << 10, 1 << 20, 2 << 20):
                 V.vcommSetChunkBytes(comm, chunk)
-            try:
-                t = time_allreduce(V, torch, comm, send, recv, COUNT, 3, 1, stream)
-                pred = V.vcommQueryPlan(comm, V.vCollAllReduce, COUNT, torch.float32, 32)["predictedUs"]
-                out.append({"algo": algo, "proto": pname, "channels": ch, "chunk_bytes": chunk,
-                            "busbw_gbs": BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9,
-                            "measured_us": t * 1e6, "model_us": pred})
-            except V.VcommError as e:
-                out.append({"algo": algo, "proto": pname, "channels": ch, "chunk_bytes": chunk,
-                            "error": str(e)})
+                try:
+                    t = time_allreduce(V, torch, comm, send, recv, COUNT, 3, 1, stream)
+                    pred = V.vcommQueryPlan(comm, V.vCollAllReduce, COUNT, torch.float32, 32)["predictedUs"]
+                    rows.append([pname, ch, chunk, round(t * 1e6, 1), round(pred, 1),
+                                 round(BYTES_PER_RANK / t * bus_factor(N_RANKS) / 1e9, 1)])
+                except V.VcommError as e:
+                    rows.append([pname, ch, chunk, None, str(e), None])
             V.vcommDestroy(comm)
-    return out
+    return {"columns": ["proto", "channels", "chunk_bytes", "measured_us", "model_us", "busbw_gbs"],
+            "rows": rows}
 
 
 def run_workloads(only=None):
@@ -771,16 +947,36 @@ def run_workloads(only=None):
     return 0
 
 
+def run_ring_sweep():
+    """The staged ring's side measurements alone (the planner's calibration data)."""
+    import torch
+
+    from collective_communication_virtual_gb300 import build, vcomm as V
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    send = [torch.rand(COUNT, device=dev) for _ in range(N_RANKS)]
+    recv = [torch.empty(COUNT, device=dev) for _ in range(N_RANKS)]
+    grid = ring_grid(torch, V, send, recv, torch.cuda.current_stream())
+    del send, recv
+    torch.cuda.empty_cache()
+    emit([("ring_sweep", ring_sweep(torch, V, dev))], {"extra": "ring_allreduce_chunk_channel_grid", "data": grid})
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-extras", action="store_true", help="skip e2e, sweeps and the CPU baseline")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the side measurements (sweeps, grids, other workloads)")
     ap.add_argument("--workloads", action="store_true",
                     help="only time the other collectives (FSDP bucket, MoE dispatch, all-to-all, "
                          "reduce-scatter, all-gather, broadcast) and print them as one JSON line")
+    ap.add_argument("--ring-sweep", action="store_true",
+                    help="only time the staged ring's protocol x channel x size sweep and chunk grid")
     ap.add_argument("--only", default=None,
                     help="with --workloads: a comma-separated list of the workload names to run")
     args = ap.parse_args()
@@ -791,6 +987,8 @@ def main():
         return run_reference(args)
     if args.workloads:
         return run_workloads(args.only)
+    if args.ring_sweep:
+        return run_ring_sweep()
     return run_ours(args)
 
 

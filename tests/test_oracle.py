@@ -417,6 +417,16 @@ def test_btree_worked_example_golden(golden_dir):
     assert oracle.tree_links(n, rank, 0) == (parent, c0, c1)
 
 
+def test_tree_links_hand_worked_table(golden_dir):
+    # Both trees at 5, 6, 7 and 12 ranks, worked by hand from the ncclGetBtree rules and
+    # the ncclGetDtree mirror (even n) / shift (odd n): the up >= n fallback, the shrinking
+    # second-child step and the root's single child are all exercised.
+    rows = _read_rows(os.path.join(golden_dir, "btree_links.txt"))
+    assert sorted({r[0] for r in rows}) == [5, 6, 7, 12] and len(rows) == 2 * (5 + 6 + 7 + 12)
+    for n, tree, rank, parent, c0, c1 in rows:
+        assert oracle.tree_links(n, rank, tree) == (parent, c0, c1), (n, tree, rank)
+
+
 @pytest.mark.parametrize("tree", [0, 1])
 def test_trees_are_spanning_trees(tree):
     for n in range(1, 65):

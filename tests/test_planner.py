@@ -302,6 +302,14 @@ def test_tree_links_match_the_pages_example_and_the_oracle(golden_dir):
                 assert V.vPlanTreeLinks(n, r, t) == oracle.tree_links(n, r, t), (n, t, r)
 
 
+def test_tree_links_match_the_hand_worked_table(golden_dir):
+    with open(os.path.join(golden_dir, "btree_links.txt")) as f:
+        rows = [list(map(int, l.split())) for l in f if l.strip() and not l.startswith("#")]
+    assert len(rows) == 60
+    for n, tree, rank, parent, c0, c1 in rows:
+        assert V.vPlanTreeLinks(n, rank, tree) == (parent, c0, c1), (n, tree, rank)
+
+
 def test_tree_plan():
     p = plan(algo=V.vAlgoTree, count=16 << 20)
     assert p.algo == V.vAlgoTree and p.blockElems == 8 << 20

@@ -58,9 +58,14 @@ struct A2AvArgs {
     Status* status;                  // device copy
     volatile Status* statusHost;     // pinned mirror
 };
-// Tile-counter pairs a communicator rotates through, so that variable all-to-alls in
-// flight at the same time (on different streams) use different counters.
+// Tile-counter pairs of a communicator.  Eager variable all-to-alls rotate through the
+// first kTileCounterSlots pairs, so that calls in flight at the same time (on different
+// streams) use different counters; a call captured into a CUDA graph keeps its pair for
+// every replay, so captured calls take theirs, one per captured call, from the next
+// kCapturedCounterSlots pairs, which eager calls never use.
 constexpr int kTileCounterSlots = 64;
+constexpr int kCapturedCounterSlots = 64;
+constexpr int kAllCounterSlots = kTileCounterSlots + kCapturedCounterSlots;
 
 // Staged ring kernels: one CTA per (channel, rank).
 struct RingArgs {

@@ -96,7 +96,8 @@ struct vcomm {
     std::vector<GroupRec>* group;
     vc::GroupArgs* groupArgs;        // host copy of a batch's parameter block
     unsigned int* tileCounters;      // variable all-to-all tile counters (device)
-    unsigned int tileCounterSeq;
+    unsigned int tileCounterSeq;     // eager calls: next pair of the rotating set
+    unsigned int capturedCounterSeq; // captured calls: next pair of the captured set
     unsigned long long endMagic;
 };
 
@@ -583,9 +584,9 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
     if ((e = cudaMemset(c->statusDev, 0, sizeof(vc::Status))) != cudaSuccess) goto fail;
     if ((e = cudaMalloc(&c->abortDev, sizeof(unsigned int))) != cudaSuccess) goto fail;
     if ((e = cudaMemset(c->abortDev, 0, sizeof(unsigned int))) != cudaSuccess) goto fail;
-    if ((e = cudaMalloc(&c->tileCounters, vc::kTileCounterSlots * 2 * sizeof(unsigned int))) != cudaSuccess)
+    if ((e = cudaMalloc(&c->tileCounters, vc::kAllCounterSlots * 2 * sizeof(unsigned int))) != cudaSuccess)
         goto fail;
-    if ((e = cudaMemset(c->tileCounters, 0, vc::kTileCounterSlots * 2 * sizeof(unsigned int))) != cudaSuccess)
+    if ((e = cudaMemset(c->tileCounters, 0, vc::kAllCounterSlots * 2 * sizeof(unsigned int))) != cudaSuccess)
         goto fail;
     if ((e = cudaHostAlloc(&c->statusHost, sizeof(vc::Status), cudaHostAllocMapped)) != cudaSuccess) goto fail;
     std::memset(c->statusHost, 0, sizeof(vc::Status));
@@ -1055,7 +1056,12 @@ vResult_t vAllToAllv(const void* const* send, void* const* recv, const int32_t* 
     a.nRanks = c->nRanks;
     a.elemSize = (int)esz;
     a.tileBytes = 64 * 1024;
-    a.tileCounter = c->tileCounters + 2 * (size_t)(c->tileCounterSeq++ % vc::kTileCounterSlots);
+    // A captured launch replays with the pair it was captured with: it takes one of the
+    // captured set, which eager launches never rotate into.
+    const size_t pair = stream_capturing(stream)
+                            ? vc::kTileCounterSlots + (size_t)(c->capturedCounterSeq++ % vc::kCapturedCounterSlots)
+                            : (size_t)(c->tileCounterSeq++ % vc::kTileCounterSlots);
+    a.tileCounter = c->tileCounters + 2 * pair;
     a.status = c->statusDev;
     a.statusHost = c->statusHostDev;
     return finish_launch(c, vc::launch_alltoallv(a, p.gridCtas, p.threadsPerCta, stream), stream, "alltoallv",

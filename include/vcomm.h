@@ -248,7 +248,14 @@ vResult_t vAllToAll(const void* const* sendbuffs, void* const* recvbuffs, size_t
  * (receives) nothing may pass a NULL send (receive) buffer, as an empty tensor has.  A
  * negative entry, or a positive count whose source or destination buffer is NULL, makes
  * the kernel skip that block and sets the sticky error vInvalidArgument.  Send and
- * receive buffers must not overlap. */
+ * receive buffers must not overlap.
+ * Each call hands out its tiles from a pair of counters that the communicator owns.
+ * Eager calls rotate through 64 pairs; a call captured into a CUDA graph keeps the pair
+ * it was captured with, taken from a second set of 64 that eager calls never use.  So an
+ * eager call may run on the GPU at the same time as a replay of a captured call, and up
+ * to 64 eager calls may be in flight together; beyond that, vAllToAllv kernels on one
+ * communicator must not overlap on the GPU (two replays of one graph, or of calls
+ * captured 64 captured calls apart, share a pair). */
 vResult_t vAllToAllv(const void* const* sendbuffs, void* const* recvbuffs, const int32_t* counts,
                      const int32_t* sdispls, const int32_t* rdispls, vDataType_t datatype,
                      vcomm_t comm, cudaStream_t stream);

@@ -558,6 +558,52 @@ def test_alltoallv_tile_counter_resets_across_launches_and_graph_replays():
         V.vcommDestroy(c)
 
 
+def test_alltoallv_eager_calls_overlapping_graph_replays():
+    # A captured variable all-to-all keeps its tile counters for every replay; eager calls
+    # rotate through a separate set.  More eager calls than that set holds (70 > 64), each
+    # issued on a second stream while a replay of the captured call runs on the first, so
+    # every eager counter pair meets a running replay: every output must still equal the
+    # oracle's.
+    n = 8
+    g = torch.Generator().manual_seed(33)
+    counts = torch.randint(0, 40_000, (n, n), generator=g, dtype=torch.int32)
+    sd = (torch.cumsum(counts, 1) - counts).to(torch.int32)
+    rd = (torch.cumsum(counts, 0) - counts).t().contiguous().to(torch.int32)
+    recv_elems = [int(v) for v in counts.sum(0)]
+    tabs = [t.to(DEV) for t in (counts, sd, rd)]
+    xa = [inputs.uniform_ranks(1, int(counts[i].sum()), torch.float32, 700 + i)[0] for i in range(n)]
+    xb = [inputs.uniform_ranks(1, int(counts[i].sum()), torch.float32, 800 + i)[0] for i in range(n)]
+    sa, sb = [x.to(DEV) for x in xa], [x.to(DEV) for x in xb]
+    ra = [torch.full((e,), -7.0, device=DEV) for e in recv_elems]
+    rb = [torch.full((e,), -7.0, device=DEV) for e in recv_elems]
+    c = V.vcommInit(n, 1, V.vProtoSimple)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    try:
+        V.vAllToAllv(sa, ra, *tabs, torch.float32, c)            # warm-up before capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            V.vAllToAllv(sa, ra, *tabs, torch.float32, c)
+        torch.cuda.synchronize()
+        want_a = oracle.alltoallv(xa, counts, sd, rd, recv_elems)
+        want_b = oracle.alltoallv(xb, counts, sd, rd, recv_elems)
+        for k in range(70):
+            with torch.cuda.stream(s1):
+                graph.replay()
+            V.vAllToAllv(sb, rb, *tabs, torch.float32, c, s2)
+            if k % 10 == 9:
+                torch.cuda.synchronize()
+                assert_bits_equal(ra, want_a, f"replay {k}")
+                assert_bits_equal(rb, want_b, f"eager {k}")
+                for t in ra + rb:
+                    t.fill_(-7.0)
+                torch.cuda.synchronize()
+        assert V.vcommGetAsyncError(c) == V.vSuccess
+    finally:
+        torch.cuda.synchronize()
+        V.vcommDestroy(c)
+
+
 def test_alltoallv_positive_count_into_null_buffer_sets_async_error():
     n = 2
     c = V.vcommInit(n, 1, V.vProtoSimple)

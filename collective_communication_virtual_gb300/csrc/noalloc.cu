@@ -22,7 +22,10 @@ namespace {
 constexpr size_t kCtrlRegion = 64 * 1024;                 // status + per-(channel, rank) control
 constexpr size_t kFifoRegion = 8u << 20;                  // FIFO slots
 constexpr size_t kScratchBytes = kCtrlRegion + kFifoRegion;
-constexpr size_t kChunkBytes = 64 * 1024;                 // 4 slots of 16 KiB
+// Data bytes per chunk (4 slots): 64 KiB for Simple; 32 KiB for LL and LL128, whose slots
+// take more FIFO bytes than they carry.  Every protocol then fits 64 (channel, rank) FIFOs.
+constexpr size_t kChunkBytes = 64 * 1024;
+constexpr size_t kChunkBytesFlagged = 32 * 1024;
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kTimeoutNs = 2000ull * 1000 * 1000;
 
@@ -76,7 +79,7 @@ extern "C" vResult_t vAllReduceNoAlloc(const void* const* sendbuffs, void* const
     q.coll = vCollAllReduce;
     q.datatype = datatype;
     q.count = count;
-    q.chunkBytes = kChunkBytes;
+    q.chunkBytes = protocol == vProtoSimple ? kChunkBytes : kChunkBytesFlagged;
     bool a16 = true;
     for (int r = 0; r < nRanks; r++) {
         const uintptr_t s = (uintptr_t)sendbuffs[r], d = (uintptr_t)recvbuffs[r];

@@ -290,22 +290,32 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
     }
 
     // ---- ring geometry ------------------------------------------------------------------
+    // A chunk is chunkBytes of data per rank, 4 slots of chunkBytes / 4 data bytes each; a
+    // slot's size in the FIFO follows the protocol: the same for Simple, twice for LL (a
+    // flag beside every 4 data bytes), and whole 128-byte lines of 120 data bytes for LL128
+    // (an even number of lines, so every slot starts on 256 bytes).  Sizing slots by their
+    // data keeps the three protocols' steps aligned: a channel's share of a block that
+    // fills a Simple slot fills an LL or LL128 slot too, rather than spilling a sliver into
+    // a second slot that costs a whole handshake.
     const int proto = ringProto;
     p->proto = proto;
     size_t chunk = q->chunkBytes;
     if (chunk == 0) {
-        // 1 MiB chunks, or smaller so that all FIFOs (2 chunks per (channel, rank)) stay
-        // within 1 GiB.  Measured on GB300, large chunks win even when the FIFOs overflow L2:
-        // a ring moves its literal bytes at 0.87 of the copy rate once the per-slot handshake
-        // is amortised, while L2-sized chunks (64-128 KiB at 32 channels) spend the time in
-        // that handshake (8 x 64 MiB, 32 channels: 484 against 644 us for Simple).
-        const size_t fit = ((size_t)1 << 30) / (2 * (size_t)q->nChannels * (size_t)N);
+        // 1 MiB chunks, or smaller so that all FIFOs (2 chunks per (channel, rank), in wire
+        // bytes) stay within 1 GiB.  Measured on GB300, large chunks win even when the FIFOs
+        // do not fit in L2 (the slots in flight mostly stay there, being kept ahead of the
+        // user data), while L2-sized chunks (64-128 KiB at 32 channels) spend the time in
+        // the per-slot handshake (8 x 64 MiB, 32 channels, Simple: 428 us with 1 MiB chunks
+        // against 627 us with 128 KiB).
+        size_t fit = ((size_t)1 << 30) / (2 * (size_t)q->nChannels * (size_t)N);   // wire bytes per chunk
+        if (proto == vProtoLL) fit /= 2;
+        else if (proto == vProtoLL128) fit = fit / 128 * 120;
         chunk = std::min<size_t>((size_t)1 << 20, std::max<size_t>(16384, pow2_floor(fit)));
     }
-    const size_t slotBytes = chunk / vc::kChunkSlots;   // >= 1 KiB, a multiple of 256
-    size_t slotPayload = slotBytes;
-    if (proto == vProtoLL) slotPayload = slotBytes / 2;
-    else if (proto == vProtoLL128) slotPayload = slotBytes / 128 * 120;
+    const size_t slotPayload = chunk / vc::kChunkSlots;   // >= 1 KiB, a power of two
+    size_t slotBytes = slotPayload;
+    if (proto == vProtoLL) slotBytes = 2 * slotPayload;
+    else if (proto == vProtoLL128) slotBytes = align_up(div_up(slotPayload, (size_t)120), 2) * 128;
     p->slotBytes = slotBytes;
     p->slotPayloadElems = slotPayload / esz;
     p->chunkElems = p->slotPayloadElems * vc::kChunkSlots;

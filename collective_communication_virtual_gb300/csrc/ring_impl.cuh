@@ -55,21 +55,60 @@ __device__ __forceinline__ uint4 op_vec_rt(int op, uint4 a, uint4 b) {
                       op_word_rt<DT>(op, a.z, b.z), op_word_rt<DT>(op, a.w, b.w));
 }
 
-__device__ __forceinline__ uint2 ld_stream8(const void* p) {
-    uint2 v;
-    asm("ld.global.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+// L2 residency.  The ring streams every user byte through once but passes each FIFO slot
+// from one SM to another a few microseconds after writing it, so user loads and stores are
+// marked to leave L2 first and FIFO stores to stay, which keeps slots in L2 between their
+// write and their read instead of sending them through DRAM; a FIFO load marks the line
+// as the first to go, since the slot is dead once read.
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+    unsigned long long p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ unsigned long long l2_evict_last() {
+    unsigned long long p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_user16(const void* p) {
+    uint4 v;
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(l2_evict_first()));
     return v;
 }
-__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
-    asm volatile("st.global.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-__device__ __forceinline__ uint2 ld_cg8(const void* p) {
+__device__ __forceinline__ uint2 ld_user8(const void* p) {
     uint2 v;
-    asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    asm("ld.global.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+        : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(l2_evict_first()));
     return v;
 }
-__device__ __forceinline__ void st_cg8(void* p, uint2 v) {
-    asm volatile("st.global.cg.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+__device__ __forceinline__ void st_user16(void* p, uint4 v) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(l2_evict_first()) : "memory");
+}
+__device__ __forceinline__ void st_user8(void* p, uint2 v) {
+    asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "l"(l2_evict_first()) : "memory");
+}
+__device__ __forceinline__ uint4 ld_fifo16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(l2_evict_first()) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint2 ld_fifo8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(l2_evict_first()) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_fifo16(void* p, uint4 v) {
+    asm volatile("st.global.cg.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(l2_evict_last()) : "memory");
+}
+__device__ __forceinline__ void st_fifo8(void* p, uint2 v) {
+    asm volatile("st.global.cg.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "l"(l2_evict_last()) : "memory");
 }
 
 // Load UB bytes of user data (ne valid elements, the rest zero).  ALIGN is the byte
@@ -78,10 +117,10 @@ template <int ESZ, int UB, int ALIGN>
 __device__ __forceinline__ uint4 load_unit(const char* p, int ne, bool aligned) {
     constexpr int UE = UB / ESZ;
     if (aligned && ne == UE) {
-        if (UB == 16 && ALIGN == 16) return ld_stream(p);
-        const uint2 lo = ld_stream8(p);
+        if (UB == 16 && ALIGN == 16) return ld_user16(p);
+        const uint2 lo = ld_user8(p);
         if (UB == 8) return make_uint4(lo.x, lo.y, 0u, 0u);
-        const uint2 hi = ld_stream8(p + 8);
+        const uint2 hi = ld_user8(p + 8);
         return make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
     uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -106,9 +145,9 @@ __device__ __forceinline__ void store_unit(char* p, uint4 v, int ne, bool aligne
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     if (!epi) {
         if (aligned && ne == UE) {
-            if (UB == 16 && ALIGN == 16) { st_stream(p, v); return; }
-            st_stream8(p, make_uint2(v.x, v.y));
-            if (UB == 16) st_stream8(p + 8, make_uint2(v.z, v.w));
+            if (UB == 16 && ALIGN == 16) { st_user16(p, v); return; }
+            st_user8(p, make_uint2(v.x, v.y));
+            if (UB == 16) st_user8(p + 8, make_uint2(v.z, v.w));
             return;
         }
 #pragma unroll
@@ -132,7 +171,7 @@ __device__ __forceinline__ void store_unit(char* p, uint4 v, int ne, bool aligne
 }
 
 struct RingCtx {
-    int ch, r, N;
+    int ch, r;
     char* myFifo;
     char* nextFifo;
     unsigned long long* myHead;      // I post: slots of my FIFO consumed
@@ -155,50 +194,57 @@ __device__ __forceinline__ void test_jitter(const RingArgs& a, unsigned salt) {
     __nanosleep(h % a.testJitterNs);
 }
 
-// Spin until *p >= target (monotonic 64-bit counters).  Bounded.
-static __device__ __noinline__ bool wait_counter(const RingArgs& a, const RingCtx& c,
-                                          const unsigned long long* p, unsigned long long target,
-                                          unsigned int seq) {
+// Acquire/release fence at GPU scope: after a relaxed (volatile) read of a counter or
+// flag it completes an acquire, before a relaxed write of one it completes a release (and,
+// after a barrier, covers what the other threads stored before the barrier).  Lighter than
+// the sequentially consistent fence, which the protocols do not need.
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Give up a wait: record why (abort or timeout); a timeout also raises the device abort
+// word so every other waiter gives up too.  Returns false for the caller to pass on.
+static __device__ __noinline__ bool wait_failed(const RingArgs& a, int ch, int r, unsigned int seq, bool timedOut) {
+    report_error(a.status, a.statusHost, (!timedOut && *a.abortHost) ? vAborted : vTimeout, ch, r, seq);
+    if (timedOut) atomicExch(a.abortDev, 1u);
+    return false;
+}
+
+// Checked every 64 polls: an abort raised by the host or another CTA, or this wait's
+// deadline.  Returns 0 to keep waiting, 1 aborted, 2 timed out.
+__device__ __forceinline__ int wait_check(const RingArgs& a, unsigned long long t0) {
+    if (*(volatile unsigned int*)a.abortDev || *a.abortHost) return 1;
+    if (global_timer_ns() - t0 > a.timeoutNs) return 2;
+    return 0;
+}
+
+// Spin until *p >= target (monotonic 64-bit counters), then fence.  Bounded.
+static __device__ __noinline__ bool wait_counter(const RingArgs& a, int ch, int r, const unsigned long long* p,
+                                                 unsigned long long target, unsigned int seq) {
     const unsigned long long t0 = global_timer_ns();
     for (unsigned int it = 0;; it++) {
-        if (ld_volatile_u64(p) >= target) { __threadfence(); return true; }
+        if (ld_volatile_u64(p) >= target) { fence_acq_rel(); return true; }
         if ((it & 63u) == 63u) {
-            if (*(volatile unsigned int*)a.abortDev || *a.abortHost) {
-                report_error(a.status, a.statusHost, *a.abortHost ? vAborted : vTimeout, c.ch, c.r, seq);
-                return false;
-            }
-            if (global_timer_ns() - t0 > a.timeoutNs) {
-                report_error(a.status, a.statusHost, vTimeout, c.ch, c.r, seq);
-                atomicExch(a.abortDev, 1u);
-                return false;
-            }
+            const int why = wait_check(a, t0);
+            if (why) return wait_failed(a, ch, r, seq, why == 2);
         }
     }
 }
 
 // Spin until the 64-bit flag at p equals target.  Bounded.
-static __device__ __noinline__ bool wait_flag64(const RingArgs& a, const RingCtx& c, const void* p,
-                                         unsigned long long target, unsigned int seq) {
+static __device__ __noinline__ bool wait_flag64(const RingArgs& a, int ch, int r, const void* p,
+                                                unsigned long long target, unsigned int seq) {
     const unsigned long long t0 = global_timer_ns();
     for (unsigned int it = 0;; it++) {
         if (ld_volatile_u64(p) == target) return true;
         if ((it & 63u) == 63u) {
-            if (*(volatile unsigned int*)a.abortDev || *a.abortHost) {
-                report_error(a.status, a.statusHost, *a.abortHost ? vAborted : vTimeout, c.ch, c.r, seq);
-                return false;
-            }
-            if (global_timer_ns() - t0 > a.timeoutNs) {
-                report_error(a.status, a.statusHost, vTimeout, c.ch, c.r, seq);
-                atomicExch(a.abortDev, 1u);
-                return false;
-            }
+            const int why = wait_check(a, t0);
+            if (why) return wait_failed(a, ch, r, seq, why == 2);
         }
     }
 }
 
 // Spin until both LL words at p carry `flag`; returns their data halves.  Bounded.
-static __device__ __noinline__ bool wait_ll_slow(const RingArgs& a, const RingCtx& c, const void* p,
-                                     unsigned int flag, uint2* data, unsigned int seq) {
+static __device__ __noinline__ bool wait_ll_slow(const RingArgs& a, int ch, int r, const void* p,
+                                                 unsigned int flag, uint2* data, unsigned int seq) {
     const unsigned long long t0 = global_timer_ns();
     for (unsigned int it = 0;; it++) {
         unsigned long long w0, w1;
@@ -208,51 +254,32 @@ static __device__ __noinline__ bool wait_ll_slow(const RingArgs& a, const RingCt
             return true;
         }
         if ((it & 63u) == 63u) {
-            if (*(volatile unsigned int*)a.abortDev || *a.abortHost) {
-                report_error(a.status, a.statusHost, *a.abortHost ? vAborted : vTimeout, c.ch, c.r, seq);
-                return false;
-            }
-            if (global_timer_ns() - t0 > a.timeoutNs) {
-                report_error(a.status, a.statusHost, vTimeout, c.ch, c.r, seq);
-                atomicExch(a.abortDev, 1u);
-                return false;
-            }
+            const int why = wait_check(a, t0);
+            if (why) return wait_failed(a, ch, r, seq, why == 2);
         }
     }
 }
 
-// LL read: one inline attempt, then the bounded spin out of line.
-__device__ __forceinline__ bool wait_ll(const RingArgs& a, const RingCtx& c, const void* p,
-                                       unsigned int flag, uint2* data, unsigned int seq) {
-    unsigned long long w0, w1;
-    ld_volatile_u64x2(p, w0, w1);
-    if ((unsigned int)(w0 >> 32) == flag && (unsigned int)(w1 >> 32) == flag) {
-        *data = make_uint2((unsigned int)w0, (unsigned int)w1);
-        return true;
-    }
-    return wait_ll_slow(a, c, p, flag, data, seq);
-}
-
 // Thread 0 takes the slot credit (and, for Simple, waits for the slot's data); the CTA
 // then agrees on success.
-template <int PROTO>
-__device__ __forceinline__ bool slot_begin(const RingArgs& a, const RingCtx& c, int kind) {
+template <int PROTO, int kind>
+__device__ __forceinline__ bool slot_begin(const RingArgs& a, const RingCtx& c) {
     test_jitter(a, c.recvSeq * 3u + c.sendSeq);
     bool fail = false;
     if (threadIdx.x == 0) {
         if (PROTO == vProtoSimple && (kind & kRecv))
-            fail = !wait_counter(a, c, c.myTail, a.epochHi | (c.recvSeq + 1ull), c.recvSeq);
+            fail = !wait_counter(a, c.ch, c.r, c.myTail, a.epochHi | (c.recvSeq + 1ull), c.recvSeq);
         if (!fail && (kind & kSend) && c.sendSeq >= (unsigned)kFifoSlots)
-            fail = !wait_counter(a, c, c.nextHead, a.epochHi | (c.sendSeq - kFifoSlots + 1ull), c.sendSeq);
+            fail = !wait_counter(a, c.ch, c.r, c.nextHead, a.epochHi | (c.sendSeq - kFifoSlots + 1ull), c.sendSeq);
     }
     return !__syncthreads_or(fail);
 }
 
 // Publish the slot (Simple tail) and return consumed slots (head).  Call after a barrier.
-template <int PROTO>
-__device__ __forceinline__ void slot_end(const RingArgs& a, RingCtx& c, int kind) {
+template <int PROTO, int kind>
+__device__ __forceinline__ void slot_end(const RingArgs& a, RingCtx& c) {
     if (threadIdx.x == 0) {
-        __threadfence();
+        fence_acq_rel();
         if (PROTO == vProtoSimple && (kind & kSend))
             st_volatile_u64(c.nextTail, a.epochHi | (c.sendSeq + 1ull));
         if (kind & kRecv) st_volatile_u64(c.myHead, a.epochHi | (c.recvSeq + 1ull));
@@ -261,79 +288,83 @@ __device__ __forceinline__ void slot_end(const RingArgs& a, RingCtx& c, int kind
     if (kind & kRecv) c.recvSeq++;
 }
 
-// Units per thread whose loads are in flight together; the flag protocols hold more per
-// unit, so they take fewer to stay within 64 registers (two 512-thread CTAs per SM).
-template <int PROTO> struct RingUnroll { static constexpr int value = PROTO == vProtoSimple ? 4 : 2; };
+// Units per thread whose loads are in flight together: as many as fit in the 64
+// registers of a thread of a 512-thread CTA, two of which share an SM (the 16-bit LL128
+// instances hold fewer: their packed ops need more registers).
+template <int PROTO, int ESZ> struct RingUnroll {
+    static constexpr int value = PROTO == vProtoLL ? 2 : (PROTO == vProtoLL128 && ESZ == 2) ? 2 : 4;
+};
 
-// One slot of m elements.  `in`: user input at the slot's first element (kLocal);
-// `out`: user output at the slot's first element (kOut).  Each thread takes R units at a
-// time and issues all their loads (FIFO data or flags, user data) before
-// combining and storing any of them.
-template <int DT, int OUT, int PROTO>
-__device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kind, const char* in,
-                                          char* out, size_t m, bool epi) {
+// One slot of m elements (a slot is at most 16 MiB, so 32-bit offsets).  `in`: user input
+// at the slot's first element (kLocal); `out`: user output at the slot's first element
+// (kOut).  Each thread takes R units at a time and issues all their loads (FIFO data or
+// flags, user data) before combining and storing any of them.
+template <int DT, int OUT, int PROTO, int kind>
+__device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const char* in, char* out,
+                                          unsigned int m, bool epi) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int OSZ = DTypeOf<OUT>::size;
-    constexpr int R = RingUnroll<PROTO>::value;
+    constexpr int R = RingUnroll<PROTO, ESZ>::value;
     const bool aligned = a.aligned != 0;
     const bool hasScale = a.hasScale != 0;
-    if (!slot_begin<PROTO>(a, c, kind)) return false;
+    if (!slot_begin<PROTO, kind>(a, c)) return false;
     const char* rs = c.myFifo + (size_t)(c.recvSeq % kFifoSlots) * a.slotBytes;
     char* ss = c.nextFifo + (size_t)(c.sendSeq % kFifoSlots) * a.slotBytes;
+    const unsigned int T = blockDim.x;
     bool fail = false;
     if (PROTO == vProtoSimple) {
         // 16 payload bytes per unit, contiguous in the slot.
         constexpr int UE = 16 / ESZ;
-        const size_t units = (m + UE - 1) / UE;
-        for (size_t u0 = threadIdx.x; u0 < units; u0 += (size_t)R * blockDim.x) {
+        const unsigned int units = (m + UE - 1) / UE;
+        for (unsigned int u0 = threadIdx.x; u0 < units; u0 += R * T) {
             uint4 v[R], l[R];
 #pragma unroll
             for (int k = 0; k < R; k++) {
-                const size_t u = u0 + (size_t)k * blockDim.x;
+                const unsigned int u = u0 + k * T;
                 v[k] = make_uint4(0u, 0u, 0u, 0u);
                 l[k] = v[k];
                 if (u < units) {
-                    if (kind & kRecv) v[k] = ld_cg(rs + u * 16);
-                    if (kind & kLocal) l[k] = load_unit<ESZ, 16, 16>(in + u * 16, (int)min((size_t)UE, m - u * UE), aligned);
+                    if (kind & kRecv) v[k] = ld_fifo16(rs + (size_t)u * 16);
+                    if (kind & kLocal) l[k] = load_unit<ESZ, 16, 16>(in + (size_t)u * 16, (int)min((unsigned)UE, m - u * UE), aligned);
                 }
             }
 #pragma unroll
             for (int k = 0; k < R; k++) {
-                const size_t u = u0 + (size_t)k * blockDim.x;
+                const unsigned int u = u0 + k * T;
                 if (u >= units) break;
-                const int ne = (int)min((size_t)UE, m - u * UE);
+                const int ne = (int)min((unsigned)UE, m - u * UE);
                 uint4 x = v[k];
                 if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
                 if (kind & kOut)
-                    store_unit<DT, OUT, 16, 16>(out + u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
-                if (kind & kSend) st_cg(ss + u * 16, x);
+                    store_unit<DT, OUT, 16, 16>(out + (size_t)u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
+                if (kind & kSend) st_fifo16(ss + (size_t)u * 16, x);
             }
-            test_jitter(a, (unsigned)u0);
+            test_jitter(a, u0);
         }
     } else if (PROTO == vProtoLL) {
         // 8 payload bytes per unit, stored as two {data, flag} 64-bit words.
         constexpr int UE = 8 / ESZ;
-        const size_t units = (m + UE - 1) / UE;
+        const unsigned int units = (m + UE - 1) / UE;
         const unsigned int rflag = a.llEpoch | ((c.recvSeq + 1u) & 0xFFFFFFu);
         const unsigned long long sflag = (unsigned long long)(a.llEpoch | ((c.sendSeq + 1u) & 0xFFFFFFu)) << 32;
-        for (size_t u0 = threadIdx.x; u0 < units && !fail; u0 += (size_t)R * blockDim.x) {
+        for (unsigned int u0 = threadIdx.x; u0 < units && !fail; u0 += R * T) {
             unsigned long long w0[R], w1[R];
             uint4 l[R];
 #pragma unroll
             for (int k = 0; k < R; k++) {
-                const size_t u = u0 + (size_t)k * blockDim.x;
+                const unsigned int u = u0 + k * T;
                 w0[k] = w1[k] = 0ull;
                 l[k] = make_uint4(0u, 0u, 0u, 0u);
                 if (u < units) {
-                    if (kind & kRecv) ld_volatile_u64x2(rs + u * 16, w0[k], w1[k]);
-                    if (kind & kLocal) l[k] = load_unit<ESZ, 8, 8>(in + u * 8, (int)min((size_t)UE, m - u * UE), aligned);
+                    if (kind & kRecv) ld_volatile_u64x2(rs + (size_t)u * 16, w0[k], w1[k]);
+                    if (kind & kLocal) l[k] = load_unit<ESZ, 8, 8>(in + (size_t)u * 8, (int)min((unsigned)UE, m - u * UE), aligned);
                 }
             }
 #pragma unroll
             for (int k = 0; k < R; k++) {
-                const size_t u = u0 + (size_t)k * blockDim.x;
+                const unsigned int u = u0 + k * T;
                 if (u >= units || fail) break;
-                const int ne = (int)min((size_t)UE, m - u * UE);
+                const int ne = (int)min((unsigned)UE, m - u * UE);
                 uint4 x = make_uint4(0u, 0u, 0u, 0u);
                 if (kind & kRecv) {
                     if ((unsigned int)(w0[k] >> 32) == rflag && (unsigned int)(w1[k] >> 32) == rflag) {
@@ -341,116 +372,127 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, int kin
                         x.y = (unsigned int)w1[k];
                     } else {
                         uint2 d;
-                        if (!wait_ll_slow(a, c, rs + u * 16, rflag, &d, c.recvSeq)) { fail = true; break; }
+                        if (!wait_ll_slow(a, c.ch, c.r, rs + (size_t)u * 16, rflag, &d, c.recvSeq)) { fail = true; break; }
                         x.x = d.x;
                         x.y = d.y;
                     }
                 }
                 if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
                 if (kind & kOut)
-                    store_unit<DT, OUT, 8, 8>(out + u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
-                if (kind & kSend) st_volatile_u64x2(ss + u * 16, sflag | x.x, sflag | x.y);
+                    store_unit<DT, OUT, 8, 8>(out + (size_t)u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
+                if (kind & kSend) st_volatile_u64x2(ss + (size_t)u * 16, sflag | x.x, sflag | x.y);
             }
-            test_jitter(a, (unsigned)u0);
+            test_jitter(a, u0);
         }
     } else {
         // LL128: 128-byte lines of 120 payload bytes + an 8-byte flag.  Eight lanes share a
         // line: lanes 0..6 carry 16 payload bytes, lane 7 carries 8 bytes and the flag.
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nWarps = blockDim.x >> 5;
-        const int g = lane >> 3, t = lane & 7;
-        const size_t lines = (m * ESZ + 119) / 120;
-        const size_t perIter = (size_t)nWarps * 4;
+        // Payload layout of a slot of P bytes in `lines` lines: bytes [0, 112 lines) fill the
+        // 16-byte places in order (line L, place t holds bytes 112 L + 16 t), and the rest,
+        // [112 lines, P), the 8-byte places (line L holds bytes 112 lines + 8 L), so every
+        // 16-byte place maps to a 16-byte aligned piece of the user buffer and a warp's 28
+        // full places (4 consecutive lines) to 448 contiguous bytes.
+        const unsigned int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const unsigned int g = lane >> 3, t = lane & 7;
+        const unsigned int P = m * ESZ;
+        const unsigned int lines = (P + 119) / 120;
+        const unsigned int perIter = (T >> 5) * 4;       // lines the CTA covers per step
         const unsigned long long rflag = a.epochHi | (c.recvSeq + 1ull);
         const unsigned long long sflag = a.epochHi | (c.sendSeq + 1ull);
         if (kind & kRecv) {
-            if (t == 7) {
-                // Flags of this lane's lines, 8 loads in flight at a time; only a flag that
-                // is not yet set is waited for on its own.
-                for (size_t L0 = (size_t)warp * 4 + g; L0 < lines && !fail; L0 += 8 * perIter) {
-                    unsigned long long f[8];
+            // The flags of this warp's lines (warp * 4 + j * perIter + (0..3)), polled by all
+            // 32 lanes, four per lane per round (128 flags in flight per warp); a flag not
+            // yet set is waited for on its own.
+            const unsigned int mine = lines > warp * 4 ? (lines - warp * 4 + perIter - 1) / perIter * 4 : 0;
+            for (unsigned int q0 = lane; q0 < mine && !fail; q0 += 128) {
+                unsigned long long f[4];
 #pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        const size_t L = L0 + (size_t)k * perIter;
-                        f[k] = L < lines ? ld_volatile_u64(rs + L * 128 + 120) : rflag;
-                    }
+                for (int k = 0; k < 4; k++) {
+                    const unsigned int q = q0 + k * 32;
+                    const unsigned int L = warp * 4 + (q >> 2) * perIter + (q & 3);
+                    f[k] = (q < mine && L < lines) ? ld_volatile_u64(rs + (size_t)L * 128 + 120) : rflag;
+                }
 #pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        const size_t L = L0 + (size_t)k * perIter;
-                        if (f[k] != rflag && !fail && !wait_flag64(a, c, rs + L * 128 + 120, rflag, c.recvSeq))
-                            fail = true;
-                    }
+                for (int k = 0; k < 4; k++) {
+                    const unsigned int q = q0 + k * 32;
+                    const unsigned int L = warp * 4 + (q >> 2) * perIter + (q & 3);
+                    if (f[k] != rflag && !fail &&
+                        !wait_flag64(a, c.ch, c.r, rs + (size_t)L * 128 + 120, rflag, c.recvSeq))
+                        fail = true;
                 }
             }
-            __threadfence();
+            fence_acq_rel();
             __syncwarp();
         }
         if (!__any_sync(0xFFFFFFFFu, fail)) {
-            const int pb = t < 7 ? 16 * t : 112;              // payload byte offset in the line
-            const int UEl = t < 7 ? 16 / ESZ : 8 / ESZ;        // elements of this lane
-            for (size_t L0 = (size_t)warp * 4 + g; L0 < lines; L0 += (size_t)R * perIter) {
+            const unsigned int halfBase = 112 * lines;
+            for (unsigned int L0 = warp * 4 + g; L0 < lines; L0 += R * perIter) {
                 uint4 v[R], l[R];
 #pragma unroll
                 for (int k = 0; k < R; k++) {
-                    const size_t L = L0 + (size_t)k * perIter;
-                    const size_t e0 = (L * 120 + pb) / ESZ;    // first element of this lane
+                    const unsigned int L = L0 + k * perIter;
+                    const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;   // payload byte
                     v[k] = make_uint4(0u, 0u, 0u, 0u);
                     l[k] = v[k];
-                    if (L < lines && e0 < m) {
-                        const int ne = (int)min((size_t)UEl, m - e0);
+                    if (L < lines && b < P) {
                         if (kind & kRecv) {
-                            if (t < 7) v[k] = ld_cg(rs + L * 128 + 16 * t);
-                            else { const uint2 d = ld_cg8(rs + L * 128 + 112); v[k].x = d.x; v[k].y = d.y; }
+                            if (t < 7) v[k] = ld_fifo16(rs + (size_t)L * 128 + 16 * t);
+                            else { const uint2 d = ld_fifo8(rs + (size_t)L * 128 + 112); v[k].x = d.x; v[k].y = d.y; }
                         }
-                        if (kind & kLocal)
-                            l[k] = t < 7 ? load_unit<ESZ, 16, 8>(in + e0 * ESZ, ne, aligned)
-                                         : load_unit<ESZ, 8, 8>(in + e0 * ESZ, ne, aligned);
+                        if (kind & kLocal) {
+                            const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
+                            l[k] = t < 7 ? load_unit<ESZ, 16, 16>(in + b, ne, aligned)
+                                         : load_unit<ESZ, 8, 8>(in + b, ne, aligned);
+                        }
                     }
                 }
 #pragma unroll
                 for (int k = 0; k < R; k++) {
-                    const size_t L = L0 + (size_t)k * perIter;
-                    const size_t e0 = (L * 120 + pb) / ESZ;
-                    if (L >= lines || e0 >= m) continue;
-                    const int ne = (int)min((size_t)UEl, m - e0);
+                    const unsigned int L = L0 + k * perIter;
+                    const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;
+                    if (L >= lines) break;
                     uint4 x = v[k];
-                    if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
-                    if (t < 7) {
-                        if (kind & kOut)
-                            store_unit<DT, OUT, 16, 8>(out + e0 * OSZ, x, ne, aligned, epi, hasScale, a.scale);
-                        if (kind & kSend) st_cg(ss + L * 128 + 16 * t, x);
-                    } else {
-                        if (kind & kOut)
-                            store_unit<DT, OUT, 8, 8>(out + e0 * OSZ, x, ne, aligned, epi, hasScale, a.scale);
-                        if (kind & kSend) st_cg8(ss + L * 128 + 112, make_uint2(x.x, x.y));
+                    if (b < P) {
+                        if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
+                        if (kind & kOut) {
+                            const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
+                            char* o = out + (size_t)(b / ESZ) * OSZ;
+                            if (t < 7) store_unit<DT, OUT, 16, 16>(o, x, ne, aligned, epi, hasScale, a.scale);
+                            else store_unit<DT, OUT, 8, 8>(o, x, ne, aligned, epi, hasScale, a.scale);
+                        }
+                    }
+                    if (kind & kSend) {
+                        if (t < 7) st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
+                        else st_fifo8(ss + (size_t)L * 128 + 112, make_uint2(x.x, x.y));
                     }
                 }
-                test_jitter(a, (unsigned)L0);
+                test_jitter(a, L0);
             }
             if (kind & kSend) {
                 test_jitter(a, 0x5157u);
                 __syncwarp();
-                __threadfence();
+                fence_acq_rel();
                 if (t == 7)
-                    for (size_t L = (size_t)warp * 4 + g; L < lines; L += perIter)
-                        st_volatile_u64(ss + L * 128 + 120, sflag);
+                    for (unsigned int L = warp * 4 + g; L < lines; L += perIter)
+                        st_volatile_u64(ss + (size_t)L * 128 + 120, sflag);
             }
         }
     }
     if (__syncthreads_or(fail)) return false;
-    slot_end<PROTO>(a, c, kind);
+    slot_end<PROTO, kind>(a, c);
     return true;
 }
 
 // One transfer of n elements of one block: ceil(n / slotElems) slots.
-template <int DT, int OUT, int PROTO>
-__device__ __forceinline__ bool ring_transfer(const RingArgs& a, RingCtx& c, int kind,
-                                              const char* in, char* out, size_t n, bool epi) {
+template <int DT, int OUT, int PROTO, int kind>
+__device__ __forceinline__ bool ring_transfer(const RingArgs& a, RingCtx& c, const char* in, char* out,
+                                              size_t n, bool epi) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int OSZ = DTypeOf<OUT>::size;
     for (size_t k = 0; k < n; k += a.slotElems) {
-        const size_t m = min(a.slotElems, n - k);
-        if (!ring_slot<DT, OUT, PROTO>(a, c, kind, in ? in + k * ESZ : nullptr,
-                                       out ? out + k * OSZ : nullptr, m, epi))
+        const unsigned int m = (unsigned int)min(a.slotElems, n - k);
+        if (!ring_slot<DT, OUT, PROTO, kind>(a, c, (kind & kLocal) ? in + k * ESZ : nullptr,
+                                             (kind & kOut) ? out + k * OSZ : nullptr, m, epi))
             return false;
     }
     return true;
@@ -475,7 +517,6 @@ __global__ void __launch_bounds__(kRingThreads, 2) k_ring(const __grid_constant_
     constexpr int OSZ = DTypeOf<OUT>::size;
     const int N = a.nRanks;
     RingCtx c;
-    c.N = N;
     c.ch = blockIdx.x / N;
     c.r = blockIdx.x - c.ch * N;
     if (c.r == a.testStallRank) return;             // test hook: a rank that never shows up
@@ -510,54 +551,60 @@ __global__ void __launch_bounds__(kRingThreads, 2) k_ring(const __grid_constant_
             // reduce-scatter stages
             int blk = r == 0 ? N - 1 : r - 1;
             size_t n = seg_len(a, ch, blk, o, &st);
-            if (!ring_transfer<DT, DT, PROTO>(a, c, kLocal | kSend, mySend + (st + o) * ESZ, nullptr, n, false)) return;
+            if (!ring_transfer<DT, DT, PROTO, kLocal | kSend>(a, c, mySend + (st + o) * ESZ, nullptr, n, false)) return;
             for (int s = 1; s < N - 1; s++) {
                 blk = (r + N - 1 - s) % N;
                 n = seg_len(a, ch, blk, o, &st);
-                if (!ring_transfer<DT, DT, PROTO>(a, c, kRecv | kLocal | kSend, mySend + (st + o) * ESZ,
+                if (!ring_transfer<DT, DT, PROTO, kRecv | kLocal | kSend>(a, c, mySend + (st + o) * ESZ,
                                                   nullptr, n, false)) return;
             }
             n = seg_len(a, ch, r, o, &st);
             if (a.coll == vCollAllReduce) {
-                if (!ring_transfer<DT, DT, PROTO>(a, c, kRecv | kLocal | kOut | kSend, mySend + (st + o) * ESZ,
+                if (!ring_transfer<DT, DT, PROTO, kRecv | kLocal | kOut | kSend>(a, c, mySend + (st + o) * ESZ,
                                                   myRecv + (st + o) * ESZ, n, false)) return;
                 // all-gather rounds: receive block (r - i - 1), forward unless last
                 for (int i = 0; i < N - 1; i++) {
                     blk = ((r - i - 1) % N + N) % N;
                     n = seg_len(a, ch, blk, o, &st);
-                    const int kind = i < N - 2 ? (kRecv | kOut | kSend) : (kRecv | kOut);
-                    if (!ring_transfer<DT, DT, PROTO>(a, c, kind, nullptr, myRecv + (st + o) * ESZ, n, false))
-                        return;
+                    const bool ok = i < N - 2
+                        ? ring_transfer<DT, DT, PROTO, kRecv | kOut | kSend>(a, c, nullptr, myRecv + (st + o) * ESZ, n, false)
+                        : ring_transfer<DT, DT, PROTO, kRecv | kOut>(a, c, nullptr, myRecv + (st + o) * ESZ, n, false);
+                    if (!ok) return;
                 }
             } else {
                 // block r lands at recv[r][st - r * rc + o] = recv[r][ch * Lc + o]
                 const size_t t0 = st - (size_t)r * a.blockElems + o;
-                if (!ring_transfer<DT, OUT, PROTO>(a, c, kRecv | kLocal | kOut, mySend + (st + o) * ESZ,
+                if (!ring_transfer<DT, OUT, PROTO, kRecv | kLocal | kOut>(a, c, mySend + (st + o) * ESZ,
                                                    myRecv + t0 * OSZ, n, epi)) return;
             }
         } else if (a.coll == vCollAllGather) {
             // own block r: copy to recv[r] at block r and send it on
             size_t n = seg_len(a, ch, r, o, &st);
             const size_t inOff = st - (size_t)r * a.blockElems + o;     // within send[r]
-            if (!ring_transfer<DT, DT, PROTO>(a, c, kLocal | kOut | kSend, mySend + inOff * ESZ,
+            if (!ring_transfer<DT, DT, PROTO, kLocal | kOut | kSend>(a, c, mySend + inOff * ESZ,
                                               myRecv + (st + o) * ESZ, n, false)) return;
             for (int i = 0; i < N - 1; i++) {
                 const int blk = ((r - i - 1) % N + N) % N;
                 n = seg_len(a, ch, blk, o, &st);
-                const int kind = i < N - 2 ? (kRecv | kOut | kSend) : (kRecv | kOut);
-                if (!ring_transfer<DT, DT, PROTO>(a, c, kind, nullptr, myRecv + (st + o) * ESZ, n, false))
-                    return;
+                const bool ok = i < N - 2
+                    ? ring_transfer<DT, DT, PROTO, kRecv | kOut | kSend>(a, c, nullptr, myRecv + (st + o) * ESZ, n, false)
+                    : ring_transfer<DT, DT, PROTO, kRecv | kOut>(a, c, nullptr, myRecv + (st + o) * ESZ, n, false);
+                if (!ok) return;
             }
         } else {
             // broadcast: a chain root, root+1, ..., root-1
             const int pos = ((r - a.root) % N + N) % N;
             const size_t n = seg_len(a, ch, 0, o, &st);
-            int kind;
-            if (pos == 0) kind = kLocal | kOut | kSend;
-            else if (pos < N - 1) kind = kRecv | kOut | kSend;
-            else kind = kRecv | kOut;
-            const char* src = pos == 0 ? (const char*)a.send[a.root] + (st + o) * ESZ : nullptr;
-            if (!ring_transfer<DT, DT, PROTO>(a, c, kind, src, myRecv + (st + o) * ESZ, n, false)) return;
+            char* dst = myRecv + (st + o) * ESZ;
+            bool ok;
+            if (pos == 0)
+                ok = ring_transfer<DT, DT, PROTO, kLocal | kOut | kSend>(
+                    a, c, (const char*)a.send[a.root] + (st + o) * ESZ, dst, n, false);
+            else if (pos < N - 1)
+                ok = ring_transfer<DT, DT, PROTO, kRecv | kOut | kSend>(a, c, nullptr, dst, n, false);
+            else
+                ok = ring_transfer<DT, DT, PROTO, kRecv | kOut>(a, c, nullptr, dst, n, false);
+            if (!ok) return;
         }
     }
 }

@@ -178,10 +178,13 @@ vResult_t vcommGroupStart(vcomm_t comm);
 vResult_t vcommGroupEnd(vcomm_t comm);
 
 /* Tuning knobs (host only, take effect for later calls).  chunkBytes is the ring
- * path's bytes per rank per chunk (one chunk = 4 FIFO slots, one slice = 2 slots;
- * NCCL book chapter 6, ALLREDUCE_CHUNKSTEPS / ALLREDUCE_SLICESTEPS); it must be a
- * power of two in [4 KiB, 64 MiB], or 0 for the planner's default (the largest power
- * of two <= 1 MiB that keeps all FIFOs within half of L2).  timeoutMs bounds every device-side wait (>= 1). */
+ * path's data bytes per rank per chunk (one chunk = 4 FIFO slots, one slice = 2 slots;
+ * NCCL book chapter 6, ALLREDUCE_CHUNKSTEPS / ALLREDUCE_SLICESTEPS); a slot holds
+ * chunkBytes / 4 data bytes in chunkBytes / 4 FIFO bytes (Simple), twice that (LL) or
+ * 128-byte lines of 120 data bytes (LL128).  It must be a power of two in [4 KiB,
+ * 64 MiB], or 0 for the planner's default: the largest power of two <= 1 MiB that keeps
+ * all of the communicator's FIFOs (8 slots per channel and rank) within 1 GiB.
+ * timeoutMs bounds every device-side wait (>= 1). */
 vResult_t vcommSetAlgo(vcomm_t comm, vAlgo_t algo);
 vResult_t vcommSetProtocol(vcomm_t comm, vProto_t protocol);
 vResult_t vcommSetChunkBytes(vcomm_t comm, size_t chunkBytes);
@@ -287,7 +290,8 @@ vResult_t vScatter(const void* const* sendbuffs, void* const* recvbuffs, size_t 
  * (64 KiB + 8 MiB, held on every GPU that loads the library until the process exits).
  * The result is bit-identical to vAllReduce.  The caller passes the buffers as for
  * vAllReduce plus nRanks (2..64), nChannels and protocol (Simple, LL or LL128); the
- * ring uses 64 KiB chunks, so nRanks * nChannels may be at most 64 -- larger rings
+ * ring uses chunks of 64 KiB of data (32 KiB for LL and LL128, whose slots take more FIFO
+ * bytes than they carry), so nRanks * nChannels may be at most 64 -- larger rings
  * return vInvalidArgument (as do the usual argument errors), and a ring whose CTAs
  * cannot all be resident returns vInvalidUsage.  The first call on a device looks up
  * the array's address (cudaGetSymbolAddress), so make it before any stream capture.

@@ -76,22 +76,34 @@ def test_vector_path_requires_aligned_blocks():
 
 
 def test_ring_geometry_follows_the_step_constants():
-    for proto, payload in [(V.vProtoSimple, 1.0), (V.vProtoLL, 0.5), (V.vProtoLL128, 120 / 128)]:
+    # A chunk is 4 slots of chunk / 4 data bytes; a slot's wire size follows the protocol:
+    # the data itself (Simple), a 4-byte flag per 4 data bytes (LL), 120 data bytes per
+    # 128-byte line, an even number of lines (LL128).
+    for proto, wire in [(V.vProtoSimple, 256 << 10), (V.vProtoLL, 512 << 10),
+                        (V.vProtoLL128, (-(-(256 << 10) // 120) + 1) // 2 * 2 * 128)]:
         p = plan(algo=V.vAlgoRing, proto=proto, count=1 << 24, chunkBytes=1 << 20)
         assert p.algo == V.vAlgoRing and p.proto == proto
-        assert p.slotBytes * 4 == 1 << 20                 # a chunk is 4 slots
-        assert p.fifoBytes == 8 * p.slotBytes             # NCCL_STEPS = 8
-        assert p.slotPayloadElems * 4 == int(p.slotBytes * payload)
+        assert p.slotPayloadElems * 4 * 4 == 1 << 20      # a chunk is 4 slots of data
         assert p.chunkElems == 4 * p.slotPayloadElems
+        assert p.slotBytes == wire
+        assert p.fifoBytes == 8 * p.slotBytes             # NCCL_STEPS = 8
         assert p.gridCtas == 8 and p.ctasPerChannel == 8
+    ll128 = plan(algo=V.vAlgoRing, proto=V.vProtoLL128, count=1 << 24, chunkBytes=1 << 20)
+    assert ll128.slotBytes // 128 * 120 >= ll128.slotPayloadElems * 4 > (ll128.slotBytes // 128 - 2) * 120
 
 
 def test_default_chunk_is_1_mib_within_a_1_gib_fifo_budget():
     for n, nch in [(8, 1), (8, 8), (8, 32), (4, 64)]:
-        p = plan(algo=V.vAlgoRing, nRanks=n, nChannels=nch, count=1 << 26)
-        assert p.slotBytes * 4 == 1 << 20 and p.fifoBytes * n * nch <= 1 << 30
+        for proto in (V.vProtoSimple, V.vProtoLL, V.vProtoLL128):
+            p = plan(algo=V.vAlgoRing, proto=proto, nRanks=n, nChannels=nch, count=1 << 26)
+            chunk = p.chunkElems * 4
+            assert p.fifoBytes * n * nch <= 1 << 30
+            if proto != V.vProtoLL or n * nch <= 256:
+                assert chunk == 1 << 20
+            else:
+                assert chunk == 512 << 10
     p = plan(algo=V.vAlgoRing, nRanks=64, nChannels=64, count=1 << 26)
-    assert p.slotBytes * 4 == 128 << 10 and p.fifoBytes * 64 * 64 <= 1 << 30
+    assert p.chunkElems * 4 == 128 << 10 and p.fifoBytes * 64 * 64 <= 1 << 30
 
 
 def test_auto_protocol_follows_the_fitted_ring_model():

@@ -292,8 +292,60 @@ __device__ __forceinline__ void slot_end(const RingArgs& a, RingCtx& c) {
 // registers of a thread of a 512-thread CTA, two of which share an SM (the 16-bit LL128
 // instances hold fewer: their packed ops need more registers).
 template <int PROTO, int ESZ> struct RingUnroll {
-    static constexpr int value = PROTO == vProtoLL ? 2 : (PROTO == vProtoLL128 && ESZ == 2) ? 2 : 4;
+    static constexpr int value = PROTO == vProtoLL ? 2 : PROTO == vProtoLL128 ? (ESZ == 2 ? 2 : 4) : 4;
 };
+
+// The general step of an LL128 slot (out of line, so the common whole-line steps keep their
+// registers): bounds per lane, element accesses at ragged ends, the epilogue; lane 7 moves
+// its 8 data bytes alone.  Lines Lb + g + k * perIter, as in ring_slot.
+template <int DT, int OUT, int kind, int R>
+__device__ __noinline__ void ll128_step_general(const RingArgs& a, const char* rs, char* ss, const char* in,
+                                                char* out, unsigned int Lb, unsigned int lines, unsigned int P,
+                                                bool epi) {
+    constexpr int ESZ = DTypeOf<DT>::size;
+    constexpr int OSZ = DTypeOf<OUT>::size;
+    const bool aligned = a.aligned != 0;
+    const bool hasScale = a.hasScale != 0;
+    const unsigned int lane = threadIdx.x & 31, g = lane >> 3, t = lane & 7;
+    const unsigned int perIter = (blockDim.x >> 5) * 4;
+    const unsigned int halfBase = 112 * lines;
+    uint4 v[R], l[R];
+#pragma unroll
+    for (int k = 0; k < R; k++) {
+        const unsigned int L = Lb + g + k * perIter;
+        const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;   // payload byte
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        l[k] = v[k];
+        if (L < lines && b < P) {
+            if (kind & kRecv) v[k] = ld_fifo16(rs + (size_t)L * 128 + 16 * t);
+            if (kind & kLocal) {
+                const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
+                l[k] = t < 7 ? load_unit<ESZ, 16, 16>(in + b, ne, aligned)
+                             : load_unit<ESZ, 8, 8>(in + b, ne, aligned);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < R; k++) {
+        const unsigned int L = Lb + g + k * perIter;
+        const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;
+        if (L >= lines) break;
+        uint4 x = v[k];
+        if (b < P) {
+            if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
+            if (kind & kOut) {
+                const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
+                char* o = out + (size_t)(b / ESZ) * OSZ;
+                if (t < 7) store_unit<DT, OUT, 16, 16>(o, x, ne, aligned, epi, hasScale, a.scale);
+                else store_unit<DT, OUT, 8, 8>(o, x, ne, aligned, epi, hasScale, a.scale);
+            }
+        }
+        if (kind & kSend) {
+            if (t < 7) st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
+            else st_fifo8(ss + (size_t)L * 128 + 112, make_uint2(x.x, x.y));
+        }
+    }
+}
 
 // One slot of m elements (a slot is at most 16 MiB, so 32-bit offsets).  `in`: user input
 // at the slot's first element (kLocal); `out`: user output at the slot's first element
@@ -399,11 +451,12 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
         const unsigned int perIter = (T >> 5) * 4;       // lines the CTA covers per step
         const unsigned long long rflag = a.epochHi | (c.recvSeq + 1ull);
         const unsigned long long sflag = a.epochHi | (c.sendSeq + 1ull);
+        // The lines of this warp: warp * 4 + j * perIter + (0..3) for j = 0, 1, ...; the q-th
+        // of them (q = 4 j + i) is line warp * 4 + (q / 4) * perIter + q % 4.
+        const unsigned int mine = lines > warp * 4 ? (lines - warp * 4 + perIter - 1) / perIter * 4 : 0;
         if (kind & kRecv) {
-            // The flags of this warp's lines (warp * 4 + j * perIter + (0..3)), polled by all
-            // 32 lanes, four per lane per round (128 flags in flight per warp); a flag not
-            // yet set is waited for on its own.
-            const unsigned int mine = lines > warp * 4 ? (lines - warp * 4 + perIter - 1) / perIter * 4 : 0;
+            // Their flags, polled by all 32 lanes, four per lane per round (128 flags in
+            // flight per warp); a flag not yet set is waited for on its own.
             for (unsigned int q0 = lane; q0 < mine && !fail; q0 += 128) {
                 unsigned long long f[4];
 #pragma unroll
@@ -426,55 +479,72 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
         }
         if (!__any_sync(0xFFFFFFFFu, fail)) {
             const unsigned int halfBase = 112 * lines;
-            for (unsigned int L0 = warp * 4 + g; L0 < lines; L0 += R * perIter) {
-                uint4 v[R], l[R];
+            // Steps of R lines per lane group; lane group g takes lines Lb + g + k * perIter.
+            for (unsigned int Lb = warp * 4; Lb < lines; Lb += R * perIter) {
+                const bool whole = aligned && !epi && halfBase + 8 * (Lb + (R - 1) * perIter + 4) <= P;
+                if (whole) {
+                    // Every line of the step exists and is full: one 16-byte FIFO access per
+                    // lane (lane 7's covers its 8 data bytes and the flag's place, written as
+                    // zero -- never a valid flag -- until the flags follow the fence), one
+                    // 16-byte user access per lane 0..6, and the four 8-byte places of a step
+                    // (32 contiguous user bytes) read and written by lane 7 of groups 0 and 1,
+                    // 16 bytes each, and shared out with shuffles.
+                    uint4 v[R], l[R];
 #pragma unroll
-                for (int k = 0; k < R; k++) {
-                    const unsigned int L = L0 + k * perIter;
-                    const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;   // payload byte
-                    v[k] = make_uint4(0u, 0u, 0u, 0u);
-                    l[k] = v[k];
-                    if (L < lines && b < P) {
-                        if (kind & kRecv) {
-                            if (t < 7) v[k] = ld_fifo16(rs + (size_t)L * 128 + 16 * t);
-                            else { const uint2 d = ld_fifo8(rs + (size_t)L * 128 + 112); v[k].x = d.x; v[k].y = d.y; }
-                        }
+                    for (int k = 0; k < R; k++) {
+                        const unsigned int L = Lb + g + k * perIter;
+                        v[k] = make_uint4(0u, 0u, 0u, 0u);
+                        l[k] = v[k];
+                        if (kind & kRecv) v[k] = ld_fifo16(rs + (size_t)L * 128 + 16 * t);
                         if (kind & kLocal) {
-                            const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
-                            l[k] = t < 7 ? load_unit<ESZ, 16, 16>(in + b, ne, aligned)
-                                         : load_unit<ESZ, 8, 8>(in + b, ne, aligned);
+                            if (t < 7) l[k] = ld_user16(in + 112 * L + 16 * t);
+                            else if (g < 2) l[k] = ld_user16(in + halfBase + 8 * (Lb + k * perIter) + 16 * g);
                         }
                     }
-                }
 #pragma unroll
-                for (int k = 0; k < R; k++) {
-                    const unsigned int L = L0 + k * perIter;
-                    const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;
-                    if (L >= lines) break;
-                    uint4 x = v[k];
-                    if (b < P) {
-                        if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
-                        if (kind & kOut) {
-                            const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
-                            char* o = out + (size_t)(b / ESZ) * OSZ;
-                            if (t < 7) store_unit<DT, OUT, 16, 16>(o, x, ne, aligned, epi, hasScale, a.scale);
-                            else store_unit<DT, OUT, 8, 8>(o, x, ne, aligned, epi, hasScale, a.scale);
+                    for (int k = 0; k < R; k++) {
+                        const unsigned int L = Lb + g + k * perIter;
+                        uint4 x = v[k];
+                        if (kind & kLocal) {
+                            uint4 y = l[k];
+                            const int src = 7 + 8 * (g >> 1);       // lane 7 of group 0 or 1
+                            const unsigned int w0 = __shfl_sync(0xFFFFFFFFu, y.x, src);
+                            const unsigned int w1 = __shfl_sync(0xFFFFFFFFu, y.y, src);
+                            const unsigned int w2 = __shfl_sync(0xFFFFFFFFu, y.z, src);
+                            const unsigned int w3 = __shfl_sync(0xFFFFFFFFu, y.w, src);
+                            if (t == 7) y = (g & 1) ? make_uint4(w2, w3, 0u, 0u) : make_uint4(w0, w1, 0u, 0u);
+                            x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, y) : y;
                         }
+                        if (t == 7) {
+                            x.z = 0u;
+                            x.w = 0u;
+                        }
+                        if (kind & kOut) {
+                            const int lo = 7 + 16 * (g & 1), hi = lo + 8;   // lines 2g and 2g + 1 of the step
+                            const unsigned int a0 = __shfl_sync(0xFFFFFFFFu, x.x, lo);
+                            const unsigned int a1 = __shfl_sync(0xFFFFFFFFu, x.y, lo);
+                            const unsigned int b0 = __shfl_sync(0xFFFFFFFFu, x.x, hi);
+                            const unsigned int b1 = __shfl_sync(0xFFFFFFFFu, x.y, hi);
+                            if (t < 7) st_user16(out + 112 * L + 16 * t, x);
+                            else if (g < 2)
+                                st_user16(out + halfBase + 8 * (Lb + k * perIter) + 16 * g, make_uint4(a0, a1, b0, b1));
+                        }
+                        if (kind & kSend) st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
                     }
-                    if (kind & kSend) {
-                        if (t < 7) st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
-                        else st_fifo8(ss + (size_t)L * 128 + 112, make_uint2(x.x, x.y));
-                    }
+                } else {
+                    ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi);
                 }
-                test_jitter(a, L0);
+                test_jitter(a, Lb);
             }
             if (kind & kSend) {
+                // After every lane's data stores: the flags, by all 32 lanes.
                 test_jitter(a, 0x5157u);
                 __syncwarp();
                 fence_acq_rel();
-                if (t == 7)
-                    for (unsigned int L = warp * 4 + g; L < lines; L += perIter)
-                        st_volatile_u64(ss + (size_t)L * 128 + 120, sflag);
+                for (unsigned int q = lane; q < mine; q += 32) {
+                    const unsigned int L = warp * 4 + (q >> 2) * perIter + (q & 3);
+                    if (L < lines) st_volatile_u64(ss + (size_t)L * 128 + 120, sflag);
+                }
             }
         }
     }

@@ -1,9 +1,8 @@
 // noalloc.cu -- the staged ring all-reduce for callers that cannot allocate memory.
 //
-// Some callers cannot call cudaMalloc: code running while a CUDA graph is being
-// captured (a cudaMalloc there is not captured and breaks the capture), allocators and
-// memory-pool callbacks that must not recurse into the allocator, and runtimes that
-// hand out all device memory themselves ahead of time.  vcommInit allocates (its status
+// Some callers cannot call cudaMalloc: allocators and memory-pool callbacks that must not
+// recurse into the allocator, and runtimes that hand out all device memory themselves
+// ahead of time and own every byte of it.  vcommInit allocates (its status
 // words, and the ring FIFOs on first use), so those callers cannot use a communicator.
 // vAllReduceNoAlloc gives them the ring all-reduce without one: its FIFOs and control
 // words live in a fixed array compiled into this library.
@@ -12,7 +11,9 @@
 // device address (on the host the name is only a stand-in), so the first call on each
 // device looks the real address up with cudaGetSymbolAddress while that device is
 // current and keeps it.  Every GPU that loads the library holds the array until the
-// process exits.
+// process exits.  A cudaDeviceReset unloads the module and with it the array; every call
+// therefore first checks, with cudaPointerGetAttributes, that the kept address is still a
+// device allocation of the current context, and looks it up again if not.
 #include <mutex>
 
 #include "internal.h"
@@ -45,9 +46,18 @@ size_t elem_size(int dt) {
     }
 }
 
-// Per-device set-up: the scratch array's device address, looked up with the device current.
+// Per-device set-up: the scratch array's device address, looked up with the device current
+// (again if a device reset has invalidated the kept one).
 cudaError_t scratch_address(int dev, unsigned char** out) {
     std::lock_guard<std::mutex> lock(g_setupMutex);
+    if (g_scratchAddr[dev]) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, g_scratchAddr[dev]) != cudaSuccess || attr.type != cudaMemoryTypeDevice ||
+            attr.device != dev) {
+            cudaGetLastError();
+            g_scratchAddr[dev] = nullptr;
+        }
+    }
     if (!g_scratchAddr[dev]) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_ringScratch);

@@ -283,18 +283,21 @@ vResult_t vScatter(const void* const* sendbuffs, void* const* recvbuffs, size_t 
                    vDataType_t datatype, int root, vcomm_t comm, cudaStream_t stream);
 
 /* Ring all-reduce for callers that cannot allocate device memory.  The pages have no
- * counterpart to this call; it exists for code that must not call cudaMalloc (code
- * running during CUDA graph capture, allocator or memory-pool callbacks, runtimes that
- * own all device memory).  No communicator is needed and nothing is allocated: the
- * staging FIFOs and control words live in one fixed device array inside this library
- * (64 KiB + 8 MiB, held on every GPU that loads the library until the process exits).
+ * counterpart to this call; it exists for code that must not call cudaMalloc (allocator
+ * or memory-pool callbacks, which must not re-enter the allocator; runtimes that own all
+ * device memory and hand it out themselves).  No communicator is needed and nothing is
+ * allocated: the staging FIFOs and control words live in one fixed device array inside
+ * this library (64 KiB + 8 MiB, held on every GPU that loads the library until the
+ * process exits).
  * The result is bit-identical to vAllReduce.  The caller passes the buffers as for
  * vAllReduce plus nRanks (2..64), nChannels and protocol (Simple, LL or LL128); the
  * ring uses chunks of 64 KiB of data (32 KiB for LL and LL128, whose slots take more FIFO
  * bytes than they carry), so nRanks * nChannels may be at most 64 -- larger rings
  * return vInvalidArgument (as do the usual argument errors), and a ring whose CTAs
  * cannot all be resident returns vInvalidUsage.  The first call on a device looks up
- * the array's address (cudaGetSymbolAddress), so make it before any stream capture.
+ * the array's address (cudaGetSymbolAddress), so make it before any stream capture;
+ * every call checks the kept address (cudaPointerGetAttributes) and looks it up again
+ * after a cudaDeviceReset.
  * Every call clears and reuses the same array: calls whose kernels overlap on the GPU
  * (another stream, another thread) race and must be serialized by the caller.  Waits
  * inside the kernel still end after 2 s without progress, but such a failure is not

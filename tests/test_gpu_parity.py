@@ -355,22 +355,30 @@ def test_invalid_arguments_launch_nothing(comms):
 # Full-size workloads, element by element
 # ---------------------------------------------------------------------------------------
 
+@pytest.fixture(scope="module")
+def allreduce_64mib():
+    """The 8 x 64 MiB fp32 uniform[-1, 1) workload (seed 1) and its oracle result, computed
+    once for every channel / chunk / protocol cell that checks against it."""
+    n, count = 8, 16 << 20                                          # 64 MiB fp32 per rank
+    xs = inputs.uniform_ranks(n, count, torch.float32, 1)
+    return xs, oracle.allreduce(xs, "sum", nthreads=NTHREADS)
+
+
 @pytest.mark.parametrize("variant", [("onepass", V.vProtoSimple), ("ring", V.vProtoSimple),
                                      ("ring", V.vProtoLL), ("ring", V.vProtoLL128)],
                          ids=["onepass", "ring-simple", "ring-ll", "ring-ll128"])
-def test_allreduce_64MiB_8_ranks(comms, variant):
-    # the 8 x 64 MiB fp32 workload: channels {1, 8, 16, 32} and, for the staged ring,
-    # chunks from 128 KiB to 2 MiB, all bit-identical to the oracle
+def test_allreduce_64MiB_8_ranks(comms, variant, allreduce_64mib):
+    # the 8 x 64 MiB fp32 workload: channels {1, 8, 16, 32}; for the staged ring with Simple
+    # every chunk size from 128 KiB to 2 MiB, with LL and LL128 chunks of 128 KiB, 1 MiB and
+    # 2 MiB; all bit-identical to the oracle
     algo, proto = variant
-    n, count = 8, 16 << 20                                          # 64 MiB fp32 per rank
-    xs = inputs.uniform_ranks(n, count, torch.float32, 1)
-    want = oracle.allreduce(xs, "sum", nthreads=NTHREADS)
+    xs, want = allreduce_64mib
     if algo == "onepass":
         cases = [(ch, None) for ch in (1, 8, 16, 32)]
     elif proto == V.vProtoSimple:
-        cases = [(ch, chunk) for ch in (1, 8, 16, 32) for chunk in (128 << 10, 512 << 10, 2 << 20)]
+        cases = [(ch, chunk) for ch in (1, 8, 16, 32) for chunk in (128 << 10, 256 << 10, 512 << 10, 1 << 20, 2 << 20)]
     else:
-        cases = [(32, 128 << 10), (32, 1 << 20)]
+        cases = [(ch, chunk) for ch in (1, 8, 16, 32) for chunk in (128 << 10, 1 << 20, 2 << 20)]
     for channels, chunk in cases:
         got = run_allreduce(comms, xs, "sum", algo, proto, channels=channels, chunk=chunk)
         assert_bits_equal(got, want, f"64MiB channels={channels} chunk={chunk}")

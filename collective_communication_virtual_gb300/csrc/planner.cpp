@@ -234,14 +234,19 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
             } else {
                 size_t blocks = q->coll == vCollBroadcast ? 1 : q->coll == vCollAllToAll ? (size_t)N * N : (size_t)N;
                 // Copies: 64 KiB tiles (128 bytes in flight per thread of a 512-thread CTA)
-                // unless that leaves fewer than four waves of resident CTAs (two per SM);
-                // then 32 or 16 KiB tiles, so the last, partly filled wave is a smaller
-                // share of the launch.
+                // unless that leaves fewer than 8 tiles per SM; then 32 or 16 KiB tiles, so the
+                // last, partly filled wave is a smaller share of the launch.  The fan-out
+                // copies (all-gather, broadcast: 8 stores per loaded byte) go on halving to
+                // 8 KiB while there are fewer than 16 tiles per SM: measured on GB300, the
+                // 8-rank FSDP bucket all-gather (3.125 MiB bf16 per rank) takes 37.5 us with
+                // 16 KiB tiles and 36.5 us with 8 KiB (4 KiB: 37.3).
                 // Small messages: tiles down to 2 KiB until there is a tile for every SM.
+                const bool fanoutCopy = q->coll == vCollAllGather || q->coll == vCollBroadcast;
                 size_t tile = (size_t)64 * 1024;
                 auto tiles = [&](size_t t) { return div_up(chElems * esz, t) * blocks * (size_t)q->nChannels; };
                 if (!q->persistentGrid) {
                     while (tile > 16 * 1024 && tiles(tile) < (size_t)8 * smCount) tile /= 2;
+                    while (fanoutCopy && tile > 8 * 1024 && tiles(tile) < (size_t)16 * smCount) tile /= 2;
                     while (tile > 2 * 1024 && tiles(tile) < (size_t)smCount) tile /= 2;
                 }
                 p->tileBytes = tile;
@@ -252,7 +257,6 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
                 // Measured on GB300 with 32 bytes for all: gather and scatter of 64 MiB at
                 // the root ran at 0.87-0.89 of the copy bandwidth, against 0.98-1.03 with
                 // 128, and the 8 x 4 MiB all-to-all took 14.1 us, against 7.2.
-                const bool fanoutCopy = q->coll == vCollAllGather || q->coll == vCollBroadcast;
                 const size_t perThread = fanoutCopy ? 32 : 128;
                 p->threadsPerCta = (int)std::min<size_t>(vc::kOnePassThreads, std::max<size_t>(64, tile / perThread));
                 maxPer = div_up(chElems * esz, tile) * blocks;
@@ -311,6 +315,14 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         if (proto == vProtoLL) fit /= 2;
         else if (proto == vProtoLL128) fit = fit / 128 * 120;
         chunk = std::min<size_t>((size_t)1 << 20, std::max<size_t>(16384, pow2_floor(fit)));
+        // Broadcast passes the whole buffer down a chain of N-1 hops, so its time is about
+        // (hops + slots - 1) slot times: a channel's share is cut into at least 8 slots so the
+        // hops overlap (for the ring collectives every step moves another block, and large
+        // slots, which amortise the per-slot handshake, win).
+        if (q->coll == vCollBroadcast) {
+            const size_t share = std::min(p->channelElems, B) * esz;
+            chunk = std::max<size_t>(4096, std::min(chunk, pow2_floor(std::max<size_t>(1, share / 2))));
+        }
     }
     const size_t slotPayload = chunk / vc::kChunkSlots;   // >= 1 KiB, a power of two
     size_t slotBytes = slotPayload;

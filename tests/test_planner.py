@@ -235,12 +235,17 @@ def test_element_path_threads_take_8_elements_of_every_rank():
 
 
 def test_copy_threads_follow_how_often_a_loaded_byte_is_stored():
-    # 8 MiB blocks, 8 ranks: 32 KiB tiles.  All-gather and broadcast store every loaded byte
-    # 8 times: 32 bytes of a tile per thread (capped at 512 threads).  Gather, scatter and
-    # all-to-all store it once: 128 bytes per thread.
-    for coll in (V.vCollAllGather, V.vCollBroadcast):
-        p = plan(coll=coll, count=1 << 21, aligned32=1, noBulkCopy=1)
-        assert p.threadsPerCta == 512
+    # 8 MiB blocks, 8 ranks.  All-gather and broadcast store every loaded byte 8 times: 32
+    # bytes of a tile per thread (capped at 512 threads); their tiles halve to 8 KiB while
+    # there are fewer than 16 per SM (all-gather: 16 KiB, 4096 tiles; broadcast, one block:
+    # 8 KiB).  Gather, scatter and all-to-all store it once: 128 bytes per thread.
+    p = plan(coll=V.vCollAllGather, count=1 << 21, aligned32=1, noBulkCopy=1)
+    assert p.tileBytes == 16384 and p.threadsPerCta == 512
+    p = plan(coll=V.vCollBroadcast, count=1 << 21, aligned32=1, noBulkCopy=1)
+    assert p.tileBytes == 8192 and p.threadsPerCta == 256 and p.gridCtas == 1024
+    # the FSDP bucket's all-gather: 3.125 MiB bf16 blocks -> 8 KiB tiles, 3200 CTAs
+    p = plan(coll=V.vCollAllGather, count=1_638_400, datatype=V.vBFloat16, aligned32=1, noBulkCopy=1)
+    assert p.tileBytes == 8192 and p.threadsPerCta == 256 and p.gridCtas == 3200
     for coll in (V.vCollGather, V.vCollScatter):
         p = plan(coll=coll, count=1 << 21, aligned32=1, noBulkCopy=1)
         assert p.tileBytes == 32768 and p.threadsPerCta == 256 and p.gridCtas == 2048
@@ -354,7 +359,7 @@ def test_small_work_spreads_over_more_smaller_ctas():
     p = plan(coll=V.vCollAllGather, count=1024, aligned32=1, noBulkCopy=1)     # 4 KiB blocks
     assert p.tileBytes == 2048 and p.threadsPerCta == 64 and p.gridCtas == 2 * 8
     p = plan(coll=V.vCollAllGather, count=1 << 20, aligned32=1, noBulkCopy=1)  # 4 MiB blocks
-    assert p.tileBytes == 16384 and p.threadsPerCta == 512
+    assert p.tileBytes == 8192 and p.threadsPerCta == 256                     # 4096 tiles
     # the persistent shape keeps 512-thread CTAs and 64 KiB tiles
     p = plan(count=4096, aligned32=1, persistentGrid=1)
     assert p.threadsPerCta == 512

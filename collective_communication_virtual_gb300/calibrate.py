@@ -1,79 +1,112 @@
-"""Refit the planner's cost-model constants on the GPU at hand.
+"""Refit the planner's ring cost model from measured staged-ring times.
 
-The planner models a ring all-reduce as latency + bus bytes / bus rate per protocol and
-channel count (the ring.cc form of the NCCL book, chapter 5), and the one-pass kernels as
-latency + minimum HBM bytes / rate.  This script measures the anchor points through the
-library -- an fp32 sum all-reduce over 8 virtual ranks, replayed from a CUDA graph, at
-1 KiB per rank (latency) and 256 MiB per rank (rate), for 1, 8 and 32 channels -- and
-prints the constants in the form `csrc/planner.cpp` declares them.
+The planner predicts a staged-ring collective of x bytes per rank over N ranks as
+  ring steps (all-reduce, reduce-scatter, all-gather):  lat + max(0, x - knee) / rate
+  broadcast chain:                                       lat + c * sqrt(x) + x / rate
+for each (collective, protocol) at 1, 8 and 32 channels (interpolated in log2 of the
+channel count, held flat beyond), with lat and the byte terms scaled from N = 8 by the
+step count (the ring.cc form of the NCCL book, chapter 5: time = latency + bus bytes /
+bus bandwidth, with LL and LL128 trading bandwidth for latency).  The knee is the payload
+that the pipeline's first round carries at no extra cost; the broadcast's square-root
+term is the pipeline fill of a chain whose slot count grows as sqrt(bytes) (the planner's
+broadcast slot rule).
 
-    python -m collective_communication_virtual_gb300.calibrate
+Input: the `ring_sweep` rows that `bench.py --ring-sweep` prints (device time of fp32 sum
+over 8 ranks, default chunks, 1 KiB .. 1 GiB per rank in powers of 4), committed as
+ring_timings_gb300.json.  Output: the table planner.cpp declares.
+
+    python -m collective_communication_virtual_gb300.calibrate [timings.json]
 """
 from __future__ import annotations
 
-N_RANKS = 8
-SMALL, LARGE = 1024, 256 << 20
+import json
+import math
+import os
+import sys
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+DATA = os.path.join(HERE, "ring_timings_gb300.json")
+COLLS = ("allreduce", "reduce_scatter", "allgather", "broadcast")
+PROTOS = ("simple", "ll", "ll128")
+CHANNELS = (1, 8, 32)
 
 
-def graph_time_us(torch, V, comm, send, recv, count, launches, reps):
-    for _ in range(2):
-        V.vAllReduce(send, recv, count, torch.float32, "sum", comm)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(launches):
-            V.vAllReduce(send, recv, count, torch.float32, "sum", comm)
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e3 / (reps * launches)
+def load(path=DATA):
+    with open(path) as f:
+        d = json.load(f)
+    cols = d["columns"]
+    return [dict(zip(cols, r)) for r in d["rows"] if r[cols.index("device_us")] is not None]
+
+
+def _lsq(cols, m):
+    """Least squares on the relative error: minimise sum((cols . p) / m - 1)^2."""
+    A = np.stack([c / m for c in cols], 1)
+    p, *_ = np.linalg.lstsq(A, np.ones_like(m), rcond=None)
+    return p
+
+
+def fit_curve(coll, x, m):
+    """(lat_us, bytes_per_us, third) for one (collective, protocol, channels) curve; third
+    is the knee in bytes (ring steps) or the square-root coefficient (broadcast)."""
+    x, m = np.asarray(x, float), np.asarray(m, float)
+    one = np.ones_like(x)
+    if coll == "broadcast":
+        lat, c, inv = _lsq([one, np.sqrt(x), x], m)
+        if c < 0 or inv <= 0:
+            (lat, inv), c = _lsq([one, x], m), 0.0
+        return float(lat), float(1.0 / inv), float(c)
+    best = None
+    for knee in [0.0] + [float(2 ** k) for k in range(10, 26)]:
+        xe = np.maximum(0.0, x - knee)
+        lat, inv = _lsq([one, xe], m)
+        if lat < 0 or inv <= 0:
+            continue
+        score = float(np.sum(((lat + inv * xe) / m - 1.0) ** 2))
+        if best is None or score < best[0]:
+            best = (score, float(lat), float(1.0 / inv), knee)
+    return best[1], best[2], best[3]
+
+
+def fit(rows):
+    table = {}
+    for coll in COLLS:
+        for proto in PROTOS:
+            table[(coll, proto)] = []
+            for ch in CHANNELS:
+                pts = sorted((r["bytes_per_rank"], r["device_us"]) for r in rows
+                             if r["coll"] == coll and r["proto"] == proto and r["channels"] == ch)
+                table[(coll, proto)].append(fit_curve(coll, [p[0] for p in pts], [p[1] for p in pts]))
+    return table
+
+
+def cpp(table):
+    out = ["const RingFit kRingFit[4][3] = {                         // calibrate.py prints these"]
+    for coll in COLLS:
+        out.append(f"    {{  // {coll}")
+        for proto in PROTOS:
+            f = table[(coll, proto)]
+            lat = ", ".join(f"{v[0]:.2f}" for v in f)
+            rate = ", ".join(f"{v[1]:.1f}" for v in f)
+            third = ", ".join((f"{v[2]:.0f}" if coll != "broadcast" else f"{v[2]:.5f}") for v in f)
+            out.append(f"        {{{{{lat}}}, {{{rate}}}, {{{third}}}}},   // {proto}")
+        out.append("    },")
+    out.append("};")
+    return "\n".join(out)
 
 
 def main() -> None:
-    import torch
-
-    from collective_communication_virtual_gb300 import build, vcomm as V
-
-    build.build()
-    dev = torch.device("cuda:0")
-    bufs = {}
-    for nbytes in (SMALL, LARGE):
-        count = nbytes // 4
-        bufs[nbytes] = ([torch.rand(count, device=dev) for _ in range(N_RANKS)],
-                        [torch.empty(count, device=dev) for _ in range(N_RANKS)], count)
-    steps = 2 * (N_RANKS - 1)
-    rows = []
-    for proto, name in ((V.vProtoSimple, "Simple"), (V.vProtoLL, "LL"), (V.vProtoLL128, "LL128")):
-        lat, rate = [], []
-        for ch in (1, 8, 32):
-            comm = V.vcommInit(N_RANKS, ch, proto)
-            V.vcommSetAlgo(comm, "ring")
-            send, recv, count = bufs[SMALL]
-            t0 = graph_time_us(torch, V, comm, send, recv, count, 20, 5)
-            send, recv, count = bufs[LARGE]
-            t1 = graph_time_us(torch, V, comm, send, recv, count, 1, 2)
-            V.vcommDestroy(comm)
-            lat.append(t0)
-            rate.append(LARGE * steps / N_RANKS / (t1 - t0))
-        rows.append(f"    {{{{{lat[0]:.1f}, {lat[1]:.1f}, {lat[2]:.1f}}}, "
-                    f"{{{rate[0]:.1f}, {rate[1]:.1f}, {rate[2]:.1f}}}}},   // {name}")
-    comm = V.vcommInit(N_RANKS, 1, V.vProtoSimple)
-    V.vcommSetAlgo(comm, "onepass")
-    send, recv, count = bufs[SMALL]
-    t0 = graph_time_us(torch, V, comm, send, recv, count, 20, 5)
-    send, recv, count = bufs[LARGE]
-    t1 = graph_time_us(torch, V, comm, send, recv, count, 4, 3)
-    V.vcommDestroy(comm)
-    print("const RingFit kRingFit[3] = {")
-    print("\n".join(rows))
-    print("};")
-    print(f"const double kOnePassLatUs = {t0:.1f};")
-    print(f"const double kOnePassBytesPerUs = {2 * N_RANKS * LARGE / (t1 - t0):.3e};")
+    rows = load(sys.argv[1] if len(sys.argv) > 1 else DATA)
+    table = fit(rows)
+    print(cpp(table))
+    errs = []
+    for r in rows:
+        lat, rate, third = table[(r["coll"], r["proto"])][CHANNELS.index(r["channels"])]
+        x = r["bytes_per_rank"]
+        pred = lat + (third * math.sqrt(x) + x / rate if r["coll"] == "broadcast" else max(0.0, x - third) / rate)
+        errs.append(abs(pred / r["device_us"] - 1.0))
+    print(f"// median relative error {float(np.median(errs)):.3f}, max {max(errs):.3f} over {len(errs)} points")
 
 
 if __name__ == "__main__":

@@ -44,22 +44,46 @@ size_t pow2_floor(size_t x) {
 // The ring model of the NCCL book chapter 5 (ring.cc): time = latency + bus bytes / bus
 // bandwidth, where a collective of S bytes per rank moves S * nSteps / N bus bytes
 // (nSteps = 2(N-1) for all-reduce, N-1 otherwise), and LL / LL128 trade bandwidth for
-// latency.  The constants are refit on a GB300 (collective_communication_virtual_gb300/
-// calibrate.py) from CUDA-graph replay times of an fp32 all-reduce over 8 virtual ranks
-// at 1 KiB and 256 MiB per rank: latency = time at 1 KiB;
-// bus rate from the 256 MiB point, at 1, 8 and 32 channels (interpolated in log2 of the
-// channel count, held flat beyond).  Ring latency grows with the number of steps, so it
-// is scaled by nSteps / 14 (14 steps for an 8-rank all-reduce).  The one-pass kernels are
-// modelled as latency + minimum HBM bytes / effective HBM rate.
+// latency.  Fitted on GB300 per collective and protocol at 1, 8 and 32 channels
+// (collective_communication_virtual_gb300/calibrate.py, from the staged-ring times in
+// ring_timings_gb300.json: fp32 sum over 8 ranks, default chunks, 1 KiB .. 1 GiB per rank)
+// with one more term each, which the data ask for:
+//  * ring steps (all-reduce, reduce-scatter, all-gather): lat + max(0, x - knee) / rate --
+//    the first round of the pipeline carries up to `knee` bytes at no extra cost;
+//  * broadcast (a chain): lat + c sqrt(x) + x / rate -- the pipeline fill of a chain whose
+//    slot count grows as sqrt(x) (the broadcast slot rule below).
+// x is bytes per rank at 8 ranks; for N ranks the latency scales by nSteps, the ring
+// steps' bytes by the bus bytes per rank byte (nSteps / N) and the chain's fill by
+// sqrt(N - 2).  Channel counts between the anchors interpolate in log2; beyond 32 the fit
+// is held flat.  The one-pass kernels are modelled as latency + minimum HBM bytes / rate.
 struct RingFit {
     double latUs[3];           // at 1, 8, 32 channels
-    double busBytesPerUs[3];
+    double bytesPerUs[3];      // bytes per rank per microsecond, at 8 ranks
+    double shape[3];           // ring steps: knee (bytes per rank); broadcast: sqrt coefficient
 };
-const RingFit kRingFit[3] = {                                // calibrate.py prints these
-    {{39.1, 37.1, 37.6}, {14987.1, 103612.9, 246451.2}},    // Simple
-    {{29.7, 27.2, 27.7}, {7345.8, 44947.7, 128509.1}},      // LL
-    {{49.2, 43.2, 44.9}, {8382.1, 62053.3, 134930.9}},      // LL128
+const RingFit kRingFit[4][3] = {                         // calibrate.py prints these
+    {  // allreduce
+        {{41.80, 38.78, 39.12}, {8645.2, 65752.5, 157985.2}, {32768, 0, 0}},   // simple
+        {{30.19, 27.14, 28.47}, {4033.7, 28378.9, 77010.5}, {32768, 131072, 524288}},   // ll
+        {{50.82, 49.01, 50.49}, {6348.7, 47577.8, 109244.0}, {32768, 1024, 0}},   // ll128
+    },
+    {  // reduce_scatter
+        {{22.75, 18.97, 19.33}, {13597.1, 98357.8, 261865.1}, {131072, 1024, 1024}},   // simple
+        {{17.26, 13.55, 14.11}, {6366.2, 45197.8, 138044.6}, {131072, 131072, 65536}},   // ll
+        {{29.58, 25.49, 27.10}, {8987.6, 68731.7, 187890.3}, {131072, 1024, 1024}},   // ll128
+    },
+    {  // allgather
+        {{21.10, 18.12, 18.29}, {22941.9, 173400.9, 318753.8}, {131072, 524288, 2097152}},   // simple
+        {{16.47, 13.48, 14.40}, {9764.9, 65943.3, 161778.7}, {32768, 131072, 262144}},   // ll
+        {{27.26, 24.82, 25.75}, {17484.4, 132884.4, 228045.0}, {1024, 1024, 1024}},   // ll128
+    },
+    {  // broadcast
+        {{17.60, 14.47, 15.31}, {22657.9, 170398.2, 372302.7}, {0.03436, 0.01178, 0.00796}},   // simple
+        {{10.44, 7.92, 8.03}, {9969.6, 63832.6, 117667.4}, {0.00468, 0.00518, 0.00734}},   // ll
+        {{20.84, 18.70, 19.50}, {15826.4, 121668.0, 253030.2}, {0.04972, 0.02105, 0.01647}},   // ll128
+    },
 };
+// median relative error 0.028, max 0.223 over 396 points
 const double kOnePassLatUs = 1.5;
 const double kOnePassBytesPerUs = 7.097e6;                   // minimum bytes / (time - latency)
 
@@ -71,12 +95,23 @@ double interp_ch(const double v[3], int ch) {
 
 int n_steps(int coll, int N) { return coll == vCollAllReduce ? 2 * (N - 1) : N - 1; }
 
+int fit_row(int coll) {
+    switch (coll) {
+    case vCollAllReduce: return 0;
+    case vCollReduceScatter: return 1;
+    case vCollAllGather: return 2;
+    default: return 3;
+    }
+}
+
 double predict_ring_us(int proto, int coll, int N, int nCh, double bytesPerRank) {
-    const RingFit& f = kRingFit[proto];
-    const double steps = (double)n_steps(coll, N);
-    const double lat = interp_ch(f.latUs, nCh) * steps / 14.0;
-    const double busBytes = bytesPerRank * steps / N;
-    return lat + busBytes / interp_ch(f.busBytesPerUs, nCh);
+    const RingFit& f = kRingFit[fit_row(coll)][proto];
+    const double lat = interp_ch(f.latUs, nCh) * n_steps(coll, N) / n_steps(coll, 8);
+    const double rate = interp_ch(f.bytesPerUs, nCh), shape = interp_ch(f.shape, nCh);
+    if (coll == vCollBroadcast)
+        return lat + shape * std::sqrt(bytesPerRank * std::max(0, N - 2) / 6.0) + bytesPerRank / rate;
+    const double scale = ((double)n_steps(coll, N) / N) / ((double)n_steps(coll, 8) / 8.0);
+    return lat + std::max(0.0, bytesPerRank * scale - shape) / rate;
 }
 
 double predict_onepass_us(double minBytes) { return kOnePassLatUs + minBytes / kOnePassBytesPerUs; }
@@ -315,13 +350,18 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
         if (proto == vProtoLL) fit /= 2;
         else if (proto == vProtoLL128) fit = fit / 128 * 120;
         chunk = std::min<size_t>((size_t)1 << 20, std::max<size_t>(16384, pow2_floor(fit)));
-        // Broadcast passes the whole buffer down a chain of N-1 hops, so its time is about
-        // (hops + slots - 1) slot times: a channel's share is cut into at least 8 slots so the
-        // hops overlap (for the ring collectives every step moves another block, and large
-        // slots, which amortise the per-slot handshake, win).
-        if (q->coll == vCollBroadcast) {
-            const size_t share = std::min(p->channelElems, B) * esz;
-            chunk = std::max<size_t>(4096, std::min(chunk, pow2_floor(std::max<size_t>(1, share / 2))));
+        // Broadcast passes a channel's whole share (D bytes) down a chain of N-1 hops in k
+        // slots, which takes about (N - 2 + k) (h + D / (k R)) for a per-slot handshake h
+        // and a per-CTA rate R; the best k is sqrt((N - 2) D / (h R)).  With h R about
+        // 40 KB on GB300 (2 us at 20 GB/s), the slot is D / k rounded up to a power of two,
+        // between 1 KiB and a quarter of the chunk.  (For the ring collectives every step
+        // moves another block, and large slots, which amortise the handshake, win.)
+        if (q->coll == vCollBroadcast && N > 2) {
+            const double share = (double)(std::min(p->channelElems, B) * esz);
+            const double k = std::max(1.0, std::sqrt((double)(N - 2) * share / 40960.0));
+            size_t slot = 1024;
+            while ((double)slot < share / k && slot * vc::kChunkSlots < chunk) slot *= 2;
+            chunk = slot * vc::kChunkSlots;
         }
     }
     const size_t slotPayload = chunk / vc::kChunkSlots;   // >= 1 KiB, a power of two

@@ -118,15 +118,19 @@ def test_auto_protocol_follows_the_fitted_ring_model():
         assert auto.predictedUs == pytest.approx(min(each))
 
 
-def test_model_reproduces_its_measured_anchor_points():
-    # fp32 all-reduce, 8 ranks: one-pass 1.5 us at 1 KiB and 1.5 + 4 GiB / 7.097e6 B/us at
-    # 256 MiB per rank; ring Simple at 32 channels 37.6 us and 37.6 + 256 MiB * 14/8 / 246451.2
+def test_model_evaluates_its_fitted_constants():
+    # fp32 all-reduce, 8 ranks: one-pass 1.5 us + minimum bytes / 7.097e6 B/us; the staged
+    # ring with Simple at 32 channels: 39.12 us + bytes per rank / 157985.2 B/us (knee 0),
+    # at 1 channel 41.80 us + max(0, bytes - 32 KiB) / 8645.2 B/us
     big = 256 << 20
-    assert plan(count=256).predictedUs == pytest.approx(1.5, rel=0.01)
+    assert plan(count=256).predictedUs == pytest.approx(1.5 + 16 * 1024 / 7.097e6, rel=0.001)
     assert plan(count=64 << 20).predictedUs == pytest.approx(1.5 + 16 * big / 7.097e6, rel=0.001)
-    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(37.6, rel=0.01)
+    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(39.12 + 1024 / 157985.2,
+                                                                                        rel=1e-4)
     assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=32).predictedUs == \
-        pytest.approx(37.6 + big * 14 / 8 / 246451.2, rel=0.001)
+        pytest.approx(39.12 + big / 157985.2, rel=1e-4)
+    assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=1).predictedUs == \
+        pytest.approx(41.80 + (big - 32768) / 8645.2, rel=1e-4)
 
 
 def test_auto_algorithm_picks_the_one_pass_kernels():

@@ -106,6 +106,15 @@ __device__ __forceinline__ void st_fifo16(void* p, uint4 v) {
     asm volatile("st.global.cg.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(l2_evict_last()) : "memory");
 }
+// Drop a consumed 128-byte FIFO line from L2 without writing it back to DRAM (its data is
+// dead until the producer rewrites it; PTX treats the discard as a weak write of an
+// indeterminate value, which the fence before the head word orders before that rewrite).
+// Only Simple slots are discarded: their validity lives in the tail counters, while a flag
+// protocol could find an old flag of the same value in the stale DRAM copy the discard
+// exposes (an LL epoch byte that wrapped, or a captured graph replaying its fixed epoch).
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" :: "l"(p) : "memory");
+}
 __device__ __forceinline__ void st_fifo8(void* p, uint2 v) {
     asm volatile("st.global.cg.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;"
                  :: "l"(p), "r"(v.x), "r"(v.y), "l"(l2_evict_last()) : "memory");
@@ -390,6 +399,18 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                 if (kind & kOut)
                     store_unit<DT, OUT, 16, 16>(out + (size_t)u * UE * OSZ, x, ne, aligned, epi, hasScale, a.scale);
                 if (kind & kSend) st_fifo16(ss + (size_t)u * 16, x);
+            }
+            if (kind & kRecv) {
+                // The warp read R runs of 32 units (4 lines each); once every lane has used
+                // them, lanes 0..4R-1 discard one line each.  Only when every run is whole,
+                // which the warp decides alike (ub is the warp's first unit of the round).
+                const unsigned int ub = u0 - (threadIdx.x & 31u);
+                if (ub + (R - 1) * T + 32 <= units) {
+                    __syncwarp();
+                    const unsigned int lane = threadIdx.x & 31u;
+                    if (lane < 4u * R)
+                        discard_l2_line(rs + (size_t)(ub + (lane >> 2) * T) * 16 + 128 * (lane & 3u));
+                }
             }
             test_jitter(a, u0);
         }

@@ -205,7 +205,9 @@ vResult_t vcommSetTimeoutMs(vcomm_t comm, int timeoutMs);
 /* collective is a copy.                                                             */
 /* ------------------------------------------------------------------------------- */
 
-/* recvbuffs[r][e] = the reduction over all ranks of sendbuffs[.][e], e < count, for
+/* All-reduce ("AI Systems Performance Engineering (3)", collective table, all-reduce row;
+ * NCCL book section 2.3, the ring as reduce-scatter then all-gather):
+ * recvbuffs[r][e] = the reduction over all ranks of sendbuffs[.][e], e < count, for
  * every rank r.  Element e belongs to block b = e / B with
  * B = alignUp(ceil(count / nRanks), 16 / elemSize) (the tail-chunk rule of
  * RingARAlgorithm::getNextSendAddr, NCCL book section 2.3), and block b is reduced in
@@ -214,7 +216,10 @@ vResult_t vcommSetTimeoutMs(vcomm_t comm, int timeoutMs);
 vResult_t vAllReduce(const void* const* sendbuffs, void* const* recvbuffs, size_t count,
                      vDataType_t datatype, vRedOp_t op, vcomm_t comm, cudaStream_t stream);
 
-/* sendbuffs[r] holds nRanks * recvcount elements; recvbuffs[r][t] = the reduction of
+/* Reduce-scatter ("AI Systems Performance Engineering (3)", collective table,
+ * reduce-scatter row: rank r ends with the reduction of block r; the reduce-scatter half
+ * of the ring in the NCCL book section 2.3).
+ * sendbuffs[r] holds nRanks * recvcount elements; recvbuffs[r][t] = the reduction of
  * sendbuffs[.][r * recvcount + t] in ring order ranks r+1, ..., r.  In place means
  * recvbuffs[r] == sendbuffs[r] + r * recvcount. */
 vResult_t vReduceScatter(const void* const* sendbuffs, void* const* recvbuffs, size_t recvcount,
@@ -229,18 +234,25 @@ vResult_t vReduceScatterScaleCast(const void* const* sendbuffs, void* const* rec
                                   vDataType_t outType, float scale, vcomm_t comm,
                                   cudaStream_t stream);
 
-/* recvbuffs[r][s * sendcount + t] = sendbuffs[s][t] for every r.  op is ignored (the
+/* All-gather ("AI Systems Performance Engineering (3)", collective table, all-gather row:
+ * every rank ends with every rank's piece, in rank order; the ring all-gather of "NCCL
+ * Expert Course 17" and NCCL book section 2.3 when staged):
+ * recvbuffs[r][s * sendcount + t] = sendbuffs[s][t] for every r.  op is ignored (the
  * data is moved as bytes).  In place means sendbuffs[r] == recvbuffs[r] + r * sendcount. */
 vResult_t vAllGather(const void* const* sendbuffs, void* const* recvbuffs, size_t sendcount,
                      vDataType_t datatype, vRedOp_t op, vcomm_t comm, cudaStream_t stream);
 
-/* recvbuffs[r][0..count) = sendbuffs[root][0..count) for every r; root in [0, nRanks).
+/* Broadcast ("AI Systems Performance Engineering (3)", collective table, broadcast row:
+ * the root's buffer copied to every rank):
+ * recvbuffs[r][0..count) = sendbuffs[root][0..count) for every r; root in [0, nRanks).
  * Only sendbuffs[root] is read; the other entries may be NULL.  op is ignored. */
 vResult_t vBroadcast(const void* const* sendbuffs, void* const* recvbuffs, size_t count,
                      vDataType_t datatype, vRedOp_t op, int root, vcomm_t comm,
                      cudaStream_t stream);
 
-/* Uniform all-to-all: count elements per block, nRanks blocks per buffer;
+/* Uniform all-to-all ("AI Systems Performance Engineering (3)", collective table,
+ * all-to-all row: rank i's block j goes to rank j as its block i): count elements per
+ * block, nRanks blocks per buffer;
  * recvbuffs[j][i * count + t] = sendbuffs[i][j * count + t].  op is ignored.
  * Send and receive buffers must not overlap. */
 vResult_t vAllToAll(const void* const* sendbuffs, void* const* recvbuffs, size_t count,

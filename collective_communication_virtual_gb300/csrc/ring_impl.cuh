@@ -109,9 +109,10 @@ __device__ __forceinline__ void st_fifo16(void* p, uint4 v) {
 // Drop a consumed 128-byte FIFO line from L2 without writing it back to DRAM (its data is
 // dead until the producer rewrites it; PTX treats the discard as a weak write of an
 // indeterminate value, which the fence before the head word orders before that rewrite).
-// Only Simple slots are discarded: their validity lives in the tail counters, while a flag
-// protocol could find an old flag of the same value in the stale DRAM copy the discard
-// exposes (an LL epoch byte that wrapped, or a captured graph replaying its fixed epoch).
+// Simple slots are discarded (their validity lives in the tail counters) and LL128 slots of
+// eager launches; a flag protocol must not discard where the stale DRAM copy the discard
+// exposes could hold an old flag of the same value (an LL epoch byte that wrapped, or a
+// captured graph replaying its fixed epoch).
 __device__ __forceinline__ void discard_l2_line(const void* p) {
     asm volatile("discard.global.L2 [%0], 128;" :: "l"(p) : "memory");
 }
@@ -472,12 +473,17 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
         const unsigned int perIter = (T >> 5) * 4;       // lines the CTA covers per step
         const unsigned long long rflag = a.epochHi | (c.recvSeq + 1ull);
         const unsigned long long sflag = a.epochHi | (c.sendSeq + 1ull);
+        // Eager launches carry a 32-bit epoch no other launch used, so no stale copy of a
+        // line in DRAM can hold a flag this launch waits for, and consumed lines may be
+        // dropped from L2; captured graphs (and the no-alloc path) replay epoch 1 and keep them.
+        const bool discardLL128 = a.epochHi != (1ull << 32);
         // The lines of this warp: warp * 4 + j * perIter + (0..3) for j = 0, 1, ...; the q-th
         // of them (q = 4 j + i) is line warp * 4 + (q / 4) * perIter + q % 4.
         const unsigned int mine = lines > warp * 4 ? (lines - warp * 4 + perIter - 1) / perIter * 4 : 0;
         if (kind & kRecv) {
             // Their flags, polled by all 32 lanes, four per lane per round (128 flags in
-            // flight per warp); a flag not yet set is waited for on its own.
+            // flight per warp; eight per lane would spill the data pass's registers); a flag
+            // not yet set is waited for on its own.
             for (unsigned int q0 = lane; q0 < mine && !fail; q0 += 128) {
                 unsigned long long f[4];
 #pragma unroll
@@ -551,6 +557,13 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                                 st_user16(out + halfBase + 8 * (Lb + k * perIter) + 16 * g, make_uint4(a0, a1, b0, b1));
                         }
                         if (kind & kSend) st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
+                    }
+                    if ((kind & kRecv) && discardLL128) {
+                        // the step's R x 4 lines of the warp, read by every lane: dropped
+                        // from L2 (one lane per line) once all have used them
+                        __syncwarp();
+                        if (lane < 4u * R)
+                            discard_l2_line(rs + (size_t)(Lb + (lane >> 2) * perIter + (lane & 3u)) * 128);
                     }
                 } else {
                     ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi);

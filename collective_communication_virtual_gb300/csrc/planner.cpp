@@ -279,9 +279,22 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
                 const bool fanoutCopy = q->coll == vCollAllGather || q->coll == vCollBroadcast;
                 size_t tile = (size_t)64 * 1024;
                 auto tiles = [&](size_t t) { return div_up(chElems * esz, t) * blocks * (size_t)q->nChannels; };
+                // Copies that 16-byte vectors cannot cover (ragged blocks, pointers off 16
+                // bytes) take 32 KiB tiles: half the 64 KiB of a large vector copy (twice the
+                // CTAs for loops that keep fewer bytes in flight per thread), twice the 16 KiB
+                // the fan-out rule gives 2-byte all-gathers (half as many element heads,
+                // tails and realignment set-ups per byte).  Measured on GB300 at
+                // 64 MiB per rank with ragged blocks: bf16 all-gather 0.64 -> 0.77 (3 ranks)
+                // and 0.76 -> 0.85 (8 ranks), fp32 all-to-all 0.88 -> 0.97 and 0.93 -> 1.01;
+                // the fp32 all-gather (8 ranks) fell from 0.94 to 0.88, so 4-byte fan-out
+                // copies keep the vector rule.
                 if (!q->persistentGrid) {
-                    while (tile > 16 * 1024 && tiles(tile) < (size_t)8 * smCount) tile /= 2;
-                    while (fanoutCopy && tile > 8 * 1024 && tiles(tile) < (size_t)16 * smCount) tile /= 2;
+                    if (vec || (fanoutCopy && esz == 4)) {
+                        while (tile > 16 * 1024 && tiles(tile) < (size_t)8 * smCount) tile /= 2;
+                        while (fanoutCopy && tile > 8 * 1024 && tiles(tile) < (size_t)16 * smCount) tile /= 2;
+                    } else {
+                        tile = (size_t)32 * 1024;
+                    }
                     while (tile > 2 * 1024 && tiles(tile) < (size_t)smCount) tile /= 2;
                 }
                 p->tileBytes = tile;

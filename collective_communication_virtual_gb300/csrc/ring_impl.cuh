@@ -19,11 +19,13 @@
 //    CTA barrier and a fence, the consumer returns it by another counter ("head");
 //  * LL: every 8-byte word is {4 data bytes, 4-byte flag}, written and read as one
 //    single-copy-atomic 64-bit access, so a word is valid exactly when its flag matches;
-//  * LL128: every 128-byte line is 120 data bytes and an 8-byte flag.  A warp stores its
-//    lines' data, synchronizes, fences, then stores the flags; the reader polls the
-//    flags, fences, synchronizes, then loads the data.  (NCCL relies on NVLink's
-//    128-byte atomicity; within one GPU the PTX memory model only orders the flag after
-//    the data through the fence, so the fence is explicit here.)
+//  * LL128: every 128-byte line is 120 data bytes and an 8-byte flag.  NCCL relies on
+//    NVLink delivering a 128-byte line at once, so a reader that sees a line's flag sees
+//    its data; within one GPU the PTX memory model orders a flag after data only through
+//    a fence.  So a warp stores its lines with their flags (the first line's flag as
+//    zero), synchronizes, fences and then sets the first line's flag: the release flag.
+//    The reader polls that one flag, fences and synchronizes, then loads the lines and
+//    checks their flags as it reads them.
 //  Simple counters are 64-bit (launch epoch << 32 | slot count) so values from earlier
 //  launches always compare lower; LL flags are (epoch & 0xFF) << 24 | slot count and the
 //  host clears the FIFOs whenever that byte wraps.
@@ -218,6 +220,13 @@ static __device__ __noinline__ bool wait_failed(const RingArgs& a, int ch, int r
     return false;
 }
 
+// A flag-protocol invariant failed (a line flag that does not match after its warp's
+// release flag did): record it and raise the device abort word.
+static __device__ __noinline__ void protocol_failed(const RingArgs& a, int ch, int r, unsigned int seq) {
+    report_error(a.status, a.statusHost, vInternalError, ch, r, seq);
+    atomicExch(a.abortDev, 1u);
+}
+
 // Checked every 64 polls: an abort raised by the host or another CTA, or this wait's
 // deadline.  Returns 0 to keep waiting, 1 aborted, 2 timed out.
 __device__ __forceinline__ int wait_check(const RingArgs& a, unsigned long long t0) {
@@ -307,11 +316,14 @@ template <int PROTO, int ESZ> struct RingUnroll {
 
 // The general step of an LL128 slot (out of line, so the common whole-line steps keep their
 // registers): bounds per lane, element accesses at ragged ends, the epilogue; lane 7 moves
-// its 8 data bytes alone.  Lines Lb + g + k * perIter, as in ring_slot.
+// its 8 data bytes alone, with the line's flag.  Lines Lb + g + k * perIter, as in
+// ring_slot.  rseq / sseq: the sequence halves of the received and sent flags.  Returns
+// whether a received line's flag did not match (checked where lane 7's place holds payload;
+// the release flag has already ordered every line).
 template <int DT, int OUT, int kind, int R>
-__device__ __noinline__ void ll128_step_general(const RingArgs& a, const char* rs, char* ss, const char* in,
+__device__ __noinline__ bool ll128_step_general(const RingArgs& a, const char* rs, char* ss, const char* in,
                                                 char* out, unsigned int Lb, unsigned int lines, unsigned int P,
-                                                bool epi) {
+                                                bool epi, unsigned int rseq, unsigned int sseq, unsigned int L0) {
     constexpr int ESZ = DTypeOf<DT>::size;
     constexpr int OSZ = DTypeOf<OUT>::size;
     const bool aligned = a.aligned != 0;
@@ -319,6 +331,7 @@ __device__ __noinline__ void ll128_step_general(const RingArgs& a, const char* r
     const unsigned int lane = threadIdx.x & 31, g = lane >> 3, t = lane & 7;
     const unsigned int perIter = (blockDim.x >> 5) * 4;
     const unsigned int halfBase = 112 * lines;
+    bool bad = false;
     uint4 v[R], l[R];
 #pragma unroll
     for (int k = 0; k < R; k++) {
@@ -326,8 +339,10 @@ __device__ __noinline__ void ll128_step_general(const RingArgs& a, const char* r
         const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;   // payload byte
         v[k] = make_uint4(0u, 0u, 0u, 0u);
         l[k] = v[k];
+        // lane 7 reads its 8-byte place with the line's flag whether or not the place holds
+        // payload
+        if ((kind & kRecv) && L < lines && b < P) v[k] = ld_fifo16(rs + (size_t)L * 128 + 16 * t);
         if (L < lines && b < P) {
-            if (kind & kRecv) v[k] = ld_fifo16(rs + (size_t)L * 128 + 16 * t);
             if (kind & kLocal) {
                 const int ne = (int)(min(t < 7 ? 16u : 8u, P - b) / ESZ);
                 l[k] = t < 7 ? load_unit<ESZ, 16, 16>(in + b, ne, aligned)
@@ -340,6 +355,8 @@ __device__ __noinline__ void ll128_step_general(const RingArgs& a, const char* r
         const unsigned int L = Lb + g + k * perIter;
         const unsigned int b = t < 7 ? 112 * L + 16 * t : halfBase + 8 * L;
         if (L >= lines) break;
+        if ((kind & kRecv) && t == 7 && b < P)     // the line's flag, in lane 7's place
+            bad |= ((v[k].z ^ rseq) | (v[k].w ^ (unsigned int)(a.epochHi >> 32))) != 0u;
         uint4 x = v[k];
         if (b < P) {
             if (kind & kLocal) x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, l[k]) : l[k];
@@ -351,10 +368,16 @@ __device__ __noinline__ void ll128_step_general(const RingArgs& a, const char* r
             }
         }
         if (kind & kSend) {
-            if (t < 7) st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
-            else st_fifo8(ss + (size_t)L * 128 + 112, make_uint2(x.x, x.y));
+            if (t < 7) {
+                st_fifo16(ss + (size_t)L * 128 + 16 * t, x);
+            } else {
+                const bool rel = L == L0;     // the release flag follows the fence
+                st_fifo16(ss + (size_t)L * 128 + 112,
+                          make_uint4(x.x, x.y, rel ? 0u : sseq, rel ? 0u : (unsigned int)(a.epochHi >> 32)));
+            }
         }
     }
+    return bad;
 }
 
 // One slot of m elements (a slot is at most 16 MiB, so 32-bit offsets).  `in`: user input
@@ -480,27 +503,15 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
         // The lines of this warp: warp * 4 + j * perIter + (0..3) for j = 0, 1, ...; the q-th
         // of them (q = 4 j + i) is line warp * 4 + (q / 4) * perIter + q % 4.
         const unsigned int mine = lines > warp * 4 ? (lines - warp * 4 + perIter - 1) / perIter * 4 : 0;
-        if (kind & kRecv) {
-            // Their flags, polled by all 32 lanes, four per lane per round (128 flags in
-            // flight per warp; eight per lane would spill the data pass's registers); a flag
-            // not yet set is waited for on its own.
-            for (unsigned int q0 = lane; q0 < mine && !fail; q0 += 128) {
-                unsigned long long f[4];
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const unsigned int q = q0 + k * 32;
-                    const unsigned int L = warp * 4 + (q >> 2) * perIter + (q & 3);
-                    f[k] = (q < mine && L < lines) ? ld_volatile_u64(rs + (size_t)L * 128 + 120) : rflag;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const unsigned int q = q0 + k * 32;
-                    const unsigned int L = warp * 4 + (q >> 2) * perIter + (q & 3);
-                    if (f[k] != rflag && !fail &&
-                        !wait_flag64(a, c.ch, c.r, rs + (size_t)L * 128 + 120, rflag, c.recvSeq))
-                        fail = true;
-                }
-            }
+        // The warp's first line carries its release flag: written as zero with the data,
+        // then, after the warp's data stores, a barrier and a fence, set to the slot's flag.
+        // A reader that sees it set (and fences) sees every line the warp stored, so it
+        // polls that one flag; the other lines' flags are stored with their data and checked
+        // as the data pass reads them.
+        const unsigned int L0 = warp * 4;
+        if ((kind & kRecv) && mine > 0) {
+            const char* fp = rs + (size_t)L0 * 128 + 120;
+            if (ld_volatile_u64(fp) != rflag && !wait_flag64(a, c.ch, c.r, fp, rflag, c.recvSeq)) fail = true;
             fence_acq_rel();
             __syncwarp();
         }
@@ -511,8 +522,9 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                 const bool whole = aligned && !epi && halfBase + 8 * (Lb + (R - 1) * perIter + 4) <= P;
                 if (whole) {
                     // Every line of the step exists and is full: one 16-byte FIFO access per
-                    // lane (lane 7's covers its 8 data bytes and the flag's place, written as
-                    // zero -- never a valid flag -- until the flags follow the fence), one
+                    // lane (lane 7's covers its 8 data bytes and the line's flag; the warp's
+                    // first line gets zero there -- never a valid flag -- until the release
+                    // flag follows the fence), one
                     // 16-byte user access per lane 0..6, and the four 8-byte places of a step
                     // (32 contiguous user bytes) read and written by lane 7 of groups 0 and 1,
                     // 16 bytes each, and shared out with shuffles.
@@ -527,6 +539,13 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                             if (t < 7) l[k] = ld_user16(in + 112 * L + 16 * t);
                             else if (g < 2) l[k] = ld_user16(in + halfBase + 8 * (Lb + k * perIter) + 16 * g);
                         }
+                    }
+                    if (kind & kRecv) {
+                        // the flag's halves: the launch epoch over the slot's sequence number
+                        const unsigned int rlo = c.recvSeq + 1u, hi = (unsigned int)(a.epochHi >> 32);
+#pragma unroll
+                        for (int k = 0; k < R; k++)
+                            if (t == 7) fail |= ((v[k].z ^ rlo) | (v[k].w ^ hi)) != 0u;
                     }
 #pragma unroll
                     for (int k = 0; k < R; k++) {
@@ -543,8 +562,9 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                             x = (kind & kRecv) ? op_vec_rt<DT>(a.op, x, y) : y;
                         }
                         if (t == 7) {
-                            x.z = 0u;
-                            x.w = 0u;
+                            const bool rel = L == L0;     // the release flag follows the fence
+                            x.z = rel ? 0u : c.sendSeq + 1u;
+                            x.w = rel ? 0u : (unsigned int)(a.epochHi >> 32);
                         }
                         if (kind & kOut) {
                             const int lo = 7 + 16 * (g & 1), hi = lo + 8;   // lines 2g and 2g + 1 of the step
@@ -566,18 +586,23 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                             discard_l2_line(rs + (size_t)(Lb + (lane >> 2) * perIter + (lane & 3u)) * 128);
                     }
                 } else {
-                    ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi);
+                    fail |= ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi, c.recvSeq + 1u,
+                                                                 c.sendSeq + 1u, L0);
                 }
                 test_jitter(a, Lb);
             }
-            if (kind & kSend) {
-                // After every lane's data stores: the flags, by all 32 lanes.
+            // In the data pass `fail` marks a line flag that did not match after the release
+            // flag did: a broken protocol invariant, reported, and the ring stops.
+            if ((kind & kRecv) && __any_sync(0xFFFFFFFFu, fail)) {
+                if (lane == 0) protocol_failed(a, c.ch, c.r, c.recvSeq);
+                fail = true;
+            } else if ((kind & kSend) && mine > 0) {
+                // after every lane's data stores: the release flag
                 test_jitter(a, 0x5157u);
                 __syncwarp();
-                fence_acq_rel();
-                for (unsigned int q = lane; q < mine; q += 32) {
-                    const unsigned int L = warp * 4 + (q >> 2) * perIter + (q & 3);
-                    if (L < lines) st_volatile_u64(ss + (size_t)L * 128 + 120, sflag);
+                if (lane == 0) {
+                    fence_acq_rel();
+                    st_volatile_u64(ss + (size_t)L0 * 128 + 120, sflag);
                 }
             }
         }

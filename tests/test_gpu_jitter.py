@@ -1,6 +1,6 @@
 """The staged ring's protocols under skewed timing: with the jitter test hook every thread
 sleeps for pseudo-random times where a producer publishes a slot (Simple: before its
-counter; LL: between 16-byte units; LL128: between lines and before the flags) and where
+counter; LL: between 16-byte units; LL128: between lines and before the release flag) and where
 a consumer starts one.  Consumers then see slots half written, flags ahead of or behind
 their neighbours, and FIFOs full or empty at other moments than usual.  Every result must
 still equal the oracle bit for bit."""

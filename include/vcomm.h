@@ -152,7 +152,11 @@ vResult_t vcommDestroy(vcomm_t comm);
 vResult_t vcommCount(vcomm_t comm, int* nRanks);
 
 /* Store the sticky asynchronous error (vSuccess if none) in *asyncError.  Reads host
- * memory that the kernels write; it does not synchronize any stream. */
+ * memory that the kernels write; it does not synchronize any stream.  A vTimeout is
+ * fatal for the stream it happened on: the outputs of that call are undefined, and after
+ * a timed-out bulk-copy fan-out (VCOMM_COPY_TMA=1) a load that had still not landed when
+ * its CTA gave up may write into shared memory that a later kernel on the GPU uses, so
+ * no later result is to be trusted either. */
 vResult_t vcommGetAsyncError(vcomm_t comm, vResult_t* asyncError);
 
 /* Ask running and future ring transfers of this communicator to stop: their waits

@@ -492,14 +492,32 @@ def e2e_allreduce(torch, V, comm, xs, dev, stream, steps, dist=None, world=1):
         torch.cuda.synchronize()
         return max_over_ranks(start.elapsed_time(stop) / 1e3 / steps, dist, dev)
 
+    # the host link's own ceiling for this traffic: the copy engines moving the same bytes
+    # both ways at once (8 inputs in, 8 results out, on two streams)
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def copies_both_ways():
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        with torch.cuda.stream(up):
+            for d, h in zip(d_in, host_in):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(down):
+            for h, d in zip(host_out, d_out):
+                h.copy_(d, non_blocking=True)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
     t = timed(zero_copy)
     t_copy = timed(explicit)
     consistent = all(torch.equal(host_out[r], d_out[r].cpu()) for r in range(N_RANKS))
+    t_link = timed(copies_both_ways)
     nbytes = N_RANKS * BYTES_PER_RANK
     return {"value": job_busbw(world, t), "unit": "GB/s",
             "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "ms_per_step": t * 1e3,
             "steps": steps, "mode": "zero-copy: vAllReduce on pinned host buffers over NVLink-C2C",
             "explicit_copies": {"value": job_busbw(world, t_copy), "ms_per_step": t_copy * 1e3},
+            "host_link": {"copy_engines_gbs": 2 * nbytes / t_link / 1e9, "frac": t_link / t},
             "results_match_device_path": consistent}
 
 

@@ -97,6 +97,8 @@ struct RingArgs {
     int testStallRank;               // test hook: this rank never posts data (-1 = off)
     unsigned int testJitterNs;       // test hook: random sleeps up to this long where the
                                      // protocols publish or observe a slot (0 = off)
+    int testBadFlagRank;             // test hook: this rank expects wrong LL128 line flags
+                                     // (its release flags are right; -1 = off)
 };
 
 // Double-binary-tree all-reduce.  prog[t] lists tree t's ranks in post-order (children

@@ -157,6 +157,7 @@ extern "C" vResult_t vAllReduceNoAlloc(const void* const* sendbuffs, void* const
     a.statusHost = nullptr;
     a.testStallRank = -1;
     a.testJitterNs = 0;
+    a.testBadFlagRank = -1;
     const cudaError_t e =
         vc::launch_ring(a, datatype, op, datatype, (vProto_t)p.proto, p.gridCtas, p.threadsPerCta, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {

@@ -193,6 +193,13 @@ struct RingCtx {
     unsigned int sendSeq, recvSeq;
 };
 
+// The sequence half of the LL128 line flags a slot receives.  Test hook
+// (RingArgs::testBadFlagRank): that rank expects every line flag off by 2^31, as if its
+// predecessor had stored wrong ones, and must report the mismatch.
+__device__ __forceinline__ unsigned int line_seq(const RingArgs& a, const RingCtx& c) {
+    return c.recvSeq + 1u + (c.r == a.testBadFlagRank ? 0x80000000u : 0u);
+}
+
 // Test hook (RingArgs::testJitterNs): a pseudo-random sleep of up to testJitterNs
 // nanoseconds, different per thread and call, so that tests see other interleavings of
 // data stores, flag stores and flag reads than the usual ones.  Off (one uniform branch)
@@ -542,7 +549,7 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                     }
                     if (kind & kRecv) {
                         // the flag's halves: the launch epoch over the slot's sequence number
-                        const unsigned int rlo = c.recvSeq + 1u, hi = (unsigned int)(a.epochHi >> 32);
+                        const unsigned int rlo = line_seq(a, c), hi = (unsigned int)(a.epochHi >> 32);
 #pragma unroll
                         for (int k = 0; k < R; k++)
                             if (t == 7) fail |= ((v[k].z ^ rlo) | (v[k].w ^ hi)) != 0u;
@@ -586,8 +593,8 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                             discard_l2_line(rs + (size_t)(Lb + (lane >> 2) * perIter + (lane & 3u)) * 128);
                     }
                 } else {
-                    fail |= ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi, c.recvSeq + 1u,
-                                                                 c.sendSeq + 1u, L0);
+                    fail |= ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi,
+                                                                 line_seq(a, c), c.sendSeq + 1u, L0);
                 }
                 test_jitter(a, Lb);
             }

@@ -89,6 +89,7 @@ struct vcomm {
     unsigned int epoch;
     int testStallRank;
     unsigned int testJitterNs;
+    int testBadFlagRank;
     StreamEvent tracked[kTrackedStreams];   // per stream; reused round-robin when full
     unsigned int trackedNext;
     // group batching
@@ -428,6 +429,7 @@ vResult_t launch_ring_plan(vcomm* c, int coll, const void* const* send, void* co
     a.statusHost = c->statusHostDev;
     a.testStallRank = c->testStallRank;
     a.testJitterNs = c->testJitterNs;
+    a.testBadFlagRank = c->testBadFlagRank;
     e = vc::launch_ring(a, dt, op, outType, (vProto_t)p.proto, p.gridCtas, p.threadsPerCta, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();
@@ -566,6 +568,7 @@ vResult_t vcommInit(vcomm_t* comm, int nRanks, int nChannels, vProto_t protocol)
     c->proto = protocol;
     c->device = dev;
     c->testStallRank = -1;
+    c->testBadFlagRank = -1;
     c->hostError = vSuccess;
     c->epoch = 1;                    // eager ring launches use epochs >= 2
     c->group = new (std::nothrow) std::vector<GroupRec>();
@@ -717,6 +720,12 @@ vResult_t vcommSetTimeoutMs(vcomm_t c, int timeoutMs) {
 vResult_t vcommTestSetStallRank(vcomm_t c, int rank) {
     if (!comm_ok(c) || rank < -1 || rank >= c->nRanks) return vInvalidArgument;
     c->testStallRank = rank;
+    return vSuccess;
+}
+
+vResult_t vcommTestSetBadFlagRank(vcomm_t c, int rank) {
+    if (!comm_ok(c) || rank < -1 || rank >= c->nRanks) return vInvalidArgument;
+    c->testBadFlagRank = rank;
     return vSuccess;
 }
 

@@ -99,6 +99,7 @@ _SIGNATURES = {
                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vcommCount": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vcommTestSetJitterNs": ([ctypes.c_void_p, ctypes.c_uint], ctypes.c_int),
+    "vcommTestSetBadFlagRank": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
     "vAllToAllv": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "vReduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -271,6 +272,10 @@ def vcommSetTimeoutMs(comm, ms: int) -> None:
 
 def vcommTestSetStallRank(comm, rank: int) -> None:
     _check(lib().vcommTestSetStallRank(comm, rank), "vcommTestSetStallRank")
+
+
+def vcommTestSetBadFlagRank(comm, rank: int) -> None:
+    _check(lib().vcommTestSetBadFlagRank(comm, rank), "vcommTestSetBadFlagRank")
 
 
 def vcommTestSetJitterNs(comm, max_ns: int) -> None:

@@ -389,6 +389,13 @@ vResult_t vPlanChannelRange(const vPlanInfo_t* plan, size_t count, int channel, 
  * transfer ends with the sticky error vTimeout.  -1 turns the hook off. */
 vResult_t vcommTestSetStallRank(vcomm_t comm, int rank);
 
+/* Test hook for the LL128 line check: in every later LL128 ring transfer rank `rank`
+ * expects wrong line flags (as if its predecessor had stored wrong ones; the per-warp
+ * release flags it polls stay right), so it finds a line whose flag does not match after
+ * the release flag did and ends the transfer with the sticky error vInternalError.  -1
+ * turns the hook off. */
+vResult_t vcommTestSetBadFlagRank(vcomm_t comm, int rank);
+
 /* Test hook: staged ring transfers sleep for pseudo-random times of up to maxNs
  * nanoseconds (0 = off, at most 1,000,000) where a producer publishes a slot and where a
  * consumer observes one, so that tests exercise orderings of stores and flag reads that

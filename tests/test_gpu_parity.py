@@ -483,6 +483,40 @@ def test_stalled_rank_times_out_flag_protocols(proto):
         V.vcommDestroy(c)
 
 
+@pytest.mark.parametrize("count", [1 << 14, 1 << 18], ids=["64KiB", "1MiB"])
+def test_ll128_line_flag_mismatch_is_reported(count):
+    # An LL128 reader polls one release flag per warp, then checks every line flag it
+    # reads.  A rank that expects wrong line flags must stop the transfer with
+    # vInternalError, in bounded time and without a fault; with the hook off again the
+    # lines pass their check.  64 KiB per rank: ragged steps (lane 7 checks lines whose
+    # 8-byte place holds payload); 1 MiB: whole-line steps.
+    n = 4
+    x = [torch.ones(count, device=DEV) for _ in range(n)]
+    c = V.vcommInit(n, 1, V.vProtoLL128)
+    try:
+        V.vcommSetAlgo(c, "ring")
+        V.vcommSetTimeoutMs(c, 200)
+        V.vcommTestSetBadFlagRank(c, 2)
+        t0 = time.time()
+        V.vAllReduce(x, [torch.empty_like(t) for t in x], count, torch.float32, "sum", c)
+        torch.cuda.synchronize()
+        assert time.time() - t0 < 20
+        assert V.vcommGetAsyncError(c) == V.vInternalError
+    finally:
+        V.vcommDestroy(c)
+    c = V.vcommInit(n, 1, V.vProtoLL128)
+    try:
+        V.vcommSetAlgo(c, "ring")
+        V.vcommTestSetBadFlagRank(c, 2)
+        V.vcommTestSetBadFlagRank(c, -1)
+        y = [torch.empty_like(t) for t in x]
+        V.vAllReduce(x, y, count, torch.float32, "sum", c)
+        _sync_ok(c)
+        assert all(torch.equal(t, torch.full_like(t, 4.0)) for t in y)
+    finally:
+        V.vcommDestroy(c)
+
+
 def test_abort_stops_a_waiting_transfer():
     c = V.vcommInit(4, 1, V.vProtoSimple)
     try:

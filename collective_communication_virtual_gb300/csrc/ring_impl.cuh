@@ -242,12 +242,19 @@ __device__ __forceinline__ int wait_check(const RingArgs& a, unsigned long long 
     return 0;
 }
 
-// Spin until *p >= target (monotonic 64-bit counters), then fence.  Bounded.
+// Spin until *p >= target (monotonic 64-bit counters), then fence; the value seen goes to
+// *seen.  Bounded.
 static __device__ __noinline__ bool wait_counter(const RingArgs& a, int ch, int r, const unsigned long long* p,
-                                                 unsigned long long target, unsigned int seq) {
+                                                 unsigned long long target, unsigned int seq,
+                                                 unsigned long long* seen) {
     const unsigned long long t0 = global_timer_ns();
     for (unsigned int it = 0;; it++) {
-        if (ld_volatile_u64(p) >= target) { fence_acq_rel(); return true; }
+        const unsigned long long v = ld_volatile_u64(p);
+        if (v >= target) {
+            fence_acq_rel();
+            *seen = v;
+            return true;
+        }
         if ((it & 63u) == 63u) {
             const int why = wait_check(a, t0);
             if (why) return wait_failed(a, ch, r, seq, why == 2);
@@ -286,6 +293,15 @@ static __device__ __noinline__ bool wait_ll_slow(const RingArgs& a, int ch, int 
     }
 }
 
+// The counter values thread 0 has seen in this launch: [0] the tail of its own FIFO, [1]
+// the head of the next rank's.  Both only grow within a launch, so a slot or a credit
+// already covered by a value seen (and fenced after) needs no load: the producer often
+// runs several slots ahead, and one head value grants up to kFifoSlots sends.
+__device__ __forceinline__ unsigned long long* seen_counters() {
+    __shared__ unsigned long long seen[2];
+    return seen;
+}
+
 // Thread 0 takes the slot credit (and, for Simple, waits for the slot's data); the CTA
 // then agrees on success.
 template <int PROTO, int kind>
@@ -293,10 +309,15 @@ __device__ __forceinline__ bool slot_begin(const RingArgs& a, const RingCtx& c) 
     test_jitter(a, c.recvSeq * 3u + c.sendSeq);
     bool fail = false;
     if (threadIdx.x == 0) {
-        if (PROTO == vProtoSimple && (kind & kRecv))
-            fail = !wait_counter(a, c.ch, c.r, c.myTail, a.epochHi | (c.recvSeq + 1ull), c.recvSeq);
-        if (!fail && (kind & kSend) && c.sendSeq >= (unsigned)kFifoSlots)
-            fail = !wait_counter(a, c.ch, c.r, c.nextHead, a.epochHi | (c.sendSeq - kFifoSlots + 1ull), c.sendSeq);
+        unsigned long long* seen = seen_counters();
+        if (PROTO == vProtoSimple && (kind & kRecv)) {
+            const unsigned long long want = a.epochHi | (c.recvSeq + 1ull);
+            if (seen[0] < want) fail = !wait_counter(a, c.ch, c.r, c.myTail, want, c.recvSeq, &seen[0]);
+        }
+        if (!fail && (kind & kSend) && c.sendSeq >= (unsigned)kFifoSlots) {
+            const unsigned long long want = a.epochHi | (c.sendSeq - kFifoSlots + 1ull);
+            if (seen[1] < want) fail = !wait_counter(a, c.ch, c.r, c.nextHead, want, c.sendSeq, &seen[1]);
+        }
     }
     return !__syncthreads_or(fail);
 }
@@ -667,6 +688,10 @@ __global__ void __launch_bounds__(kRingThreads, 2) k_ring(const __grid_constant_
     c.nextTail = c.nextHead + 16;
     c.sendSeq = 0;
     c.recvSeq = 0;
+    if (threadIdx.x == 0) {                         // only thread 0 reads them
+        seen_counters()[0] = 0ull;
+        seen_counters()[1] = 0ull;
+    }
 
     const char* mySend = (const char*)a.send[r];
     char* myRecv = (char*)a.recv[r];

@@ -94,7 +94,7 @@ typedef enum { vSum = 0, vProd = 1, vMin = 2, vMax = 3 } vRedOp_t;
  * collective, size and channel count (a ring cost model in the form of the NCCL book's
  * ring.cc, latency + bytes / bandwidth per protocol and channel count, fitted to staged-ring
  * times measured on GB300 for every collective, protocol and size from 1 KiB to 1 GiB per
- * rank: 3.3 % median error, and a pick within 15 % of the fastest protocol measured). */
+ * rank: 3.0 % median error, and a pick within 15 % of the fastest protocol measured). */
 typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 } vProto_t;
 
 /* Algorithms.  vAlgoOnePass: one kernel reads every rank's buffer once and writes
@@ -103,7 +103,7 @@ typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 }
  * section 2.3, N-1 reduce-scatter steps then N-1 all-gather steps, each hop staged
  * through a device FIFO with the communicator's protocol.  Both give identical bits.
  * vAlgoAuto picks the smaller predicted time (on GB300 the one-pass kernels are faster
- * at every size: about 2 us of latency against 8-52 us for the ring's steps).
+ * at every size: about 2 us of latency against 8-55 us for the ring's steps).
  * vAlgoTree (all-reduce only; other collectives run one-pass): the double binary tree of
  * the NCCL book chapter 4 (ncclGetBtree / ncclGetDtree).  The first half of the buffer,
  * up to alignUp(ceil(count / 2), 16 / elemSize) elements, is reduced up tree 0, the rest

@@ -120,16 +120,16 @@ def test_auto_protocol_follows_the_fitted_ring_model():
 
 def test_model_evaluates_its_fitted_constants():
     # fp32 all-reduce, 8 ranks: one-pass 1.5 us + minimum bytes / 7.097e6 B/us; the staged
-    # ring with Simple at 32 channels: 39.78 us + max(0, bytes per rank - 1 KiB) / 159585.9
-    # B/us, at 1 channel 40.98 us + max(0, bytes - 2 KiB) / 8277.4 B/us
+    # ring with Simple at 32 channels: 36.54 us + max(0, bytes per rank - 1 KiB) / 160010.9
+    # B/us, at 1 channel 36.87 us + bytes / 8738.0 B/us (knee 0)
     big = 256 << 20
     assert plan(count=256).predictedUs == pytest.approx(1.5 + 16 * 1024 / 7.097e6, rel=0.001)
     assert plan(count=64 << 20).predictedUs == pytest.approx(1.5 + 16 * big / 7.097e6, rel=0.001)
-    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(39.78, rel=1e-4)
+    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(36.54, rel=1e-4)
     assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=32).predictedUs == \
-        pytest.approx(39.78 + (big - 1024) / 159585.9, rel=1e-4)
+        pytest.approx(36.54 + (big - 1024) / 160010.9, rel=1e-4)
     assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=1).predictedUs == \
-        pytest.approx(40.98 + (big - 2048) / 8277.4, rel=1e-4)
+        pytest.approx(36.87 + big / 8738.0, rel=1e-4)
 
 
 def test_auto_algorithm_picks_the_one_pass_kernels():

@@ -1,15 +1,16 @@
 """Refit the planner's ring cost model from measured staged-ring times.
 
 The planner predicts a staged-ring collective of x bytes per rank over N ranks as
-  ring steps (all-reduce, reduce-scatter, all-gather):  lat + max(0, x - knee) / rate
+  ring steps (all-reduce, reduce-scatter, all-gather):  lat + f * min(x, knee) + max(0, x - knee) / rate
   broadcast chain:                                       lat + c * sqrt(x) + x / rate
 for each (collective, protocol) at 1, 8 and 32 channels (interpolated in log2 of the
 channel count, held flat beyond), with lat and the byte terms scaled from N = 8 by the
 step count (the ring.cc form of the NCCL book, chapter 5: time = latency + bus bytes /
-bus bandwidth, with LL and LL128 trading bandwidth for latency).  The knee is the payload
-that the pipeline's first round carries at no extra cost; the broadcast's square-root
-term is the pipeline fill of a chain whose slot count grows as sqrt(bytes) (the planner's
-broadcast slot rule).
+bus bandwidth, with LL and LL128 trading bandwidth for latency).  Below the knee a
+transfer is one slot per step and every step pays for its bytes in turn (f, microseconds
+per byte); above it the slots pipeline and the bytes cost 1 / rate; the broadcast's
+square-root term is the pipeline fill of a chain whose slot count grows as sqrt(bytes)
+(the planner's broadcast slot rule).
 
 Input: the `ring_sweep` rows that `bench.py --ring-sweep` prints (device time of fp32 sum
 over 8 ranks, default chunks, 1 KiB .. 1 GiB per rank in powers of 4), committed as
@@ -48,25 +49,30 @@ def _lsq(cols, m):
 
 
 def fit_curve(coll, x, m):
-    """(lat_us, bytes_per_us, third) for one (collective, protocol, channels) curve; third
-    is the knee in bytes (ring steps) or the square-root coefficient (broadcast)."""
+    """(lat_us, bytes_per_us, third, us_per_mib_below_knee) for one (collective, protocol,
+    channels) curve; third is the knee in bytes (ring steps) or the square-root coefficient
+    (broadcast, whose last value is 0)."""
     x, m = np.asarray(x, float), np.asarray(m, float)
     one = np.ones_like(x)
     if coll == "broadcast":
         lat, c, inv = _lsq([one, np.sqrt(x), x], m)
         if c < 0 or inv <= 0:
             (lat, inv), c = _lsq([one, x], m), 0.0
-        return float(lat), float(1.0 / inv), float(c)
+        return float(lat), float(1.0 / inv), float(c), 0.0
     best = None
-    for knee in [0.0] + [float(2 ** k) for k in range(10, 26)]:
-        xe = np.maximum(0.0, x - knee)
-        lat, inv = _lsq([one, xe], m)
+    for knee in [0.0] + [float(2 ** k) for k in range(10, 27)]:
+        below, above = np.minimum(x, knee), np.maximum(0.0, x - knee)
+        f = -1.0
+        if knee > 0:
+            lat, f, inv = _lsq([one, below, above], m)
+        if f < 0:                      # no knee, or a negative slope below it: none
+            (lat, inv), f = _lsq([one, above], m), 0.0
         if lat < 0 or inv <= 0:
             continue
-        score = float(np.sum(((lat + inv * xe) / m - 1.0) ** 2))
+        score = float(np.sum(((lat + f * below + inv * above) / m - 1.0) ** 2))
         if best is None or score < best[0]:
-            best = (score, float(lat), float(1.0 / inv), knee)
-    return best[1], best[2], best[3]
+            best = (score, float(lat), float(1.0 / inv), knee, float(f) * (1 << 20))
+    return best[1], best[2], best[3], best[4]
 
 
 def fit(rows):
@@ -90,7 +96,8 @@ def cpp(table):
             lat = ", ".join(f"{v[0]:.2f}" for v in f)
             rate = ", ".join(f"{v[1]:.1f}" for v in f)
             third = ", ".join((f"{v[2]:.0f}" if coll != "broadcast" else f"{v[2]:.5f}") for v in f)
-            out.append(f"        {{{{{lat}}}, {{{rate}}}, {{{third}}}}},   // {proto}")
+            below = ", ".join(f"{v[3]:.2f}" for v in f)
+            out.append(f"        {{{{{lat}}}, {{{rate}}}, {{{third}}}, {{{below}}}}},   // {proto}")
         out.append("    },")
     out.append("};")
     return "\n".join(out)
@@ -102,9 +109,12 @@ def main() -> None:
     print(cpp(table))
     errs = []
     for r in rows:
-        lat, rate, third = table[(r["coll"], r["proto"])][CHANNELS.index(r["channels"])]
+        lat, rate, third, below = table[(r["coll"], r["proto"])][CHANNELS.index(r["channels"])]
         x = r["bytes_per_rank"]
-        pred = lat + (third * math.sqrt(x) + x / rate if r["coll"] == "broadcast" else max(0.0, x - third) / rate)
+        if r["coll"] == "broadcast":
+            pred = lat + third * math.sqrt(x) + x / rate
+        else:
+            pred = lat + below / (1 << 20) * min(x, third) + max(0.0, x - third) / rate
         errs.append(abs(pred / r["device_us"] - 1.0))
     print(f"// median relative error {float(np.median(errs)):.3f}, max {max(errs):.3f} over {len(errs)} points")
 

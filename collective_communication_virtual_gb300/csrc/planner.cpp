@@ -48,8 +48,10 @@ size_t pow2_floor(size_t x) {
 // (collective_communication_virtual_gb300/calibrate.py, from the staged-ring times in
 // ring_timings_gb300.json: fp32 sum over 8 ranks, default chunks, 1 KiB .. 1 GiB per rank)
 // with one more term each, which the data ask for:
-//  * ring steps (all-reduce, reduce-scatter, all-gather): lat + max(0, x - knee) / rate --
-//    the first round of the pipeline carries up to `knee` bytes at no extra cost;
+//  * ring steps (all-reduce, reduce-scatter, all-gather):
+//    lat + f min(x, knee) + max(0, x - knee) / rate -- below the knee a transfer is one
+//    slot per step and its bytes cost f each, in turn at every step; above it the slots
+//    pipeline and a byte costs 1 / rate;
 //  * broadcast (a chain): lat + c sqrt(x) + x / rate -- the pipeline fill of a chain whose
 //    slot count grows as sqrt(x) (the broadcast slot rule below).
 // x is bytes per rank at 8 ranks; for N ranks the latency scales by nSteps, the ring
@@ -60,30 +62,31 @@ struct RingFit {
     double latUs[3];           // at 1, 8, 32 channels
     double bytesPerUs[3];      // bytes per rank per microsecond, at 8 ranks
     double shape[3];           // ring steps: knee (bytes per rank); broadcast: sqrt coefficient
+    double usPerMiBBelow[3];   // ring steps: microseconds per MiB below the knee
 };
 const RingFit kRingFit[4][3] = {                         // calibrate.py prints these
     {  // allreduce
-        {{36.87, 36.59, 36.54}, {8738.0, 66742.2, 160010.9}, {0, 1024, 1024}},   // simple
-        {{26.02, 23.61, 24.76}, {4263.3, 28458.5, 77213.9}, {32768, 131072, 524288}},   // ll
-        {{54.60, 49.75, 50.97}, {6138.6, 47101.3, 127067.4}, {131072, 1024, 1024}},   // ll128
+        {{32.78, 34.64, 36.88}, {8645.7, 67998.5, 136493.1}, {524288, 262144, 67108864}, {94.19, 38.18, 5.87}},   // simple
+        {{25.10, 23.29, 23.91}, {4334.9, 27992.4, 76631.0}, {524288, 524288, 2097152}, {145.06, 17.36, 9.21}},   // ll
+        {{52.89, 50.81, 52.55}, {8766.1, 65218.3, 134180.0}, {2097152, 16777216, 67108864}, {85.25, 13.40, 6.00}},   // ll128
     },
     {  // reduce_scatter
-        {{23.98, 21.51, 20.11}, {13845.9, 95973.5, 278331.1}, {131072, 2097152, 262144}},   // simple
-        {{17.26, 13.63, 14.16}, {6745.0, 45443.1, 138365.1}, {131072, 131072, 65536}},   // ll
-        {{32.02, 27.90, 29.20}, {9171.1, 69533.2, 208501.3}, {131072, 1024, 1024}},   // ll128
+        {{19.07, 20.07, 19.78}, {12499.0, 97454.3, 240898.1}, {4194304, 4194304, 67108864}, {50.13, 6.81, 3.34}},   // simple
+        {{15.20, 13.40, 13.82}, {6096.0, 45305.2, 136545.6}, {2097152, 131072, 16777216}, {98.03, 0.00, 7.34}},   // ll
+        {{31.41, 28.93, 28.64}, {15038.4, 115527.7, 312633.3}, {2097152, 16777216, 2097152}, {44.38, 7.69, 9.43}},   // ll128
     },
     {  // allgather
-        {{20.51, 18.52, 19.13}, {23104.2, 176350.9, 315569.8}, {4096, 131072, 2097152}},   // simple
-        {{16.51, 13.64, 14.51}, {9935.3, 66326.7, 161461.2}, {32768, 131072, 262144}},   // ll
-        {{28.38, 25.19, 26.16}, {17371.6, 129399.4, 282636.7}, {32768, 0, 0}},   // ll128
+        {{18.31, 18.34, 18.25}, {23649.7, 171135.6, 288958.2}, {524288, 8388608, 67108864}, {33.08, 5.15, 2.80}},   // simple
+        {{16.24, 12.94, 14.08}, {12006.0, 61903.8, 162660.8}, {65536, 16777216, 262144}, {32.94, 14.07, 1.37}},   // ll
+        {{27.45, 25.14, 26.20}, {18657.9, 134711.5, 256851.9}, {4194304, 16777216, 67108864}, {46.17, 6.69, 3.35}},   // ll128
     },
     {  // broadcast
-        {{17.20, 14.73, 15.54}, {22689.7, 178903.6, 359983.7}, {0.04178, 0.01344, 0.00802}},   // simple
-        {{10.40, 8.05, 8.11}, {10151.2, 64743.1, 118170.0}, {0.00581, 0.00525, 0.00730}},   // ll
-        {{20.78, 19.68, 19.96}, {16448.3, 131503.1, 360875.7}, {0.04478, 0.01819, 0.01702}},   // ll128
+        {{15.26, 14.93, 15.57}, {23417.9, 177952.6, 353129.7}, {0.04029, 0.01383, 0.00713}, {0.00, 0.00, 0.00}},   // simple
+        {{10.51, 7.78, 8.03}, {10609.6, 64002.3, 116232.2}, {0.00000, 0.00566, 0.00711}, {0.00, 0.00, 0.00}},   // ll
+        {{19.99, 19.25, 19.89}, {19703.6, 159264.7, 368990.6}, {0.04487, 0.01849, 0.01648}, {0.00, 0.00, 0.00}},   // ll128
     },
 };
-// median relative error 0.030, max 0.233 over 396 points
+// median relative error 0.022, max 0.241 over 396 points
 const double kOnePassLatUs = 1.5;
 const double kOnePassBytesPerUs = 7.097e6;                   // minimum bytes / (time - latency)
 
@@ -111,7 +114,8 @@ double predict_ring_us(int proto, int coll, int N, int nCh, double bytesPerRank)
     if (coll == vCollBroadcast)
         return lat + shape * std::sqrt(bytesPerRank * std::max(0, N - 2) / 6.0) + bytesPerRank / rate;
     const double scale = ((double)n_steps(coll, N) / N) / ((double)n_steps(coll, 8) / 8.0);
-    return lat + std::max(0.0, bytesPerRank * scale - shape) / rate;
+    const double x = bytesPerRank * scale, below = interp_ch(f.usPerMiBBelow, nCh) / (1 << 20);
+    return lat + below * std::min(x, shape) + std::max(0.0, x - shape) / rate;
 }
 
 double predict_onepass_us(double minBytes) { return kOnePassLatUs + minBytes / kOnePassBytesPerUs; }

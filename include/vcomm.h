@@ -94,7 +94,7 @@ typedef enum { vSum = 0, vProd = 1, vMin = 2, vMax = 3 } vRedOp_t;
  * collective, size and channel count (a ring cost model in the form of the NCCL book's
  * ring.cc, latency + bytes / bandwidth per protocol and channel count, fitted to staged-ring
  * times measured on GB300 for every collective, protocol and size from 1 KiB to 1 GiB per
- * rank: 3.0 % median error, and a pick within 15 % of the fastest protocol measured). */
+ * rank: 2.2 % median error, and a pick within 15 % of the fastest protocol measured). */
 typedef enum { vProtoSimple = 0, vProtoLL = 1, vProtoLL128 = 2, vProtoAuto = 3 } vProto_t;
 
 /* Algorithms.  vAlgoOnePass: one kernel reads every rank's buffer once and writes

@@ -120,16 +120,19 @@ def test_auto_protocol_follows_the_fitted_ring_model():
 
 def test_model_evaluates_its_fitted_constants():
     # fp32 all-reduce, 8 ranks: one-pass 1.5 us + minimum bytes / 7.097e6 B/us; the staged
-    # ring with Simple at 32 channels: 36.54 us + max(0, bytes per rank - 1 KiB) / 160010.9
-    # B/us, at 1 channel 36.87 us + bytes / 8738.0 B/us (knee 0)
-    big = 256 << 20
+    # ring with Simple at 32 channels: 36.88 us + 5.87 us per MiB up to the 64 MiB knee +
+    # the rest / 136493.1 B/us; at 1 channel 32.78 us + 94.19 us per MiB up to 512 KiB +
+    # the rest / 8645.7 B/us
+    mib = 1 << 20
+    big = 256 * mib
     assert plan(count=256).predictedUs == pytest.approx(1.5 + 16 * 1024 / 7.097e6, rel=0.001)
     assert plan(count=64 << 20).predictedUs == pytest.approx(1.5 + 16 * big / 7.097e6, rel=0.001)
-    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == pytest.approx(36.54, rel=1e-4)
+    assert plan(algo=V.vAlgoRing, count=256, nChannels=32).predictedUs == \
+        pytest.approx(36.88 + 5.87 * 1024 / mib, rel=1e-4)
     assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=32).predictedUs == \
-        pytest.approx(36.54 + (big - 1024) / 160010.9, rel=1e-4)
+        pytest.approx(36.88 + 5.87 * 64 + (big - 64 * mib) / 136493.1, rel=1e-4)
     assert plan(algo=V.vAlgoRing, count=64 << 20, nChannels=1).predictedUs == \
-        pytest.approx(36.87 + big / 8738.0, rel=1e-4)
+        pytest.approx(32.78 + 94.19 / 2 + (big - mib // 2) / 8645.7, rel=1e-4)
 
 
 def test_auto_algorithm_picks_the_one_pass_kernels():

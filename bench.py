@@ -657,14 +657,22 @@ def other_workloads(torch, V, dev, stream, hbm, only=None):
         row(name, fn, nbytes, S, factor, 10)
         if name in out:
             literal(out[name], lit * S, out[name]["us"] / 1e6)
-    # the flag protocols on the same all-reduce (32 channels, 1 MiB chunks)
+    # the flag protocols on the same three collectives (32 channels, 1 MiB chunks)
     for proto, pname in ((V.vProtoLL, "ll"), (V.vProtoLL128, "ll128")):
-        name = f"ring_allreduce_fp32_64MiB_{pname}_32ch"
-        if want(name):
-            V.vcommSetProtocol(ring, proto)
-            row(name, lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 2 * n * S, S,
-                2 * f1, 10)
-            literal(out[name], (6 * n - 4) * S, out[name]["us"] / 1e6)
+        V.vcommSetProtocol(ring, proto)
+        for name, fn, nbytes, factor, lit in (
+                (f"ring_reduce_scatter_fp32_64MiB_{pname}_32ch",
+                 lambda: V.vReduceScatter(x, part, COUNT // n, torch.float32, "sum", ring, stream), n * S + S, f1,
+                 3 * n - 1),
+                (f"ring_allgather_fp32_64MiB_{pname}_32ch",
+                 lambda: V.vAllGather(part, y, COUNT // n, torch.float32, "sum", ring, stream), S + n * S, f1,
+                 3 * n - 1),
+                (f"ring_allreduce_fp32_64MiB_{pname}_32ch",
+                 lambda: V.vAllReduce(x, y, COUNT, torch.float32, "sum", ring, stream), 2 * n * S, 2 * f1,
+                 6 * n - 4)):
+            row(name, fn, nbytes, S, factor, 10)
+            if name in out:
+                literal(out[name], lit * S, out[name]["us"] / 1e6)
     V.vcommSetProtocol(ring, V.vProtoSimple)
     # the same all-reduce with 128 KiB chunks: FIFOs small enough to stay in L2
     V.vcommSetChunkBytes(ring, 128 << 10)

@@ -336,10 +336,12 @@ __device__ __forceinline__ void slot_end(const RingArgs& a, RingCtx& c) {
 }
 
 // Units per thread whose loads are in flight together: as many as fit in the 64
-// registers of a thread of a 512-thread CTA, two of which share an SM (the 16-bit LL128
-// instances hold fewer: their packed ops need more registers).
+// registers of a thread of a 512-thread CTA, two of which share an SM (LL: two; the
+// 16-bit LL128 instances take two lines per lane group at a time in their out-of-line
+// step, whose packed ops and bounds need more registers).
 template <int PROTO, int ESZ> struct RingUnroll {
-    static constexpr int value = PROTO == vProtoLL ? 2 : PROTO == vProtoLL128 ? (ESZ == 2 ? 2 : 4) : 4;
+    static constexpr int value = PROTO == vProtoLL ? 2 : 4;
+    static constexpr int general = ESZ == 2 ? 2 : value;     // LL128's out-of-line step
 };
 
 // The general step of an LL128 slot (out of line, so the common whole-line steps keep their
@@ -604,8 +606,13 @@ __device__ __forceinline__ bool ring_slot(const RingArgs& a, RingCtx& c, const c
                             discard_l2_line(rs + (size_t)(Lb + (lane >> 2) * perIter + (lane & 3u)) * 128);
                     }
                 } else {
-                    fail |= ll128_step_general<DT, OUT, kind, R>(a, rs, ss, in, out, Lb, lines, P, epi,
-                                                                 line_seq(a, c), c.sendSeq + 1u, L0);
+                    // the general step takes RG of the step's R lines per lane group at a time
+                    constexpr int RG = RingUnroll<PROTO, ESZ>::general;
+#pragma unroll
+                    for (int h = 0; h < R; h += RG)
+                        if (Lb + h * perIter < lines)
+                            fail |= ll128_step_general<DT, OUT, kind, RG>(a, rs, ss, in, out, Lb + h * perIter, lines,
+                                                                          P, epi, line_seq(a, c), c.sendSeq + 1u, L0);
                 }
                 test_jitter(a, Lb);
             }

@@ -60,6 +60,28 @@ def test_ring_results_do_not_depend_on_timing(proto, n, channels):
         V.vcommDestroy(c)
 
 
+@pytest.mark.parametrize("proto", PROTOS, ids=["simple", "ll", "ll128"])
+def test_ring_large_slots_do_not_depend_on_timing(proto):
+    # 1 MiB chunks: 256 KiB slots, so LL128 runs its whole-line steps (four lines per lane
+    # group) and Simple its full rounds under the same random sleeps
+    n = 4
+    c = V.vcommInit(n, 1, proto)
+    try:
+        V.vcommSetAlgo(c, "ring")
+        V.vcommSetChunkBytes(c, 1 << 20)
+        V.vcommSetTimeoutMs(c, 20000)
+        V.vcommTestSetJitterNs(c, 2000)
+        for dt, op, count in ((torch.float32, "sum", 1_200_000), (torch.bfloat16, "min", 2_400_016)):
+            xs = inputs.uniform_ranks(n, count, dt, seed=11 + count)
+            recv = empty_dev(n, count, dt)
+            V.vAllReduce(to_dev(xs), recv, count, dt, op, c)
+            torch.cuda.synchronize()
+            assert V.vcommGetAsyncError(c) == V.vSuccess
+            assert_bits_equal(recv, oracle.allreduce(xs, op), f"jittered ring all-reduce, large slots, {dt}")
+    finally:
+        V.vcommDestroy(c)
+
+
 def test_jitter_hook_reaches_the_kernels():
     # sleeps of up to 200 us at every slot make the ring measurably slower (a sleep lasts
     # anywhere from 0 to about twice its request, so the check leaves wide room); the

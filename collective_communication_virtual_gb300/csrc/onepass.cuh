@@ -226,7 +226,109 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     const size_t rc = a.blockElems;
     const bool hasScale = a.hasScale != 0;
     const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, rc);
+    if constexpr (VB == 0 && ESZ == 2 && NF > 0) {
+        // 2-byte blocks off 16 bytes (a ragged block), 2 to 4 ranks: 16-byte vectors aligned
+        // to the inputs, which every rank shares when its buffer starts on a 16-byte boundary,
+        // so the loads are those of the vector path.  Warp tiles of 32 x K vectors of one block
+        // (lane l takes vectors 32 k + l), so the block arithmetic is done once a tile; the
+        // last tile of a (block, channel) range also takes the elements before the first
+        // input boundary (the head) and after the last whole vector (the tail).  The
+        // outputs sit at one offset from 16 bytes per block: a lane stores the aligned 16
+        // bytes made of its vector's last bytes and the next vector's first (a shuffle), so
+        // only the edges of a tile go element by element; outputs with an epilogue go
+        // element by element.
+        constexpr int K = 4;
+        const size_t lo = min((size_t)ch * a.chanElems, rc);
+        const size_t span = chEnd - lo;
+        const size_t tiles = span / 8 / (32 * K) + 1;
+        const bool plainOut = OUT == DT && !hasScale;
+        const unsigned int lane = threadIdx.x & 31u;
+        for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride / 32) {
+            const int r = (int)(w / tiles);
+            const size_t tl = w - (size_t)r * tiles;
+            const size_t base = (size_t)r * rc;
+            const int first = r + 1 == N ? 0 : r + 1;
+            const uintptr_t s0 = (uintptr_t)a.send[first] + (base + lo) * ESZ;
+            const size_t head = min((size_t)(((16u - (s0 & 15u)) & 15u) / ESZ), span);
+            const size_t nv = (span - head) / 8;
+            const size_t b0 = (base + lo + head) * ESZ;              // byte offset of vector 0
+            bool aligned = true;
+            for (int k = 0; k < N; k++) aligned = aligned && (((uintptr_t)a.send[k] + b0) & 15u) == 0;
+            const size_t v0 = tl * (32 * K) + lane;                   // this lane's first vector
+            if (aligned) {
+                uint4 acc[K];
+#pragma unroll
+                for (int k = 0; k < K; k++) {
+                    const size_t v = v0 + 32 * k;
+                    acc[k] = v < nv ? reduce_vec_ring<DT, OP, 16, NF>(a.send, N, first, b0 + 16 * v)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                }
+                char* out = (char*)a.recv[r] + (lo + head) * ESZ;         // vector v lands at out + 16 v
+                const unsigned int d = (unsigned int)((uintptr_t)out & 15u);
+#pragma unroll
+                for (int k = 0; k < K; k++) {
+                    const size_t v = v0 + 32 * k;
+                    const uint32_t wd[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+                    if (plainOut && d != 0) {
+                        // lane l + 1 holds vector v + 1 (lane 0 of the next k for lane 31)
+                        const uint4 src = (lane == 0 && k + 1 < K) ? acc[k + 1] : acc[k];
+                        uint4 nx;
+                        nx.x = __shfl_sync(0xFFFFFFFFu, src.x, (lane + 1) & 31u);
+                        nx.y = __shfl_sync(0xFFFFFFFFu, src.y, (lane + 1) & 31u);
+                        nx.z = __shfl_sync(0xFFFFFFFFu, src.z, (lane + 1) & 31u);
+                        nx.w = __shfl_sync(0xFFFFFFFFu, src.w, (lane + 1) & 31u);
+                        if (v < nv) {
+                            const bool nextHere = v + 1 < nv && !(lane == 31u && k == K - 1);
+                            const bool prevHere = !(lane == 0u && k == 0);     // v - 1 >= the tile's first
+                            const unsigned int split = (16u - d) / ESZ;         // elements before the boundary
+                            char* o = out + 16 * v;
+                            if (nextHere) st_stream(o + (16u - d), shift_bytes(acc[k], nx, 16u - d));
+#pragma unroll
+                            for (int e = 0; e < 8; e++)
+                                if ((e < (int)split && !prevHere) || (e >= (int)split && !nextHere))
+                                    st_elem<ESZ>(o, e, (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                        }
+                    } else if (v < nv) {
+                        if (plainOut) {
+                            st_stream(out + 16 * v, acc[k]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; e++)
+                                store_epilogue_elem<DT, OUT>(a.recv[r], lo + head + 8 * v + e,
+                                                             (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu, hasScale,
+                                                             a.scale);
+                        }
+                    }
+                }
+            } else {
+                // the ranks' blocks at different offsets from 16 bytes: element by element
+#pragma unroll
+                for (int k = 0; k < K; k++) {
+                    const size_t v = v0 + 32 * k;
+                    if (v >= nv) continue;
+                    for (int e = 0; e < 8; e++) {
+                        const size_t t = lo + head + 8 * v + e;
+                        const uint32_t x = reduce_elem_ring<DT, OP>(a.send, N, first, base + t);
+                        store_epilogue_elem<DT, OUT>(a.recv[r], t, x, hasScale, a.scale);
+                    }
+                }
+            }
+            if (tl == tiles - 1) {
+                // the head (lanes 0..7) and the tail (lanes 8..15), fewer than 8 elements each
+                const size_t tail = span - head - 8 * nv;
+                size_t t = ~(size_t)0;
+                if (lane < head) t = lo + lane;
+                else if (lane >= 8u && lane - 8u < tail) t = lo + head + 8 * nv + (lane - 8u);
+                if (t != ~(size_t)0) {
+                    const uint32_t x = reduce_elem_ring<DT, OP>(a.send, N, first, base + t);
+                    store_epilogue_elem<DT, OUT>(a.recv[r], t, x, hasScale, a.scale);
+                }
+            }
+        }
+        return;
+    }
     if constexpr (VB == 0 && ESZ == 2) {
+        // (the run-time rank count: one vector per thread)
         // 2-byte blocks off 16 bytes (a ragged block): 16-byte vectors aligned to the
         // inputs, which every rank shares when its buffer starts on a 16-byte boundary, so
         // the loads are those of the vector path; the 8 results are stored one by one (the
@@ -353,7 +455,8 @@ template <int DT, int OP, int OUT, int NF>
 static cudaError_t rs_launch_vec(const OnePassArgs& a, int vb, int grid, int threads, cudaStream_t s) {
     if (vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32, NF>, grid, threads, 0, s, a);
     else if (vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16, NF>, grid, threads, 0, s, a);
-    else if constexpr (NF == 0) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0>, grid, threads, 0, s, a);
+    else if constexpr (NF == 0 || (DTypeOf<DT>::size == 2 && NF <= 4))
+        (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0, NF>, grid, threads, 0, s, a);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

@@ -237,7 +237,7 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
         // bytes made of its vector's last bytes and the next vector's first (a shuffle), so
         // only the edges of a tile go element by element; outputs with an epilogue go
         // element by element.
-        constexpr int K = 4;
+        constexpr int K = NF <= 4 ? 4 : 1;
         const size_t lo = min((size_t)ch * a.chanElems, rc);
         const size_t span = chEnd - lo;
         const size_t tiles = span / 8 / (32 * K) + 1;
@@ -455,7 +455,7 @@ template <int DT, int OP, int OUT, int NF>
 static cudaError_t rs_launch_vec(const OnePassArgs& a, int vb, int grid, int threads, cudaStream_t s) {
     if (vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32, NF>, grid, threads, 0, s, a);
     else if (vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16, NF>, grid, threads, 0, s, a);
-    else if constexpr (NF == 0 || (DTypeOf<DT>::size == 2 && NF <= 4))
+    else if constexpr (NF == 0 || DTypeOf<DT>::size == 2)
         (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0, NF>, grid, threads, 0, s, a);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();

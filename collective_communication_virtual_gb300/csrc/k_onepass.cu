@@ -16,12 +16,10 @@ cudaError_t launch_allreduce_onepass(const OnePassArgs& a, vDataType_t dt, vRedO
 cudaError_t launch_reduce_scatter_onepass(const OnePassArgs& a, vDataType_t dt, vRedOp_t op,
                                           vDataType_t outType, int vb, int grid, int threads,
                                           cudaStream_t s) {
-    const bool twoByte = dt == vFloat16 || dt == vBFloat16;
-    if (a.nRanks == 8 && (vb != 0 || twoByte)) return rs_launch<8>(a, dt, op, outType, vb, grid, threads, s);
-    // 2 to 4 ranks: the vector paths, and the 2-byte element path (two vectors that follow
-    // the inputs per thread)
-    const bool small = a.nRanks >= 2 && a.nRanks <= 4;
-    if (small && (vb != 0 || twoByte))
+    // 2 to 4 and 8 ranks: compile-time instances of the vector paths and of the element
+    // path (warp tiles of vectors that follow the inputs)
+    if (a.nRanks == 8) return rs_launch<8>(a, dt, op, outType, vb, grid, threads, s);
+    if (a.nRanks >= 2 && a.nRanks <= 4)
         return launch_reduce_scatter_onepass_small(a, dt, op, outType, vb, grid, threads, s);
     return rs_launch<0>(a, dt, op, outType, vb, grid, threads, s);
 }

@@ -21,6 +21,12 @@
 
 namespace vc {
 
+// Element e of a 16-byte vector held as four 32-bit words (2- or 4-byte elements).
+template <int ESZ>
+__device__ __forceinline__ uint32_t vec_elem(const uint32_t (&w)[4], int e) {
+    return ESZ == 4 ? w[e] : (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+}
+
 // Per channel the work is (block, unit) pairs, flattened so that small buffers still
 // spread over all threads: unit i of block b covers elements [lo_b + i*U, lo_b + (i+1)*U)
 // with U = 16 / esz on the vector path (1 otherwise) and lo_b = b*B + ch*Lc.  Only the
@@ -226,8 +232,8 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
     const size_t rc = a.blockElems;
     const bool hasScale = a.hasScale != 0;
     const size_t chEnd = min((size_t)(ch + 1) * a.chanElems, rc);
-    if constexpr (VB == 0 && ESZ == 2 && NF > 0) {
-        // 2-byte blocks off 16 bytes (a ragged block), 2 to 4 ranks: 16-byte vectors aligned
+    if constexpr (VB == 0 && NF > 0 && (ESZ == 2 || NF <= 4)) {
+        // Blocks off 16 bytes (a ragged block), 2 to 4 ranks (and 8 of 2-byte elements): 16-byte vectors aligned
         // to the inputs, which every rank shares when its buffer starts on a 16-byte boundary,
         // so the loads are those of the vector path.  Warp tiles of 32 x K vectors of one block
         // (lane l takes vectors 32 k + l), so the block arithmetic is done once a tile; the
@@ -238,9 +244,10 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
         // only the edges of a tile go element by element; outputs with an epilogue go
         // element by element.
         constexpr int K = NF <= 4 ? 4 : 1;
+        constexpr int VE = 16 / ESZ;                                 // elements per vector
         const size_t lo = min((size_t)ch * a.chanElems, rc);
         const size_t span = chEnd - lo;
-        const size_t tiles = span / 8 / (32 * K) + 1;
+        const size_t tiles = span / VE / (32 * K) + 1;
         const bool plainOut = OUT == DT && !hasScale;
         const unsigned int lane = threadIdx.x & 31u;
         for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride / 32) {
@@ -250,7 +257,7 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
             const int first = r + 1 == N ? 0 : r + 1;
             const uintptr_t s0 = (uintptr_t)a.send[first] + (base + lo) * ESZ;
             const size_t head = min((size_t)(((16u - (s0 & 15u)) & 15u) / ESZ), span);
-            const size_t nv = (span - head) / 8;
+            const size_t nv = (span - head) / VE;
             const size_t b0 = (base + lo + head) * ESZ;              // byte offset of vector 0
             bool aligned = true;
             for (int k = 0; k < N; k++) aligned = aligned && (((uintptr_t)a.send[k] + b0) & 15u) == 0;
@@ -284,19 +291,18 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
                             char* o = out + 16 * v;
                             if (nextHere) st_stream(o + (16u - d), shift_bytes(acc[k], nx, 16u - d));
 #pragma unroll
-                            for (int e = 0; e < 8; e++)
+                            for (int e = 0; e < VE; e++)
                                 if ((e < (int)split && !prevHere) || (e >= (int)split && !nextHere))
-                                    st_elem<ESZ>(o, e, (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                                    st_elem<ESZ>(o, e, vec_elem<ESZ>(wd, e));
                         }
                     } else if (v < nv) {
                         if (plainOut) {
                             st_stream(out + 16 * v, acc[k]);
                         } else {
 #pragma unroll
-                            for (int e = 0; e < 8; e++)
-                                store_epilogue_elem<DT, OUT>(a.recv[r], lo + head + 8 * v + e,
-                                                             (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu, hasScale,
-                                                             a.scale);
+                            for (int e = 0; e < VE; e++)
+                                store_epilogue_elem<DT, OUT>(a.recv[r], lo + head + VE * v + e, vec_elem<ESZ>(wd, e),
+                                                             hasScale, a.scale);
                         }
                     }
                 }
@@ -306,19 +312,19 @@ k_reduce_scatter_onepass(const __grid_constant__ OnePassArgs a) {
                 for (int k = 0; k < K; k++) {
                     const size_t v = v0 + 32 * k;
                     if (v >= nv) continue;
-                    for (int e = 0; e < 8; e++) {
-                        const size_t t = lo + head + 8 * v + e;
+                    for (int e = 0; e < VE; e++) {
+                        const size_t t = lo + head + VE * v + e;
                         const uint32_t x = reduce_elem_ring<DT, OP>(a.send, N, first, base + t);
                         store_epilogue_elem<DT, OUT>(a.recv[r], t, x, hasScale, a.scale);
                     }
                 }
             }
             if (tl == tiles - 1) {
-                // the head (lanes 0..7) and the tail (lanes 8..15), fewer than 8 elements each
-                const size_t tail = span - head - 8 * nv;
+                // the head (lanes 0..7) and the tail (lanes 8..15), fewer than VE elements each
+                const size_t tail = span - head - VE * nv;
                 size_t t = ~(size_t)0;
                 if (lane < head) t = lo + lane;
-                else if (lane >= 8u && lane - 8u < tail) t = lo + head + 8 * nv + (lane - 8u);
+                else if (lane >= 8u && lane - 8u < tail) t = lo + head + VE * nv + (lane - 8u);
                 if (t != ~(size_t)0) {
                     const uint32_t x = reduce_elem_ring<DT, OP>(a.send, N, first, base + t);
                     store_epilogue_elem<DT, OUT>(a.recv[r], t, x, hasScale, a.scale);
@@ -455,9 +461,7 @@ template <int DT, int OP, int OUT, int NF>
 static cudaError_t rs_launch_vec(const OnePassArgs& a, int vb, int grid, int threads, cudaStream_t s) {
     if (vb == 32) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 32, NF>, grid, threads, 0, s, a);
     else if (vb == 16) (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 16, NF>, grid, threads, 0, s, a);
-    else if constexpr (NF == 0 || DTypeOf<DT>::size == 2)
-        (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0, NF>, grid, threads, 0, s, a);
-    else return cudaErrorInvalidValue;
+    else (void)pdl_launch(k_reduce_scatter_onepass<DT, OP, OUT, 0, NF>, grid, threads, 0, s, a);
     return cudaGetLastError();
 }
 

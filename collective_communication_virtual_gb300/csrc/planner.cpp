@@ -261,11 +261,12 @@ extern "C" vResult_t vPlanCompute(const vPlanRequest_t* q, vPlanInfo_t* p) {
             if (q->coll == vCollAllReduce || q->coll == vCollReduceScatter || q->coll == vCollReduce) {
                 // a thread's unit: one vector of every rank, or on the element path 8
                 // elements of every rank (32 of a warp's lanes times 8 per warp tile)
-                // (the 2-byte reduce-scatter element path takes 4 vectors of 8 elements per
-                // thread with 2 to 4 ranks)
-                const size_t per16 = (!p->vecBytes && esz == 2 && q->coll == vCollReduceScatter && N >= 2 &&
-                                      N <= 4) ? 4 : 1;
-                const size_t unit = p->vecBytes ? p->vecBytes / esz : (size_t)vc::kElemsPerThread * per16;
+                // (the reduce-scatter element path of 2 to 4 ranks takes 4 16-byte vectors per
+                // thread, of 8 ranks and 2-byte elements 1)
+                const bool tiled = !p->vecBytes && q->coll == vCollReduceScatter &&
+                                   ((N >= 2 && N <= 4) || (N == 8 && esz == 2));
+                const size_t unit = p->vecBytes ? p->vecBytes / esz
+                                                : tiled ? (16 / esz) * (N == 8 ? 1 : 4) : (size_t)vc::kElemsPerThread;
                 const size_t units = div_up(chElems, unit) * (size_t)N;
                 // Small work: smaller CTAs (down to 64 threads) spread it over more SMs
                 // instead of loading a few SMs with 512 threads each.

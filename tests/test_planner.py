@@ -234,10 +234,19 @@ def test_element_path_threads_take_8_elements_of_every_rank():
     p = plan(count=1 << 20, aligned16=0)                       # B = 131,072
     assert p.vecBytes == 0 and p.threadsPerCta == 256
     assert p.gridCtas == (131_072 // 8) * 8 // 256
-    # a ragged reduce-scatter block of 1,048,577 elements: 131,073 threads per block
+    # a ragged reduce-scatter block of 1,048,577 fp32 elements, 8 ranks: 131,073 threads per
+    # block; of bf16, warp tiles of 16-byte vectors, one per thread: 131,073 as well
     p = plan(coll=V.vCollReduceScatter, count=(1 << 20) + 1)
     assert p.vecBytes == 0 and p.threadsPerCta == 128
     assert p.gridCtas == -(-131_073 * 8 // 128)
+    p = plan(coll=V.vCollReduceScatter, count=(1 << 20) + 1, datatype=V.vBFloat16)
+    assert p.gridCtas == -(-131_073 * 8 // 128)
+    # 3 ranks: four vectors per thread, 1,536 CTAs of work, under two waves of 1,216, so
+    # one wave strides over it; 6 ranks keep the 8-element warp tiles
+    p = plan(coll=V.vCollReduceScatter, nRanks=3, count=(1 << 20) + 1)
+    assert p.gridCtas == 2 * 152 * (512 // 128)
+    p = plan(coll=V.vCollReduceScatter, nRanks=6, count=(1 << 20) + 1)
+    assert p.gridCtas == -(-131_073 * 6 // 128)
 
 
 def test_copy_threads_follow_how_often_a_loaded_byte_is_stored():

@@ -209,6 +209,30 @@ def test_reduce_scatter_unaligned_and_inplace(comms, variant):
     assert_bits_equal(run_rs(comms, xs, "max", algo, proto, 4099), oracle.reduce_scatter(xs, "max"), "odd")
 
 
+@pytest.mark.parametrize("n", [2, 3, 4, 8])
+@pytest.mark.parametrize("dtype", DTYPES, ids=dname)
+def test_reduce_scatter_ragged_warp_tiles(comms, n, dtype):
+    # Ragged blocks (rc * esz not a multiple of 16) of several warp tiles: the one-pass
+    # path reduces 16-byte vectors that follow the inputs, tile by tile, and realigns the
+    # stores to the outputs through shuffles; the head and tail elements, the tile edges
+    # (lane 31, the last vector of a tile) and a channel split all land on these sizes.
+    esz = torch.empty((), dtype=dtype).element_size()
+    for rc, channels in ((5 * 32 * 4 * (16 // esz) + 3, 1), (3 * 32 * 4 * (16 // esz) + 1, 2)):
+        assert (rc * esz) % 16 != 0
+        xs = _inputs(n, n * rc, dtype, seed=97 * n + rc)
+        for op in ("sum", "max"):
+            got = run_rs(comms, xs, op, "onepass", V.vProtoSimple, rc, channels=channels)
+            assert_bits_equal(got, oracle.reduce_scatter(xs, op), f"ragged rs n={n} rc={rc} {op}")
+        if dtype in (torch.float16, torch.bfloat16):
+            got = run_rs(comms, xs, "sum", "onepass", V.vProtoSimple, rc, out_dtype=torch.float32,
+                         scale=1.0 / n, channels=channels)
+            assert_bits_equal(got, oracle.reduce_scatter_scale(xs, "sum", 1.0 / n, torch.float32),
+                              f"ragged rs scale/cast n={n} rc={rc}")
+        # send and receive buffers one element off 16 bytes: other head and output offsets
+        got = run_rs(comms, xs, "sum", "onepass", V.vProtoSimple, rc, pad=1, channels=channels)
+        assert_bits_equal(got, oracle.reduce_scatter(xs, "sum"), f"ragged rs padded n={n} rc={rc}")
+
+
 # ---------------------------------------------------------------------------------------
 # All-gather, broadcast
 # ---------------------------------------------------------------------------------------

@@ -158,6 +158,125 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
     return t;
 }
 
+// One warp tile of a 2-byte copy off 16 bytes (a ragged block): span elements from src to
+// dst[r] + dstOff for r < ndst.  After the head elements that bring src to a 16-byte
+// boundary, lane l takes the source vectors 32 k + l of tile tl (K per lane), each loaded
+// once, aligned; the destinations share one offset d from 16 bytes, so a lane stores the
+// aligned 16 bytes made of its vector's last d bytes and the next vector's first 16 - d
+// (a shuffle), and only the edges of a tile go element by element.  The block's last tile
+// also copies the head and the tail (lanes 0..7 and 8..15).  Destinations at different
+// offsets go element by element.  All lanes of the warp call it with the same tile.
+template <int K>
+__device__ __forceinline__ void ragged16_tile(const char* src, char* const* dst, int ndst, size_t dstOff,
+                                              size_t span, size_t tl, size_t tiles) {
+    constexpr int ESZ = 2, VE = 8;
+    const unsigned int lane = threadIdx.x & 31u;
+    const size_t hs = min((size_t)(((16u - ((uintptr_t)src & 15u)) & 15u) / ESZ), span);
+    const size_t nv = (span - hs) / VE;
+    const char* sv = src + hs * ESZ;                           // 16-byte aligned
+    const size_t o0 = dstOff + hs * ESZ;                       // vector v lands at dst[r] + o0 + 16 v
+    const unsigned int d = (unsigned int)(((uintptr_t)dst[0] + o0) & 15u);
+    bool same = true;
+    for (int r = 1; r < ndst; r++) same = same && ((((uintptr_t)dst[r] + o0) & 15u) == d);
+    const size_t v0 = tl * (32 * K) + lane;
+    if (same) {
+        uint4 x[K];
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            const size_t v = v0 + 32 * k;
+            x[k] = v < nv ? ld_stream(sv + 16 * v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            const size_t v = v0 + 32 * k;
+            if (d == 0) {
+                if (v < nv)
+                    for (int r = 0; r < ndst; r++) st_stream(dst[r] + o0 + 16 * v, x[k]);
+                continue;
+            }
+            const uint4 give = (lane == 0u && k + 1 < K) ? x[k + 1] : x[k];
+            uint4 nx;
+            nx.x = __shfl_sync(0xFFFFFFFFu, give.x, (lane + 1) & 31u);
+            nx.y = __shfl_sync(0xFFFFFFFFu, give.y, (lane + 1) & 31u);
+            nx.z = __shfl_sync(0xFFFFFFFFu, give.z, (lane + 1) & 31u);
+            nx.w = __shfl_sync(0xFFFFFFFFu, give.w, (lane + 1) & 31u);
+            if (v >= nv) continue;
+            const bool nextHere = v + 1 < nv && !(lane == 31u && k == K - 1);
+            const bool prevHere = !(lane == 0u && k == 0);
+            const unsigned int split = (16u - d) / ESZ;        // elements before the boundary
+            const uint4 y = shift_bytes(x[k], nx, 16u - d);
+            const uint32_t wd[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
+            for (int r = 0; r < ndst; r++) {
+                char* o = dst[r] + o0 + 16 * v;
+                if (nextHere) st_stream(o + (16u - d), y);
+#pragma unroll
+                for (int e = 0; e < VE; e++)
+                    if ((e < (int)split && !prevHere) || (e >= (int)split && !nextHere))
+                        st_elem<ESZ>(o, e, (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            const size_t v = v0 + 32 * k;
+            if (v >= nv) continue;
+            for (int e = 0; e < VE; e++) {
+                const uint32_t x = ld_elem<ESZ>(sv, VE * v + e);
+                for (int r = 0; r < ndst; r++) st_elem<ESZ>(dst[r] + o0, VE * v + e, x);
+            }
+        }
+    }
+    if (tl == tiles - 1) {
+        size_t e = ~(size_t)0;
+        if (lane < hs) e = lane;
+        else if (lane >= 8u && lane - 8u < span - hs - VE * nv) e = hs + VE * nv + (lane - 8u);
+        if (e != ~(size_t)0) {
+            const uint32_t x = ld_elem<ESZ>(src, e);
+            for (int r = 0; r < ndst; r++) st_elem<ESZ>(dst[r] + dstOff, e, x);
+        }
+    }
+}
+
+// The ragged 2-byte all-gather and all-to-all on warp tiles of 32 x 2 vectors: two
+// 512-thread CTAs per SM, 64 registers.
+constexpr int kRaggedK = 2;
+
+__global__ void __launch_bounds__(kOnePassThreads, 2) k_allgather_ragged16(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t sc = a.count;
+    const size_t lo = min((size_t)ch * a.chanElems, sc);
+    const size_t span = min((size_t)(ch + 1) * a.chanElems, sc) - lo;
+    const size_t tiles = span / 8 / (32 * kRaggedK) + 1;
+    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x / 32;
+    for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride) {
+        const int s = (int)(w / tiles);
+        ragged16_tile<kRaggedK>((const char*)a.send[s] + lo * 2, (char* const*)a.recv, N, ((size_t)s * sc + lo) * 2,
+                                span, w - (size_t)s * tiles, tiles);
+    }
+}
+
+__global__ void __launch_bounds__(kOnePassThreads, 2) k_alltoall_ragged16(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t c = a.count;
+    const size_t lo = min((size_t)ch * a.chanElems, c);
+    const size_t span = min((size_t)(ch + 1) * a.chanElems, c) - lo;
+    const size_t tiles = span / 8 / (32 * kRaggedK) + 1;
+    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x / 32;
+    for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N * N; w += stride) {
+        const size_t p = w / tiles;                          // block p = i * N + j: send[i] -> recv[j]
+        const int i = (int)(p / N), j = (int)(p - (size_t)i * N);
+        char* dst = (char*)a.recv[j];
+        ragged16_tile<kRaggedK>((const char*)a.send[i] + ((size_t)j * c + lo) * 2, &dst, 1, ((size_t)i * c + lo) * 2,
+                                span, w - p * tiles, tiles);
+    }
+}
+
 // All-gather: block s = send[s] lands at recv[r] + s*sc for every r.  a.count = sc.
 // Gather (a.outRoot = root) writes recv[root] only.
 template <int ESZ, int VB>
@@ -168,6 +287,7 @@ k_allgather_onepass(const __grid_constant__ OnePassArgs a) {
     const int ch = blockIdx.x / a.ctasPerChannel;
     const int cta = blockIdx.x - ch * a.ctasPerChannel;
     const size_t sc = a.count;
+
     const TileSpan sp = tile_span<ESZ>(a, ch, sc);
     const size_t nTiles = sp.tilesPerBlock * (size_t)N;
     char* const* dsts = a.outRoot >= 0 ? (char* const*)&a.recv[a.outRoot] : (char* const*)a.recv;
@@ -317,6 +437,10 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
 
 cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s) {
+    if (elemSize == 2 && vb == 0 && a.outRoot < 0) {
+        (void)pdl_launch(k_allgather_ragged16, grid, threads, 0, s, a);
+        return cudaGetLastError();
+    }
     VC_COPY_LAUNCH(k_allgather_onepass);
 }
 
@@ -327,6 +451,10 @@ cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb,
 
 cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                     int threads, cudaStream_t s) {
+    if (elemSize == 2 && vb == 0) {
+        (void)pdl_launch(k_alltoall_ragged16, grid, threads, 0, s, a);
+        return cudaGetLastError();
+    }
     VC_COPY_LAUNCH(k_alltoall_onepass);
 }
 

@@ -1,7 +1,8 @@
 // k_copy.cu -- data-movement collectives: all-gather, broadcast, all-to-all (uniform and
 // variable).  They move bytes whatever the data type (NCCL book chapter 6: AllGather and
 // Broadcast are issued as ncclInt8), so each kernel is instantiated once per element
-// size and once for the 16-byte vector path.
+// size and once for the 16-byte vector path; 2-byte blocks off 16 bytes have all-gather
+// and all-to-all kernels of their own (k_allgather_ragged16, k_alltoall_ragged16).
 //
 // All-gather and broadcast read each source vector once and write it to all N receive
 // buffers: (N+1)*S bytes, the minimum.  All-to-all copies each of the N*N blocks once.

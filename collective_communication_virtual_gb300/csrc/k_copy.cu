@@ -1,8 +1,8 @@
 // k_copy.cu -- data-movement collectives: all-gather, broadcast, all-to-all (uniform and
 // variable).  They move bytes whatever the data type (NCCL book chapter 6: AllGather and
 // Broadcast are issued as ncclInt8), so each kernel is instantiated once per element
-// size and once for the 16-byte vector path; 2-byte blocks off 16 bytes have all-gather
-// and all-to-all kernels of their own (k_allgather_ragged16, k_alltoall_ragged16).
+// size and once for the 16-byte vector path; 2-byte copies off 16 bytes have kernels of
+// their own (k_*_ragged16).
 //
 // All-gather and broadcast read each source vector once and write it to all N receive
 // buffers: (N+1)*S bytes, the minimum.  All-to-all copies each of the N*N blocks once.
@@ -238,8 +238,8 @@ __device__ __forceinline__ void ragged16_tile(const char* src, char* const* dst,
     }
 }
 
-// The ragged 2-byte all-gather and all-to-all on warp tiles of 32 x 2 vectors: two
-// 512-thread CTAs per SM, 64 registers.
+// The ragged 2-byte copies on warp tiles of 32 x 2 vectors: two 512-thread CTAs per SM,
+// 64 registers.
 constexpr int kRaggedK = 2;
 
 __global__ void __launch_bounds__(kOnePassThreads, 2) k_allgather_ragged16(const __grid_constant__ OnePassArgs a) {
@@ -252,10 +252,46 @@ __global__ void __launch_bounds__(kOnePassThreads, 2) k_allgather_ragged16(const
     const size_t span = min((size_t)(ch + 1) * a.chanElems, sc) - lo;
     const size_t tiles = span / 8 / (32 * kRaggedK) + 1;
     const size_t stride = (size_t)a.ctasPerChannel * blockDim.x / 32;
+    // gather (a.outRoot = root) writes recv[root] only
+    char* const* dsts = a.outRoot >= 0 ? (char* const*)&a.recv[a.outRoot] : (char* const*)a.recv;
+    const int nd = a.outRoot >= 0 ? 1 : N;
     for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride) {
         const int s = (int)(w / tiles);
-        ragged16_tile<kRaggedK>((const char*)a.send[s] + lo * 2, (char* const*)a.recv, N, ((size_t)s * sc + lo) * 2,
-                                span, w - (size_t)s * tiles, tiles);
+        ragged16_tile<kRaggedK>((const char*)a.send[s] + lo * 2, dsts, nd, ((size_t)s * sc + lo) * 2, span,
+                                w - (size_t)s * tiles, tiles);
+    }
+}
+
+// Broadcast: the root's block to every receiver.
+__global__ void __launch_bounds__(kOnePassThreads, 2) k_broadcast_ragged16(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t lo = min((size_t)ch * a.chanElems, a.count);
+    const size_t span = min((size_t)(ch + 1) * a.chanElems, a.count) - lo;
+    const size_t tiles = span / 8 / (32 * kRaggedK) + 1;
+    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x / 32;
+    for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles; w += stride)
+        ragged16_tile<kRaggedK>((const char*)a.send[a.root] + lo * 2, (char* const*)a.recv, a.nRanks, lo * 2, span, w,
+                                tiles);
+}
+
+// Scatter: block j of the root's buffer to recv[j].
+__global__ void __launch_bounds__(kOnePassThreads, 2) k_scatter_ragged16(const __grid_constant__ OnePassArgs a) {
+    pdl_begin();
+    const int N = a.nRanks;
+    const int ch = blockIdx.x / a.ctasPerChannel;
+    const int cta = blockIdx.x - ch * a.ctasPerChannel;
+    const size_t c = a.count;
+    const size_t lo = min((size_t)ch * a.chanElems, c);
+    const size_t span = min((size_t)(ch + 1) * a.chanElems, c) - lo;
+    const size_t tiles = span / 8 / (32 * kRaggedK) + 1;
+    const size_t stride = (size_t)a.ctasPerChannel * blockDim.x / 32;
+    for (size_t w = ((size_t)cta * blockDim.x + threadIdx.x) / 32; w < tiles * (size_t)N; w += stride) {
+        const int j = (int)(w / tiles);
+        char* dst = (char*)a.recv[j];
+        ragged16_tile<kRaggedK>((const char*)a.send[a.root] + ((size_t)j * c + lo) * 2, &dst, 1, lo * 2, span,
+                                w - (size_t)j * tiles, tiles);
     }
 }
 
@@ -438,7 +474,7 @@ k_alltoallv(const __grid_constant__ A2AvArgs a) {
 
 cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s) {
-    if (elemSize == 2 && vb == 0 && a.outRoot < 0) {
+    if (elemSize == 2 && vb == 0) {
         (void)pdl_launch(k_allgather_ragged16, grid, threads, 0, s, a);
         return cudaGetLastError();
     }
@@ -447,6 +483,10 @@ cudaError_t launch_allgather_onepass(const OnePassArgs& a, int elemSize, int vb,
 
 cudaError_t launch_broadcast_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                      int threads, cudaStream_t s) {
+    if (elemSize == 2 && vb == 0) {
+        (void)pdl_launch(k_broadcast_ragged16, grid, threads, 0, s, a);
+        return cudaGetLastError();
+    }
     VC_COPY_LAUNCH(k_broadcast_onepass);
 }
 
@@ -461,6 +501,10 @@ cudaError_t launch_alltoall_onepass(const OnePassArgs& a, int elemSize, int vb, 
 
 cudaError_t launch_scatter_onepass(const OnePassArgs& a, int elemSize, int vb, int grid,
                                    int threads, cudaStream_t s) {
+    if (elemSize == 2 && vb == 0) {
+        (void)pdl_launch(k_scatter_ragged16, grid, threads, 0, s, a);
+        return cudaGetLastError();
+    }
     VC_COPY_LAUNCH(k_scatter_onepass);
 }
 

@@ -598,6 +598,18 @@ def other_workloads(torch, V, dev, stream, hbm, only=None):
         V.vcommDestroy(c3)
         del xs, ys
         torch.cuda.empty_cache()
+    # a ragged all-to-all: 3 ranks of 64 MiB bf16, blocks of 11,184,810 elements
+    if want("alltoall_bf16_3x64MiB_ragged"):
+        n3, rc3 = 3, (32 << 20) // 3
+        c3 = V.vcommInit(n3, 1, V.vProtoSimple)
+        V.vcommSetAlgo(c3, "onepass")
+        xs = [x.to(dev) for x in inputs.uniform_ranks(n3, n3 * rc3, torch.bfloat16, 10)]
+        ys = [torch.empty(n3 * rc3, dtype=torch.bfloat16, device=dev) for _ in range(n3)]
+        t = tm(lambda: V.vAllToAll(xs, ys, rc3, torch.bfloat16, "sum", c3, stream))
+        rec("alltoall_bf16_3x64MiB_ragged", t, 2 * n3 * n3 * rc3 * 2, n3 * rc3 * 2, (n3 - 1) / n3)
+        V.vcommDestroy(c3)
+        del xs, ys
+        torch.cuda.empty_cache()
     # uniform all-to-all at 1 GiB per rank
     if want("alltoall_fp32_1GiB", "ring_allreduce_fp32_1GiB_simple_32ch"):
         cnt = 1 << 28

@@ -164,7 +164,8 @@ __device__ __forceinline__ TileSpan tile_span(const OnePassArgs& a, int ch, size
 // boundary, lane l takes the source vectors 32 k + l of tile tl (K per lane), each loaded
 // once, aligned; the destinations share one offset d from 16 bytes, so a lane stores the
 // aligned 16 bytes made of its vector's last d bytes and the next vector's first 16 - d
-// (a shuffle), and only the edges of a tile go element by element.  The block's last tile
+// (a shuffle; the tile's last lane loads the next tile's first vector itself), and only
+// the block's first and last vectors go element by element.  The block's last tile
 // also copies the head and the tail (lanes 0..7 and 8..15).  Destinations at different
 // offsets go element by element.  All lanes of the warp call it with the same tile.
 template <int K>
@@ -187,6 +188,11 @@ __device__ __forceinline__ void ragged16_tile(const char* src, char* const* dst,
             const size_t v = v0 + 32 * k;
             x[k] = v < nv ? ld_stream(sv + 16 * v) : make_uint4(0u, 0u, 0u, 0u);
         }
+        // the tile's last lane also loads the next tile's first vector, so that only the
+        // block's first and last vectors go element by element
+        const size_t vLast = v0 + 32 * (K - 1);
+        const uint4 after = (lane == 31u && d != 0 && vLast + 1 < nv) ? ld_stream(sv + 16 * (vLast + 1))
+                                                                       : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int k = 0; k < K; k++) {
             const size_t v = v0 + 32 * k;
@@ -201,19 +207,22 @@ __device__ __forceinline__ void ragged16_tile(const char* src, char* const* dst,
             nx.y = __shfl_sync(0xFFFFFFFFu, give.y, (lane + 1) & 31u);
             nx.z = __shfl_sync(0xFFFFFFFFu, give.z, (lane + 1) & 31u);
             nx.w = __shfl_sync(0xFFFFFFFFu, give.w, (lane + 1) & 31u);
+            if (lane == 31u && k == K - 1) nx = after;
             if (v >= nv) continue;
-            const bool nextHere = v + 1 < nv && !(lane == 31u && k == K - 1);
-            const bool prevHere = !(lane == 0u && k == 0);
+            const bool nextHere = v + 1 < nv;
+            const bool prevHere = v > 0;
             const unsigned int split = (16u - d) / ESZ;        // elements before the boundary
             const uint4 y = shift_bytes(x[k], nx, 16u - d);
-            const uint32_t wd[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
             for (int r = 0; r < ndst; r++) {
                 char* o = dst[r] + o0 + 16 * v;
                 if (nextHere) st_stream(o + (16u - d), y);
+                if (!prevHere || !nextHere) {                  // the block's first or last vector
+                    const uint32_t wd[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
 #pragma unroll
-                for (int e = 0; e < VE; e++)
-                    if ((e < (int)split && !prevHere) || (e >= (int)split && !nextHere))
-                        st_elem<ESZ>(o, e, (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                    for (int e = 0; e < VE; e++)
+                        if ((e < (int)split && !prevHere) || (e >= (int)split && !nextHere))
+                            st_elem<ESZ>(o, e, (wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+                }
             }
         }
     } else {

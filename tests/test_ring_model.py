@@ -89,3 +89,20 @@ def test_model_scales_with_rank_and_channel_counts(coll):
     assert p16 > small8
     big = [_plan(coll, V.vProtoSimple, ch, 1 << 30).predictedUs for ch in (1, 4, 8, 16, 32, 64)]
     assert all(b >= c for b, c in zip(big, big[1:])), big
+
+
+def test_calibration_recovers_known_curves():
+    # the fit on curves drawn from the model's own forms, at the sweep's sizes, gives their
+    # parameters back: ring steps (two slopes around a knee) and the broadcast chain
+    from collective_communication_virtual_gb300 import calibrate
+    xs = [1024 * 4 ** k for k in range(11)]
+    lat, f_mib, knee, rate = 30.0, 40.0, float(1 << 20), 150_000.0
+    m = [lat + f_mib / (1 << 20) * min(x, knee) + max(0.0, x - knee) / rate for x in xs]
+    got = calibrate.fit_curve("allreduce", xs, m)
+    assert got[0] == pytest.approx(lat, rel=1e-6) and got[1] == pytest.approx(rate, rel=1e-6)
+    assert got[2] == knee and got[3] == pytest.approx(f_mib, rel=1e-6)
+    c = 0.02
+    m = [lat + c * x ** 0.5 + x / rate for x in xs]
+    got = calibrate.fit_curve("broadcast", xs, m)
+    assert got[0] == pytest.approx(lat, rel=1e-6) and got[1] == pytest.approx(rate, rel=1e-6)
+    assert got[2] == pytest.approx(c, rel=1e-6) and got[3] == 0.0
